@@ -1,0 +1,265 @@
+"""CPU oracle for the UltraQuant 4-bit KV cache (test infrastructure).
+
+Only tests/, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline and
+reference legs may import this package.  The product library never calls it and
+shares no code with it; see uq_oracle.c for the step-by-step restatement of the
+pages and the readings taken where they are silent.
+
+All arrays are numpy.  bf16 tensors are passed as uint16 bit patterns.
+"""
+import ctypes as C
+
+import numpy as np
+
+from .build import build as _build
+
+_lib = C.CDLL(_build())
+
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+
+_lib.uqo_splitmix64.restype = C.c_uint64
+_lib.uqo_splitmix64.argtypes = [C.c_uint64, C.c_uint64]
+_lib.uqo_signs.argtypes = [C.c_uint64, C.c_int, _i8p]
+_lib.uqo_inv_sqrt_d.restype = C.c_float
+_lib.uqo_inv_sqrt_d.argtypes = [C.c_int]
+_lib.uqo_rotate_fp32.argtypes = [_f32p, C.c_int, _i8p, _f32p]
+_lib.uqo_inverse_rotate_f64.argtypes = [_f64p, C.c_int, _i8p, _f64p]
+_lib.uqo_pow2_exponent.restype = C.c_int
+_lib.uqo_pow2_exponent.argtypes = [C.c_double, C.c_int]
+_lib.uqo_scale_byte.restype = C.c_int
+_lib.uqo_scale_byte.argtypes = [C.c_float, C.c_float, C.c_int]
+_lib.uqo_e2m1_code.restype = C.c_int
+_lib.uqo_e2m1_code.argtypes = [C.c_double]
+_lib.uqo_e2m1_value.restype = C.c_double
+_lib.uqo_e2m1_value.argtypes = [C.c_int]
+_lib.uqo_fp4_value.restype = C.c_double
+_lib.uqo_fp4_value.argtypes = [C.c_int, C.c_int]
+_lib.uqo_quantize_rotated.argtypes = [_f32p, C.c_int64, C.c_int, C.c_float, C.c_int, _u8p, _u8p]
+_lib.uqo_c_constant.restype = C.c_float
+_lib.uqo_quantize_vectors.argtypes = [C.c_void_p, C.c_int, C.c_int64, C.c_int, C.c_uint64, _u8p, _u8p]
+_lib.uqo_f32_to_bf16.restype = C.c_uint16
+_lib.uqo_f32_to_bf16.argtypes = [C.c_float]
+_lib.uqo_e4m3_value.restype = C.c_double
+_lib.uqo_e4m3_value.argtypes = [C.c_int]
+_lib.uqo_e4m3_code.restype = C.c_int
+_lib.uqo_e4m3_code.argtypes = [C.c_float]
+_lib.uqo_query_fp8.argtypes = [_u16p, C.c_int, C.c_uint64, _u8p]
+_lib.uqo_append_fp4.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
+                                C.c_int, C.c_uint64, _u8p, _u8p, _u8p, _u8p]
+_lib.uqo_append_fp8.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
+                                C.c_int, C.c_float, C.c_float, _u8p, _u8p]
+_lib.uqo_append_bf16.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
+                                 C.c_int, _u16p, _u16p]
+_lib.uqo_decode.argtypes = [C.c_int, _u16p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_float, C.c_float,
+                            _i32p, C.c_int, _i32p, C.c_double, C.c_uint64, _f64p]
+
+KIND_FP4, KIND_FP8, KIND_BF16 = 0, 1, 2
+DEFAULT_SEED = 42
+C_CONSTANT = float(_lib.uqo_c_constant())
+ROUND_LOG2, ROUND_LINEAR, ROUND_FLOOR, ROUND_CEIL = 0, 1, 2, 3
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def splitmix64(seed: int, i: int) -> int:
+    return int(_lib.uqo_splitmix64(seed, i))
+
+
+def signs(seed: int, d: int) -> np.ndarray:
+    s = np.empty(d, np.int8)
+    _lib.uqo_signs(seed, d, s)
+    return s
+
+
+def inv_sqrt_d(d: int) -> np.float32:
+    return np.float32(_lib.uqo_inv_sqrt_d(d))
+
+
+def rotate_fp32(x: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """R1 forward rotation of each row of x (fp32)."""
+    x = _c(x, np.float32)
+    d = x.shape[-1]
+    s = signs(seed, d)
+    flat = x.reshape(-1, d)
+    out = np.empty_like(flat)
+    for r in range(flat.shape[0]):
+        _lib.uqo_rotate_fp32(flat[r], d, s, out[r])
+    return out.reshape(x.shape)
+
+
+def inverse_rotate_f64(o: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
+    o = _c(o, np.float64)
+    d = o.shape[-1]
+    s = signs(seed, d)
+    flat = o.reshape(-1, d)
+    out = np.empty_like(flat)
+    for r in range(flat.shape[0]):
+        _lib.uqo_inverse_rotate_f64(flat[r], d, s, out[r])
+    return out.reshape(o.shape)
+
+
+def pow2_exponent(t: float, mode: int = ROUND_LOG2) -> int:
+    return int(_lib.uqo_pow2_exponent(float(t), mode))
+
+
+def scale_byte(m: float, c: float = None, mode: int = ROUND_LOG2) -> int:
+    return int(_lib.uqo_scale_byte(np.float32(m), np.float32(C_CONSTANT if c is None else c), mode))
+
+
+def e2m1_code(r: float) -> int:
+    return int(_lib.uqo_e2m1_code(float(r)))
+
+
+def e2m1_value(code: int) -> float:
+    return float(_lib.uqo_e2m1_value(code))
+
+
+def fp4_value(code: int, byte: int) -> float:
+    return float(_lib.uqo_fp4_value(code, byte))
+
+
+def quantize_rotated(y: np.ndarray, c: float = None, mode: int = ROUND_LOG2):
+    """Quantiser stage alone (R2 + R3) on already-rotated rows."""
+    y = _c(y, np.float32)
+    d = y.shape[-1]
+    n = y.size // d
+    codes = np.empty(n * d // 2, np.uint8)
+    scales = np.empty(n * d // 32, np.uint8)
+    _lib.uqo_quantize_rotated(y.reshape(-1), n, d, np.float32(C_CONSTANT if c is None else c), mode,
+                              codes, scales)
+    return codes.reshape(y.shape[:-1] + (d // 2,)), scales.reshape(y.shape[:-1] + (d // 32,))
+
+
+def _rows(x):
+    """(pointer-holding array, is_fp32) for a bf16 (uint16) or fp32 array."""
+    if x.dtype == np.uint16:
+        return _c(x, np.uint16), 0
+    return _c(x, np.float32), 1
+
+
+def quantize_vectors(x: np.ndarray, seed: int = DEFAULT_SEED):
+    """R1 + R2 + R3 on rows of x (uint16 bf16 bits or fp32)."""
+    xa, f32 = _rows(x)
+    d = xa.shape[-1]
+    n = xa.size // d
+    codes = np.empty(n * d // 2, np.uint8)
+    scales = np.empty(n * d // 32, np.uint8)
+    _lib.uqo_quantize_vectors(xa.ctypes.data, f32, n, d, seed, codes, scales)
+    return codes.reshape(xa.shape[:-1] + (d // 2,)), scales.reshape(xa.shape[:-1] + (d // 32,))
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = _c(x, np.float32).reshape(-1)
+    return np.array([_lib.uqo_f32_to_bf16(v) for v in x], np.uint16)
+
+
+def e4m3_value(byte: int) -> float:
+    return float(_lib.uqo_e4m3_value(byte))
+
+
+def e4m3_code(x: float) -> int:
+    return int(_lib.uqo_e4m3_code(np.float32(x)))
+
+
+def query_fp8(q_bf16: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """R4: rotated E4M3 query bytes for each bf16 row."""
+    q = _c(q_bf16, np.uint16)
+    d = q.shape[-1]
+    flat = q.reshape(-1, d)
+    out = np.empty(flat.shape, np.uint8)
+    for r in range(flat.shape[0]):
+        _lib.uqo_query_fp8(flat[r], d, seed, out[r])
+    return out.reshape(q.shape)
+
+
+class Cache:
+    """Host copy of a paged cache in the library's layout [P][Hkv][ps][row]."""
+
+    def __init__(self, kind, num_pages, num_kv_heads, page_size, head_dim, k_scale=1.0, v_scale=1.0,
+                 seed=DEFAULT_SEED):
+        self.kind, self.P, self.Hkv, self.ps, self.d = kind, num_pages, num_kv_heads, page_size, head_dim
+        self.k_scale, self.v_scale, self.seed = float(k_scale), float(v_scale), seed
+        rows = num_pages * num_kv_heads * page_size
+        if kind == KIND_FP4:
+            self.kc = np.zeros((rows, head_dim // 2), np.uint8)
+            self.vc = np.zeros((rows, head_dim // 2), np.uint8)
+            self.ks = np.zeros((rows, head_dim // 32), np.uint8)
+            self.vs = np.zeros((rows, head_dim // 32), np.uint8)
+        elif kind == KIND_FP8:
+            self.kc = np.zeros((rows, head_dim), np.uint8)
+            self.vc = np.zeros((rows, head_dim), np.uint8)
+            self.ks = self.vs = None
+        else:
+            self.kc = np.zeros((rows, head_dim), np.uint16)
+            self.vc = np.zeros((rows, head_dim), np.uint16)
+            self.ks = self.vs = None
+
+    def append(self, k, v, slot_mapping):
+        """Quantize-append T tokens ([T][Hkv][d], bf16 bits or fp32)."""
+        ka, f32 = _rows(k)
+        va, _ = _rows(v)
+        T = ka.shape[0]
+        slots = _c(slot_mapping, np.int64)
+        args = (ka.ctypes.data, va.ctypes.data, f32, T, slots, self.Hkv, self.ps, self.d)
+        if self.kind == KIND_FP4:
+            _lib.uqo_append_fp4(*args, self.seed, self.kc, self.ks, self.vc, self.vs)
+        elif self.kind == KIND_FP8:
+            _lib.uqo_append_fp8(*args, np.float32(self.k_scale), np.float32(self.v_scale), self.kc, self.vc)
+        else:
+            _lib.uqo_append_bf16(*args, self.kc, self.vc)
+
+    def decode(self, q_bf16, block_table, seq_lens, sm_scale=0.0):
+        """fp64 decode attention; q: [B][Hq][d] bf16 bits -> [B][Hq][d] float64."""
+        q = _c(q_bf16, np.uint16)
+        B, Hq, d = q.shape
+        bt = _c(block_table, np.int32)
+        sl = _c(seq_lens, np.int32)
+        out = np.empty((B, Hq, d), np.float64)
+        ptr = lambda a: None if a is None else a.ctypes.data
+        _lib.uqo_decode(self.kind, q.reshape(-1), B, Hq, self.Hkv, d, self.ps, ptr(self.kc), ptr(self.ks),
+                        ptr(self.vc), ptr(self.vs), np.float32(self.k_scale), np.float32(self.v_scale),
+                        bt.reshape(-1), bt.shape[1], sl, float(sm_scale), self.seed, out.reshape(-1))
+        return out
+
+
+_lib.uqo_e2m1_codes.argtypes = [_f64p, C.c_int64, _u8p]
+_lib.uqo_e4m3_codes.argtypes = [_f32p, C.c_int64, _u8p]
+_lib.uqo_scale_bytes.argtypes = [_f32p, C.c_int64, C.c_float, C.c_int, _u8p]
+_lib.uqo_group_mse.restype = C.c_double
+_lib.uqo_group_mse.argtypes = [_f32p, C.c_int64, C.c_float, C.c_int]
+ROUND_CONTINUOUS = -1
+
+
+def e2m1_codes(r: np.ndarray) -> np.ndarray:
+    r = _c(r, np.float64).reshape(-1)
+    out = np.empty(r.size, np.uint8)
+    _lib.uqo_e2m1_codes(r, r.size, out)
+    return out
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    x = _c(x, np.float32).reshape(-1)
+    out = np.empty(x.size, np.uint8)
+    _lib.uqo_e4m3_codes(x, x.size, out)
+    return out
+
+
+def scale_bytes(m: np.ndarray, c: float = None, mode: int = ROUND_LOG2) -> np.ndarray:
+    m = _c(m, np.float32).reshape(-1)
+    out = np.empty(m.size, np.uint8)
+    _lib.uqo_scale_bytes(m, m.size, np.float32(C_CONSTANT if c is None else c), mode, out)
+    return out
+
+
+def group_mse(y: np.ndarray, c: float, mode: int) -> float:
+    y = _c(y, np.float32).reshape(-1)
+    return float(_lib.uqo_group_mse(y, y.size // 32, np.float32(c), mode))

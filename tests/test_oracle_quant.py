@@ -1,0 +1,182 @@
+"""Pins of the oracle's quantiser (R2 scale byte, R3 E2M1 codes) against the
+format definition, brute-force nearest-point search, exact round trips, the
+byte accounting the pages print, and the pages' c ablation (soft pin)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+FACTS = json.load(open(os.path.join(GOLD, "format_facts.json")))
+
+
+def _e2m1_from_bits(code):
+    s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    bias = FACTS["e2m1_format"]["value"]["exponent_bias"]
+    v = m * 0.5 if e == 0 else 2.0 ** (e - bias) * (1 + m / 2)
+    return -v if s else v
+
+
+def test_e2m1_value_table_matches_format_definition():
+    for code in range(16):
+        assert oracle.e2m1_value(code) == _e2m1_from_bits(code)
+    assert [oracle.e2m1_value(c) for c in range(8)] == FACTS["e2m1_grid"]["value"]
+
+
+def _nearest_brute(r):
+    """Nearest grid magnitude by exhaustive distance, ties to the even code
+    (mantissa bit 0), saturating; sign from the IEEE sign bit."""
+    a = abs(r)
+    best, bestd = 0, math.inf
+    for code in range(8):
+        dist = abs(_e2m1_from_bits(code) - a)
+        if dist < bestd or (dist == bestd and code % 2 == 0):
+            best, bestd = code, dist
+    return best | (8 if math.copysign(1.0, r) < 0 else 0)
+
+
+def _dense_r_values():
+    vals = []
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    grid = FACTS["e2m1_grid"]["value"]
+    for p in mids + grid + [6.5, 7.0, 100.0]:
+        bits = int(np.float32(p).view(np.uint32))
+        # the fp32 neighbours p - 40 ulp .. p + 40 ulp (all p here are positive)
+        vals += np.arange(max(bits - 40, 0), bits + 41, dtype=np.int64).astype(np.uint32).view(np.float32).tolist()
+    rng = np.random.default_rng(7)
+    vals += rng.uniform(-8, 8, 20000).astype(np.float32).astype(np.float64).tolist()
+    vals += [0.0, -0.0, 1e-30, -1e-30, 0.2499999, -0.2500001]
+    return np.array(vals + [-v for v in vals], np.float64)
+
+
+def test_e2m1_encoder_matches_brute_force():
+    r = _dense_r_values()
+    got = oracle.e2m1_codes(r)
+    want = np.array([_nearest_brute(v) for v in r], np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (r[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def test_e2m1_ties_go_to_even_code():
+    assert [oracle.e2m1_code(v) for v in [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]] == [0, 2, 2, 4, 4, 6, 6]
+    assert oracle.e2m1_code(-0.0) == 8 and oracle.e2m1_code(-0.1) == 8
+    assert oracle.e2m1_code(1e9) == 7 and oracle.e2m1_code(-1e9) == 15
+
+
+def _scale_byte_brute(m):
+    """byte = clamp(E + 127, 0, 254), E the integer nearest to log2(fl32(c*m))
+    found by trying every exponent; NaN/Inf -> 0xFF; m = 0 -> 0."""
+    if not np.isfinite(m):
+        return 0xFF
+    t = float(np.float32(np.float32(FACTS["c_constant"]["value"]) * np.float32(m)))
+    if t == 0.0:
+        return 0
+    lt = math.log2(t)
+    E = min(range(-200, 200), key=lambda k: abs(lt - k))
+    return max(0, min(254, E + 127))
+
+
+def test_scale_byte_matches_brute_force():
+    rng = np.random.default_rng(8)
+    ms = list(np.exp(rng.uniform(-90, 90, 5000)).astype(np.float32))
+    # values right at the sqrt(2) crossings of t = 0.156 m, and extremes
+    for k in range(-130, 128, 3):
+        t = 2.0 ** (k + 0.5)
+        m0 = np.float32(t / 0.156)
+        for j in range(-3, 4):
+            mm = m0
+            for _ in range(abs(j)):
+                mm = np.nextafter(mm, np.float32(np.inf if j > 0 else 0), dtype=np.float32)
+            ms.append(mm)
+    ms += [np.float32(0), np.float32(1e-45), np.float32(3e38), np.float32(np.finfo(np.float32).max),
+           np.float32(np.inf), np.float32(np.nan)]
+    ms = np.array(ms, np.float32)
+    got = oracle.scale_bytes(ms)
+    want = np.array([_scale_byte_brute(m) for m in ms], np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (ms[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def test_dequant_rule():
+    """value = code * 2^(byte-127) for every (code, byte) pair, exactly."""
+    for byte in range(255):
+        for code in range(16):
+            assert oracle.fp4_value(code, byte) == _e2m1_from_bits(code) * 2.0 ** (byte - 127)
+    assert math.isnan(oracle.fp4_value(3, 0xFF))
+
+
+@pytest.mark.parametrize("E", [-100, -7, -1, 0, 1, 5, 60])
+def test_exact_round_trip_of_grid_aligned_groups(E):
+    """A group of grid values times 2^E that contains +-6*2^E is reproduced
+    exactly: 0.156 * 6 = 0.936 rounds to the power 2^0 (relative to 2^E)."""
+    rng = np.random.default_rng(100 + E)
+    grid = np.array(FACTS["e2m1_grid"]["value"])
+    vals = rng.choice(grid, size=(50, 4, 32)) * rng.choice([-1.0, 1.0], size=(50, 4, 32))
+    vals[:, :, 0] = 6.0 * rng.choice([-1.0, 1.0], size=(50, 4))
+    y = (vals * 2.0 ** E).astype(np.float32).reshape(50, 128)
+    codes, scales = oracle.quantize_rotated(y)
+    assert np.all(scales == E + 127)
+    lo, hi = codes & 15, codes >> 4
+    dec = np.empty((50, 128))
+    dec[:, 0::2] = np.vectorize(_e2m1_from_bits)(lo)
+    dec[:, 1::2] = np.vectorize(_e2m1_from_bits)(hi)
+    assert np.array_equal(dec * 2.0 ** E, y.astype(np.float64))
+
+
+def test_byte_accounting():
+    d = 128
+    codes, scales = oracle.quantize_rotated(np.ones((3, d), np.float32))
+    per_group = (codes.shape[-1] + scales.shape[-1]) / (d // FACTS["group_size"]["value"])
+    assert per_group == FACTS["bytes_per_group"]["value"]
+    assert per_group * 8 / 32 == FACTS["bits_per_element"]["value"]
+
+
+def test_nibble_order_low_first():
+    y = np.zeros((1, 32), np.float32)
+    y[0, 0], y[0, 1] = 6.0, 1.0  # m = 6 -> E = 0
+    codes, scales = oracle.quantize_rotated(y)
+    assert scales[0, 0] == 127 and codes[0, 0] == (7 | (2 << 4))
+
+
+def test_nonfinite_group():
+    y = np.ones((1, 64), np.float32)
+    y[0, 40] = np.nan
+    codes, scales = oracle.quantize_rotated(y)
+    assert scales[0].tolist() == [oracle.scale_byte(1.0), 0xFF]
+    assert np.all(codes[0, 16:] == 0)
+
+
+def _unit_vector_groups(n=40000, d=128, seed=1):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, d))
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    return x.astype(np.float32).reshape(-1)
+
+
+def _argmin_c(y, mode, lo, hi, step=0.002):
+    cs = np.arange(lo, hi, step)
+    v = [oracle.group_mse(y, c, mode) for c in cs]
+    return float(cs[int(np.argmin(v))])
+
+
+def test_c_sweep_soft_pin():
+    """The pages: c = 0.156 is the MSE-optimal constant of the objective
+    c* = argmin_c E[(z - c m q(z/(c m)))^2], and 0.195 is the optimum once the
+    scale is a power of two.  On rotated coordinates (uniform unit vectors,
+    the model of the rotation pages) the continuous optimum must sit near
+    0.156, and the power-of-two optimum of the rounding used (nearest in log2)
+    near 0.195.  Rounding in linear distance or floor/ceil does not give 0.195
+    -- this is the evidence for the log2 reading of 'nearest power of two'."""
+    y = _unit_vector_groups()
+    c_cont = _argmin_c(y, oracle.ROUND_CONTINUOUS, 0.13, 0.19)
+    c_log = _argmin_c(y, oracle.ROUND_LOG2, 0.17, 0.23)
+    c_lin = _argmin_c(y, oracle.ROUND_LINEAR, 0.17, 0.23)
+    assert 0.150 <= c_cont <= 0.172, c_cont
+    assert abs(c_log - FACTS["c_power_of_two_optimal"]["value"]) <= 0.004, c_log
+    assert abs(c_lin - 0.195) > 0.008, c_lin
+    # raw absmax (c = 1) is far worse than the shrunk constant
+    assert oracle.group_mse(y, 1.0, oracle.ROUND_LOG2) > 3 * oracle.group_mse(y, 0.156, oracle.ROUND_LOG2)
