@@ -1,0 +1,367 @@
+"""Benchmark of the UltraQuant FP4 KV-cache path on GB300.
+
+Workload (per GPU): 64K-context decode, batch 8, 8 KV heads, 64 query heads,
+head_dim 128, page size 16, shuffled pages.  Setup (untimed) quantize-appends
+32768 tokens per sequence; the prefill-append of 32768 more tokens per
+sequence is timed on its own (quantize GB/s); then one step = append one new
+token per sequence + decode attention of one query token per sequence at
+context 65536+i, straight from the packed cache.  value = decode tokens/s
+(sequences x steps / time), whole job over all ranks.
+
+--impl reference runs the CPU oracle (the plain C reference this library is
+tested against) on a bounded sample of the same workload.
+
+Output: one JSON line on rank 0.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, HKV, HQ, D, PS = 8, 8, 64, 128, 16
+CTX0, APPEND = 32768, 32768
+FP4_BYTES_PER_TOKEN_HEAD = 136   # K and V: 64 code bytes + 4 scale bytes each
+FP8_BYTES_PER_TOKEN_HEAD = 256
+BF16_BYTES_PER_TOKEN_HEAD = 512
+METRIC = "decode tokens/s at 64K ctx (KV-read GB/s and quantize GB/s reported)"
+WORKLOAD = "append64k: B8 Hkv8 Hq64 D128 ps16, 32768 cached + 32768 appended tokens/seq, then decode steps"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_baseline(w, seconds_hint=True):
+    """The oracle, as it stands, decoding one sequence (all 8 kv heads, 64 query
+    heads) at 64K context on this host's cores (single thread)."""
+    import oracle
+    L = CTX0 + APPEND
+    seq = 0
+    k, v = w.kv(seq, 0, L, device="cpu")
+    oc = oracle.Cache(oracle.KIND_FP4, L // PS, HKV, PS, D)
+    to16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    oc.append(to16(k), to16(v), np.arange(L))
+    q = to16(w.q(0, device="cpu")[seq:seq + 1])
+    bt = np.arange(L // PS, dtype=np.int32)[None]
+    t0 = time.perf_counter()
+    oc.decode(q, bt, np.array([L], np.int32))
+    dt = time.perf_counter() - t0
+    return {"value": 1.0 / dt, "unit": "decode tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "1 sequence x 8 kv heads x 64 query heads at context %d (FP4 cache, fp64 attention), "
+                      "single-threaded C oracle, %.1f s" % (L, dt)}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.make("append64k", seq_lens=[CTX0 + APPEND] * B, extra_tokens=16)
+    import oracle
+    L = CTX0 + APPEND
+    to16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    k, v = w.kv(0, 0, L, device="cpu")
+    oc = oracle.Cache(oracle.KIND_FP4, L // PS, 1, PS, D)
+    oc.append(to16(k[:, :1]), to16(v[:, :1]), np.arange(L))   # kv head 0 of sequence 0
+    bt = np.arange(L // PS, dtype=np.int32)[None]
+    q = to16(w.q(0, device="cpu")[0:1, :HQ // HKV])           # its 8 query heads
+    sl = np.array([L], np.int32)
+    for _ in range(args.warmup):
+        oc.decode(q, bt, sl)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oc.decode(q, bt, sl)
+    dt = time.perf_counter() - t0
+    per = dt / args.steps
+    value = (1.0 / HKV) / per   # one step decodes 1/8 of one sequence's token
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "decode tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "seq 0, kv head 0, 8 query heads"},
+            "cpu_baseline": {"value": value, "unit": "decode tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "1 sequence x 1 kv head x 8 query heads at context %d per step" % L},
+            "e2e": {"value": value, "unit": "decode tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _event_pair():
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def run_uq(args):
+    ws, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import ue8m0_kv_cache_gb300 as uq
+    import workloads
+
+    steps, warmup = args.steps, args.warmup
+    extra = steps + warmup + 8
+    # Each rank holds its own batch of 8 sequences (weak scaling, no collective on the data path).
+    w = workloads.make("append64k", seq_lens=[CTX0 + APPEND] * B, extra_tokens=extra, seed=1005 + 7919 * rank)
+    stream = torch.cuda.current_stream()
+    caches = {"fp4": uq.KVCache(uq.FP4_UE8M0, w.num_pages, HKV, PS, D, device=dev)}
+    if not args.no_anchors:
+        caches["fp8"] = uq.KVCache(uq.FP8_E4M3, w.num_pages, HKV, PS, D, device=dev)
+        caches["bf16"] = uq.KVCache(uq.BF16, w.num_pages, HKV, PS, D, device=dev)
+
+    # ---- setup: the cached 32768 tokens per sequence (untimed)
+    for b in range(B):
+        for t0 in range(0, CTX0, 8192):
+            k, v = w.kv(b, t0, 8192, device=dev)
+            sl = torch.from_numpy(w.slots(b, t0, 8192)).to(dev)
+            for c in caches.values():
+                uq.uq_quantize_append(k, v, sl, c)
+    # ---- the prefill-append of 32768 more tokens per sequence: inputs resident, timed alone
+    ks, vs, ss = [], [], []
+    for b in range(B):
+        k, v = w.kv(b, CTX0, APPEND, device=dev)
+        ks.append(k)
+        vs.append(v)
+        ss.append(torch.from_numpy(w.slots(b, CTX0, APPEND)).to(dev))
+    kA, vA, sA = torch.cat(ks), torch.cat(vs), torch.cat(ss)
+    del ks, vs, ss
+    for c in list(caches.values())[1:]:
+        uq.uq_quantize_append(kA, vA, sA, c)
+    fp4 = caches["fp4"]
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    q_times = []
+    for i in range(3 + 5):
+        l2_flush.zero_()
+        e0, e1 = _event_pair()
+        e0.record(stream)
+        uq.uq_quantize_append(kA, vA, sA, fp4)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            q_times.append(e0.elapsed_time(e1) * 1e-3)
+    n_th = B * APPEND * HKV
+    q_in, q_out = n_th * 2 * D * 2, n_th * FP4_BYTES_PER_TOKEN_HEAD + B * APPEND * 8
+    q_t = float(np.median(q_times))
+    quantize = {"GB_per_s": (q_in + q_out) / q_t / 1e9, "ms": q_t * 1e3, "tokens": B * APPEND,
+                "bytes_in": q_in, "bytes_out": q_out, "launches": 1}
+    del kA, vA, sA, l2_flush
+    assert uq.uq_check_device_status() == 0
+
+    # ---- decode steps: per step one new token per sequence is appended, then decoded
+    bt = torch.from_numpy(w.block_table).to(dev)
+    L0 = CTX0 + APPEND
+    n_new = steps + warmup
+    kv_new = [w.kv(b, L0, n_new, device=dev) for b in range(B)]          # [n_new][Hkv][D] per sequence
+    k_all = torch.stack([kv[0] for kv in kv_new], 1).contiguous()        # [n_new][B][Hkv][D]
+    v_all = torch.stack([kv[1] for kv in kv_new], 1).contiguous()
+    s_all = torch.from_numpy(np.stack([w.slots(b, L0, n_new) for b in range(B)], 1).copy()).to(dev)
+    newk = [k_all[s] for s in range(n_new)]
+    newv = [v_all[s] for s in range(n_new)]
+    news = [s_all[s] for s in range(n_new)]
+    q_pool = [w.q(1 + s, device=dev) for s in range(32)]
+    qs = [q_pool[s % 32] for s in range(n_new)]
+    del kv_new
+    lens = [torch.full((B,), L0 + s + 1, dtype=torch.int32, device=dev) for s in range(n_new)]
+    out = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
+    wsp = uq.workspace(B, HQ, HKV, D, dev)
+    decode_fn = {"fp4": uq.uq_decode_attention, "fp8": uq.uq_decode_attention_fp8,
+                 "bf16": uq.uq_decode_attention_bf16}
+
+    def decode_loop(name, count, offset, timed_decode):
+        c = caches[name]
+        for s in range(offset, offset + count):
+            uq.uq_quantize_append(newk[s], newv[s], news[s], c)
+            if timed_decode is not None:
+                e0, e1 = _event_pair()
+                e0.record(stream)
+            decode_fn[name](qs[s], c, bt, lens[s], out=out, workspace=wsp)
+            if timed_decode is not None:
+                e1.record(stream)
+                timed_decode.append((e0, e1))
+
+    def timed(name, clocks=None):
+        decode_loop(name, warmup, 0, None)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.start()
+        ev = []
+        t0, t1 = _event_pair()
+        t0.record(stream)
+        decode_loop(name, steps, warmup, ev)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if clocks:
+            clk = clocks.stop()
+        if ws > 1:
+            torch.distributed.barrier()
+        total = t0.elapsed_time(t1) * 1e-3
+        dec = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e-3
+        return total, dec, (clk if clocks else None)
+
+    clocks = Clocks(local if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0)
+    total, dec_t, clk = timed("fp4", clocks)
+    assert uq.uq_check_device_status() == 0
+    if ws > 1:
+        t = torch.tensor([total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    ctx_mean = L0 + warmup + (steps + 1) / 2.0
+    kv_bytes = B * HKV * ctx_mean * FP4_BYTES_PER_TOKEN_HEAD
+    hbm, peak_kind = _peaks()
+    ms_per_step = total / steps * 1e3
+    value = ws * B * steps / total
+    achieved = kv_bytes / dec_t / 1e9
+    prof = {}
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_fp4_traffic.json")) as f:
+            prof = json.load(f)
+    except Exception:
+        pass
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": prof.get("traffic_bytes_per_launch"), "peak_kind": peak_kind,
+                "kernel": "uq_decode_attention (decode + merge launches), FP4 cache",
+                "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_t * 1e3,
+                "frac_of_nominal_8TBps": achieved / 8000.0}
+
+    anchors = {}
+    for name, per in (("fp8", FP8_BYTES_PER_TOKEN_HEAD), ("bf16", BF16_BYTES_PER_TOKEN_HEAD)):
+        if name not in caches:
+            continue
+        tt, dt, _ = timed(name)
+        anchors[name] = {"decode_tokens_per_s": B * steps / tt, "ms_per_step": tt / steps * 1e3,
+                         "decode_ms": dt * 1e3, "kv_GB_per_s": B * HKV * ctx_mean * per / dt / 1e9}
+    assert uq.uq_check_device_status() == 0
+
+    # ---- end to end through the public API with host buffers
+    n_e2e = min(steps, 200)
+    pin = lambda t: t.cpu().pin_memory()
+    hk = [pin(newk[s]) for s in range(n_e2e)]
+    hv = [pin(newv[s]) for s in range(n_e2e)]
+    hs = [pin(news[s]) for s in range(n_e2e)]
+    hq = [pin(qs[s]) for s in range(n_e2e)]
+    hout = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
+    dk, dv, dsl, dq = (torch.empty_like(newk[0]), torch.empty_like(newv[0]), torch.empty_like(news[0]),
+                       torch.empty_like(qs[0]))
+    torch.cuda.synchronize()
+    t0, t1 = _event_pair()
+    t0.record(stream)
+    for s in range(n_e2e):
+        dk.copy_(hk[s], non_blocking=True)
+        dv.copy_(hv[s], non_blocking=True)
+        dsl.copy_(hs[s], non_blocking=True)
+        dq.copy_(hq[s], non_blocking=True)
+        uq.uq_quantize_append(dk, dv, dsl, fp4)
+        uq.uq_decode_attention(dq, fp4, bt, lens[s], out=out, workspace=wsp)
+        hout.copy_(out, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = t0.elapsed_time(t1) * 1e-3
+    h2d = dk.numel() * 2 + dv.numel() * 2 + dsl.numel() * 8 + dq.numel() * 2
+    e2e = {"value": ws * B * n_e2e / e2e_t, "unit": "decode tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": hout.numel() * 4, "steps": n_e2e}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        try:
+            cpu = _cpu_baseline(w)
+        except Exception as e:  # reported, not fatal
+            cpu = {"error": repr(e)}
+    line = {"metric": METRIC, "value": value, "unit": "decode tokens/s", "n_gpus": ws, "steps": steps,
+            "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e2m1/ue8m0 cache, f16 tensor-core MMA, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "context_mean": ctx_mean, "batch_per_gpu": B,
+                       "parallelism": "replicas (weak scaling, no collective)" if ws > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (FP4 KV read %.0f MB per step)" % (kv_bytes / 1e6)},
+            "kv_GB_per_s": achieved, "quantize": quantize, "anchors": anchors, "roofline": roofline,
+            "clocks": clk, "e2e": e2e, "gpu_launches": 3 * steps, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
+    ap.add_argument("--no-anchors", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_uq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * uq.h -- C ABI of libuq.so: a paged 4-bit KV cache (FP4 E2M1 codes with one
+ * UE8M0 scale byte per 32 channels, "UltraQuant") for single-token decode
+ * attention on NVIDIA GB300 (sm_103a), plus FP8-E4M3 and BF16 caches of the
+ * same shape as comparison anchors.
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [UQ-review]    "UltraQuant: 4-bit KV Caching for Context-Heavy Agents",
+ *                  review at manon006.tistory.com/395: §3.1 write path and
+ *                  storage format, §3.2 dequantisation rule and FP8 query,
+ *                  §3.3 constant c, §4.2 decode kernel (query rounded outside
+ *                  the K-tile loop, cache layout matched to the scale operand).
+ *   [UQ-residency] "kv-cache-4bit-serving-residency-collapse",
+ *                  pheeree.github.io (2026-09-01): layout and dequant rule
+ *                  (footnote 2), c ablation (footnote 13).
+ *   [TQ-guide]     "TurboQuant 완전 정리" (juhoplayground.github.io):
+ *                  randomised Hadamard rotation, orthogonality.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
+ *     The caller allocates and owns every buffer (cache, workspace, outputs);
+ *     the library allocates no memory and keeps no state between calls other
+ *     than one device status word per device (see uq_check_device_status).
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  Argument checks happen synchronously, before anything is
+ *     enqueued; a failed check enqueues nothing.
+ *   - Every call returns a uq_status; no C++ exception crosses the ABI.
+ *     UQ_ERR_CUDA means a CUDA runtime call or kernel launch failed.
+ *   - Calls are thread-safe.  Calls that write the same cache region, or share
+ *     a workspace, must be ordered by the caller (same stream or events).
+ *   - Device-side range checks (slot, page, sequence length out of bounds) and
+ *     bounded waits inside kernels never fault or hang: they record
+ *     UQ_ERR_DEVICE_BOUNDS / UQ_ERR_DEVICE_TIMEOUT in the device status word,
+ *     skip the offending access, and the host reads the word with
+ *     uq_check_device_status.
+ */
+#ifndef UQ_H_
+#define UQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum uq_status {
+  UQ_OK = 0,
+  UQ_ERR_INVALID_ARG = 1,    /* null pointer, negative size, inconsistent shapes */
+  UQ_ERR_UNSUPPORTED = 2,    /* valid but unimplemented shape (head_dim, page size, batch) */
+  UQ_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+  UQ_ERR_WORKSPACE = 4,      /* workspace too small */
+  UQ_ERR_CUDA = 5,           /* CUDA runtime / launch error */
+  UQ_ERR_DEVICE_TIMEOUT = 6, /* a bounded wait inside a kernel ran out (device status word) */
+  UQ_ERR_DEVICE_BOUNDS = 7   /* a slot / page / length index was out of range (device status word) */
+} uq_status;
+
+typedef enum uq_kv_dtype {
+  UQ_FP4_UE8M0 = 0, /* rotated FP4 E2M1 codes + UE8M0 group scales, 4.25 bit/elem */
+  UQ_FP8_E4M3 = 1,  /* unrotated E4M3 with one per-tensor scale for K and one for V */
+  UQ_BF16 = 2       /* unrotated bf16 */
+} uq_kv_dtype;
+
+typedef enum uq_in_dtype { UQ_IN_BF16 = 0, UQ_IN_FP32 = 1 } uq_in_dtype;
+
+/*
+ * A paged KV cache.  All pointers are device pointers owned by the caller.
+ * Physical rows are addressed [page][kv_head][offset] with page in
+ * [0, num_pages), offset in [0, page_size); a token's slot is
+ * page * page_size + offset (the vLLM convention).
+ *
+ *   UQ_FP4_UE8M0: k_codes, v_codes : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+ *                   byte j of a row = code(2j) | code(2j+1) << 4, codes of the
+ *                   ROTATED vector ([UQ-review] §3.1);
+ *                 k_scales, v_scales: uint8 [num_pages][num_kv_heads][page_size][head_dim/32]
+ *                   UE8M0 byte of channels 32g..32g+31; value = code * 2^(byte-127)
+ *                   ([UQ-review] §3.2); 0xFF marks a non-finite group.
+ *                 17 bytes per 32 elements ([UQ-review] §3.1).
+ *   UQ_FP8_E4M3:  k_codes, v_codes : uint8 [num_pages][num_kv_heads][page_size][head_dim],
+ *                   element = e4m3(x / k_scale) (resp. v_scale); scales unused (NULL).
+ *   UQ_BF16:      k_codes, v_codes : bf16  [num_pages][num_kv_heads][page_size][head_dim]; scales unused.
+ *
+ * rot_seed seeds the ±1 diagonal of the randomised Hadamard rotation (FP4
+ * only); one sign vector serves K, V, the query and every head.  The same
+ * seed must be used for append and decode.
+ */
+typedef struct uq_cache {
+  int32_t dtype;        /* uq_kv_dtype */
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t page_size;    /* power of two, 16..256 */
+  int32_t head_dim;     /* 64 or 128 */
+  void* k_codes;
+  void* k_scales;
+  void* v_codes;
+  void* v_scales;
+  float k_scale;        /* FP8 only (1.0 if unused) */
+  float v_scale;        /* FP8 only (1.0 if unused) */
+  uint64_t rot_seed;    /* FP4 only */
+} uq_cache;
+
+/* Byte size of array `which` of the cache (0 = k_codes, 1 = k_scales,
+ * 2 = v_codes, 3 = v_scales); 0 for an unused array or invalid arguments.
+ * Host-only; enqueues nothing. */
+size_t uq_cache_bytes(const uq_cache* cache, int32_t which);
+
+/*
+ * Quantize-append ([UQ-review] §3.1 write path): for each token t with
+ * slot_mapping[t] >= 0 and each kv head h, the rows k[t][h][:] and v[t][h][:]
+ * are written into the cache at that slot.
+ *   FP4:  y = fl32(FWHT_fp32(s .* x) * fl32(1/sqrt(head_dim))) (Walsh-Hadamard
+ *         rotation, Sylvester order, stages in ascending stride), then per
+ *         32-channel group m = max|y|, E = nearest integer to
+ *         log2(fl32(0.156f * m)), byte = clamp(E + 127, 0, 254), codes =
+ *         E2M1(y * 2^-E) rounded to nearest, ties to even, saturating at 6.
+ *   FP8:  e4m3(x / k_scale), round to nearest even, saturating at 448.
+ *   BF16: x rounded to bf16 (exact copy for bf16 input).
+ * k, v         : device, [num_tokens][num_kv_heads][head_dim], bf16 or fp32
+ *                per in_dtype, 16-byte aligned rows (contiguous).
+ * slot_mapping : device int64 [num_tokens]; negative = skip the token.
+ *                Slots >= num_pages*page_size are skipped and recorded as
+ *                UQ_ERR_DEVICE_BOUNDS.
+ * block_table, max_pages_per_seq: accepted for interface symmetry with the
+ *                decode call and unused (slots are physical); may be NULL/0.
+ * num_tokens == 0 is a no-op.
+ */
+uq_status uq_quantize_append(const void* k, const void* v, int32_t in_dtype, int64_t num_tokens,
+                             const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int64_t* slot_mapping, const uq_cache* cache,
+                             cudaStream_t stream);
+
+/* Workspace bytes that uq_decode_attention needs for this batch shape on the
+ * current device.  Host-only.  A smaller workspace is accepted as long as it
+ * holds at least one split per (sequence, kv head) plus one; the kernel then
+ * uses fewer blocks. */
+size_t uq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim);
+
+/*
+ * Decode attention for one query token per sequence, straight from the
+ * cache ([UQ-review] §3.2, §4.2):
+ *   FP4:  q~ = e4m3(R q) (rotation as in append, then E4M3 round to nearest
+ *         even, saturating; computed once per block, outside the page loop);
+ *         logits_j = sm_scale * <q~, k^_j> with k^ = code * 2^(byte-127);
+ *         softmax over j < seq_lens[b]; o = sum_j p_j v^_j; out = R^T o
+ *         (inverse rotation; R is orthogonal, [TQ-guide]).
+ *   FP8 / BF16: the same with q in bf16, k^ = e4m3 * k_scale (or bf16) and
+ *         no rotation.
+ * Query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * The key range is split over many blocks (split-K over 16-token chunks of
+ * pages) and the partial results are merged with a log-sum-exp combine.
+ * q           : device bf16 [batch][num_q_heads][head_dim]
+ * block_table : device int32 [batch][max_pages_per_seq]; logical token j of
+ *               sequence b lives in page block_table[b][j / page_size] at
+ *               offset j % page_size.
+ * seq_lens    : device int32 [batch]; 0 gives a zero output row.
+ * sm_scale    : softmax scale; <= 0 selects 1/sqrt(head_dim).
+ * out         : device fp32 [batch][num_q_heads][head_dim].
+ * workspace   : device, >= 16-byte aligned, workspace_bytes long (see
+ *               uq_decode_workspace_bytes); contents need not be initialised.
+ * Supported: head_dim 64 or 128, page_size a power of two in [16, 256],
+ * num_q_heads a multiple of num_kv_heads, batch <= 4096.
+ */
+uq_status uq_decode_attention(const void* q, const uq_cache* cache, const int32_t* block_table,
+                              int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/* The anchors: identical to uq_decode_attention but require cache->dtype to be
+ * UQ_FP8_E4M3 (resp. UQ_BF16) and return UQ_ERR_INVALID_ARG otherwise. */
+uq_status uq_decode_attention_fp8(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                  int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                  int32_t batch, int32_t num_q_heads, float sm_scale, float* out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+uq_status uq_decode_attention_bf16(const void* q, const uq_cache* cache,
+                                   const int32_t* block_table, int32_t max_pages_per_seq,
+                                   const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                   float sm_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns UQ_OK, UQ_ERR_DEVICE_TIMEOUT or UQ_ERR_DEVICE_BOUNDS (the
+ * first error recorded since the last call), or UQ_ERR_CUDA. */
+uq_status uq_check_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* uq_status_string(uq_status status);
+
+/* The ±1 sign diagonal of the rotation, written to host_out[0..d): sign i is
+ * -1 when bit 63 of output i of splitmix64 seeded with `seed` is set
+ * (Steele, Lea, Flood 2014).  Host-only. */
+void uq_rotation_signs(uint64_t seed, int32_t d, int8_t* host_out);
+
+/* ---- test hooks: single stages of the path, for bit-exact checks ---------
+ * All pointers are device pointers; d is 64 or 128. */
+
+/* Forward rotation of n_vec fp32 rows: y = fl32(FWHT(s .* x) * fl32(1/sqrt d)). */
+uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, float* y,
+                         cudaStream_t stream);
+
+/* Quantiser stage alone on already-rotated fp32 rows: codes [n_vec][d/2],
+ * scales [n_vec][d/32] exactly as in uq_quantize_append. */
+uq_status uq_test_quantize_rotated(const float* y, int64_t n_vec, int32_t d, uint8_t* codes,
+                                   uint8_t* scales, cudaStream_t stream);
+
+/* The decode prologue alone: rotated, E4M3-rounded query bytes [n_vec][d]
+ * from bf16 rows q [n_vec][d]. */
+uq_status uq_test_query_fp8(const void* q, int64_t n_vec, int32_t d, uint64_t seed, uint8_t* out,
+                            cudaStream_t stream);
+
+/* E4M3 round-to-nearest-even, saturating, of n fp32 values (n even). */
+uq_status uq_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UQ_H_ */

@@ -370,45 +370,56 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
   double qd[1024], o[1024];
   for (int b = 0; b < B; ++b) {
     int L = seq_lens[b];
-    double* logit = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
-    for (int h = 0; h < Hq; ++h) {
-      int kvh = h / G;
-      double* ob = out + ((int64_t)b * Hq + h) * d;
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
       if (L <= 0) {
-        for (int i = 0; i < d; ++i) ob[i] = 0.0;
+        for (int h = kvh * G; h < (kvh + 1) * G; ++h)
+          for (int i = 0; i < d; ++i) out[((int64_t)b * Hq + h) * d + i] = 0.0;
         continue;
       }
-      const uint16_t* qrow = q + ((int64_t)b * Hq + h) * d;
-      if (kind == 0) {
-        uint8_t q8[1024];
-        uqo_query_fp8(qrow, d, seed, q8);
-        for (int i = 0; i < d; ++i) qd[i] = uqo_e4m3_value(q8[i]);
-      } else {
-        for (int i = 0; i < d; ++i) qd[i] = (double)bf16_to_f32(qrow[i]);
-      }
-      double mx = -INFINITY;
+      /* dequantised keys and values of this (sequence, kv head), logical order */
+      double* K = (double*)malloc(sizeof(double) * (size_t)L * d);
+      double* V = (double*)malloc(sizeof(double) * (size_t)L * d);
+      double* logit = (double*)malloc(sizeof(double) * (size_t)L);
       for (int j = 0; j < L; ++j) {
         int64_t page = block_table[(int64_t)b * max_pages + j / ps];
         int64_t row = (page * Hkv + kvh) * ps + j % ps;
-        double acc = 0.0;
-        for (int i = 0; i < d; ++i) acc += qd[i] * kv_value(kind, kc, ks, row, d, i, k_scale);
-        logit[j] = sm_scale * acc;
-        if (logit[j] > mx) mx = logit[j]; /* a NaN logit reaches the output via exp */
+        for (int i = 0; i < d; ++i) {
+          K[(int64_t)j * d + i] = kv_value(kind, kc, ks, row, d, i, k_scale);
+          V[(int64_t)j * d + i] = kv_value(kind, vc, vs, row, d, i, v_scale);
+        }
       }
-      double lsum = 0.0;
-      for (int i = 0; i < d; ++i) o[i] = 0.0;
-      for (int j = 0; j < L; ++j) {
-        int64_t page = block_table[(int64_t)b * max_pages + j / ps];
-        int64_t row = (page * Hkv + kvh) * ps + j % ps;
-        double p = exp(logit[j] - mx);
-        lsum += p;
-        for (int i = 0; i < d; ++i) o[i] += p * kv_value(kind, vc, vs, row, d, i, v_scale);
+      for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+        double* ob = out + ((int64_t)b * Hq + h) * d;
+        const uint16_t* qrow = q + ((int64_t)b * Hq + h) * d;
+        if (kind == 0) {
+          uint8_t q8[1024];
+          uqo_query_fp8(qrow, d, seed, q8);
+          for (int i = 0; i < d; ++i) qd[i] = uqo_e4m3_value(q8[i]);
+        } else {
+          for (int i = 0; i < d; ++i) qd[i] = (double)bf16_to_f32(qrow[i]);
+        }
+        double mx = -INFINITY;
+        for (int j = 0; j < L; ++j) {
+          double acc = 0.0;
+          for (int i = 0; i < d; ++i) acc += qd[i] * K[(int64_t)j * d + i];
+          logit[j] = sm_scale * acc;
+          if (logit[j] > mx) mx = logit[j]; /* a NaN logit reaches the output via exp */
+        }
+        double lsum = 0.0;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        for (int j = 0; j < L; ++j) {
+          double p = exp(logit[j] - mx);
+          lsum += p;
+          for (int i = 0; i < d; ++i) o[i] += p * V[(int64_t)j * d + i];
+        }
+        for (int i = 0; i < d; ++i) o[i] /= lsum;
+        if (kind == 0) uqo_inverse_rotate_f64(o, d, s, ob);
+        else memcpy(ob, o, sizeof(double) * (size_t)d);
       }
-      for (int i = 0; i < d; ++i) o[i] /= lsum;
-      if (kind == 0) uqo_inverse_rotate_f64(o, d, s, ob);
-      else memcpy(ob, o, sizeof(double) * (size_t)d);
+      free(K);
+      free(V);
+      free(logit);
     }
-    free(logit);
   }
 }
 

@@ -24,3 +24,17 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def _load_by_path(name, path):
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def pytest_sessionstart(session):
+    """Build the C oracle and the CUDA library (nvcc cross-compiles without a GPU)."""
+    _load_by_path("_oracle_build", os.path.join(ROOT, "oracle", "build.py")).build()
+    _load_by_path("_uq_build", os.path.join(ROOT, "ue8m0_kv_cache_gb300", "build.py")).build()

@@ -1,0 +1,236 @@
+"""Python binding of libuq.so: a paged FP4 E2M1 + UE8M0 KV cache ("UltraQuant")
+for GB300, with FP8-E4M3 and BF16 caches of the same shape as anchors.
+
+This module only marshals arguments: torch tensors in, raw device pointers and
+sizes out to the C ABI declared in include/uq.h.  Every step of the path runs
+in the library's CUDA kernels; there is no fallback.  Importing the module
+fails if libuq.so has not been built (``python -m ue8m0_kv_cache_gb300.build``).
+"""
+import ctypes as C
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libuq.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libuq.so is not built (run python -m ue8m0_kv_cache_gb300.build): %s" % LIB_PATH)
+_lib = C.CDLL(LIB_PATH)
+
+UQ_OK = 0
+FP4_UE8M0, FP8_E4M3, BF16 = 0, 1, 2
+IN_BF16, IN_FP32 = 0, 1
+DEFAULT_SEED = 42
+STATUS_NAMES = {0: "UQ_OK", 1: "UQ_ERR_INVALID_ARG", 2: "UQ_ERR_UNSUPPORTED", 3: "UQ_ERR_ALIGNMENT",
+                4: "UQ_ERR_WORKSPACE", 5: "UQ_ERR_CUDA", 6: "UQ_ERR_DEVICE_TIMEOUT", 7: "UQ_ERR_DEVICE_BOUNDS"}
+
+
+class UqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s returned %s" % (where, STATUS_NAMES.get(status, status)))
+        self.status = status
+
+
+class UqCacheStruct(C.Structure):
+    """Mirror of struct uq_cache."""
+    _fields_ = [("dtype", C.c_int32), ("num_pages", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("page_size", C.c_int32), ("head_dim", C.c_int32),
+                ("k_codes", C.c_void_p), ("k_scales", C.c_void_p), ("v_codes", C.c_void_p),
+                ("v_scales", C.c_void_p), ("k_scale", C.c_float), ("v_scale", C.c_float),
+                ("rot_seed", C.c_uint64)]
+
+
+_vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
+_CP = C.POINTER(UqCacheStruct)
+_sig = {
+    "uq_cache_bytes": (_sz, [_CP, _i32]),
+    "uq_quantize_append": (C.c_int, [_vp, _vp, _i32, _i64, _vp, _i32, _vp, _CP, _vp]),
+    "uq_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "uq_decode_attention": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_decode_attention_fp8": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_decode_attention_bf16": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_check_device_status": (C.c_int, [_vp]),
+    "uq_status_string": (C.c_char_p, [C.c_int]),
+    "uq_rotation_signs": (None, [C.c_uint64, _i32, _vp]),
+    "uq_test_rotate": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _vp, _vp]),
+    "uq_test_quantize_rotated": (C.c_int, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "uq_test_query_fp8": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _vp, _vp]),
+    "uq_test_cvt_e4m3": (C.c_int, [_vp, _i64, _vp, _vp]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = sorted(_sig)
+
+
+def _check(status: int, where: str):
+    if status != UQ_OK:
+        raise UqError(status, where)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name):
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+
+
+class KVCache:
+    """Device memory of one paged cache (torch tensors) plus its uq_cache struct."""
+
+    def __init__(self, dtype: int, num_pages: int, num_kv_heads: int, page_size: int, head_dim: int,
+                 device="cuda", rot_seed: int = DEFAULT_SEED, k_scale: float = 1.0, v_scale: float = 1.0,
+                 fill: Optional[int] = None):
+        self.dtype, self.num_pages, self.num_kv_heads = dtype, num_pages, num_kv_heads
+        self.page_size, self.head_dim = page_size, head_dim
+        shape = (num_pages, num_kv_heads, page_size)
+        alloc = torch.empty if fill is None else (lambda *a, **k: torch.full(*a, fill, **k))
+        if dtype == FP4_UE8M0:
+            self.k_codes = alloc(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
+            self.v_codes = alloc(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
+            self.k_scales = alloc(shape + (head_dim // 32,), dtype=torch.uint8, device=device)
+            self.v_scales = alloc(shape + (head_dim // 32,), dtype=torch.uint8, device=device)
+        else:
+            el = torch.uint8 if dtype == FP8_E4M3 else torch.bfloat16
+            if fill is None or dtype == FP8_E4M3:
+                self.k_codes = alloc(shape + (head_dim,), dtype=el, device=device)
+                self.v_codes = alloc(shape + (head_dim,), dtype=el, device=device)
+            else:
+                self.k_codes = torch.full(shape + (head_dim,), fill, dtype=torch.int16, device=device).view(el)
+                self.v_codes = torch.full(shape + (head_dim,), fill, dtype=torch.int16, device=device).view(el)
+            self.k_scales = self.v_scales = None
+        self.struct = UqCacheStruct(dtype, num_pages, num_kv_heads, page_size, head_dim,
+                                    _ptr(self.k_codes), _ptr(self.k_scales), _ptr(self.v_codes),
+                                    _ptr(self.v_scales), k_scale, v_scale, rot_seed)
+
+    @property
+    def rot_seed(self) -> int:
+        return self.struct.rot_seed
+
+    def nbytes(self) -> int:
+        return sum(uq_cache_bytes(self, w) for w in range(4))
+
+
+def uq_cache_bytes(cache: KVCache, which: int) -> int:
+    return int(_lib.uq_cache_bytes(C.byref(cache.struct), which))
+
+
+def uq_quantize_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, cache: KVCache,
+                       block_table: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantize-append k, v [T][Hkv][D] (bf16 or fp32) into `cache` at slot_mapping [T] (int64)."""
+    if k.dtype not in (torch.bfloat16, torch.float32) or v.dtype != k.dtype:
+        raise ValueError("k, v must both be bf16 or fp32")
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, k.dtype, n)
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    T = k.shape[0]
+    if tuple(k.shape) != (T, cache.num_kv_heads, cache.head_dim) or v.shape != k.shape or slot_mapping.numel() != T:
+        raise ValueError("shape mismatch")
+    mp = 0 if block_table is None else block_table.shape[-1]
+    _check(_lib.uq_quantize_append(_ptr(k), _ptr(v), IN_FP32 if k.dtype == torch.float32 else IN_BF16, T,
+                                   _ptr(block_table), mp, _ptr(slot_mapping), C.byref(cache.struct),
+                                   _stream(stream)), "uq_quantize_append")
+
+
+def uq_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(_lib.uq_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim))
+
+
+def workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, device="cuda") -> torch.Tensor:
+    n = uq_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def _decode(fn, name, q, cache, block_table, seq_lens, out, ws, sm_scale, stream):
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    if D != cache.head_dim or block_table.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    if ws is None:
+        ws = workspace(B, Hq, cache.num_kv_heads, D, q.device)
+    _check(fn(_ptr(q), C.byref(cache.struct), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq,
+              float(sm_scale), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), name)
+    return out
+
+
+def uq_decode_attention(q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0, stream=None):
+    """Decode attention of q [B][Hq][D] bf16 over `cache`; returns fp32 [B][Hq][D]."""
+    return _decode(_lib.uq_decode_attention, "uq_decode_attention", q, cache, block_table, seq_lens, out,
+                   workspace, sm_scale, stream)
+
+
+def uq_decode_attention_fp8(q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0, stream=None):
+    return _decode(_lib.uq_decode_attention_fp8, "uq_decode_attention_fp8", q, cache, block_table, seq_lens,
+                   out, workspace, sm_scale, stream)
+
+
+def uq_decode_attention_bf16(q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0,
+                             stream=None):
+    return _decode(_lib.uq_decode_attention_bf16, "uq_decode_attention_bf16", q, cache, block_table, seq_lens,
+                   out, workspace, sm_scale, stream)
+
+
+def uq_check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(_lib.uq_check_device_status(_stream(stream)))
+
+
+def uq_status_string(status: int) -> str:
+    return _lib.uq_status_string(status).decode()
+
+
+def uq_rotation_signs(seed: int, d: int):
+    buf = (C.c_int8 * d)()
+    _lib.uq_rotation_signs(seed, d, C.cast(buf, C.c_void_p))
+    return list(buf)
+
+
+def uq_test_rotate(x: torch.Tensor, seed: int = DEFAULT_SEED, stream=None) -> torch.Tensor:
+    _need(x, torch.float32, "x")
+    y = torch.empty_like(x)
+    d = x.shape[-1]
+    _check(_lib.uq_test_rotate(_ptr(x), x.numel() // d, d, seed, _ptr(y), _stream(stream)), "uq_test_rotate")
+    return y
+
+
+def uq_test_quantize_rotated(y: torch.Tensor, stream=None):
+    _need(y, torch.float32, "y")
+    d = y.shape[-1]
+    n = y.numel() // d
+    codes = torch.empty(y.shape[:-1] + (d // 2,), dtype=torch.uint8, device=y.device)
+    scales = torch.empty(y.shape[:-1] + (d // 32,), dtype=torch.uint8, device=y.device)
+    _check(_lib.uq_test_quantize_rotated(_ptr(y), n, d, _ptr(codes), _ptr(scales), _stream(stream)),
+           "uq_test_quantize_rotated")
+    return codes, scales
+
+
+def uq_test_query_fp8(q: torch.Tensor, seed: int = DEFAULT_SEED, stream=None) -> torch.Tensor:
+    _need(q, torch.bfloat16, "q")
+    d = q.shape[-1]
+    out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    _check(_lib.uq_test_query_fp8(_ptr(q), q.numel() // d, d, seed, _ptr(out), _stream(stream)),
+           "uq_test_query_fp8")
+    return out
+
+
+def uq_test_cvt_e4m3(x: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(x, torch.float32, "x")
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(_lib.uq_test_cvt_e4m3(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "uq_test_cvt_e4m3")
+    return out

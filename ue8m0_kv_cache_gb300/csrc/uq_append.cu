@@ -1,0 +1,436 @@
+// uq_append.cu -- quantize-append kernels.
+//
+// FP4 path ("UltraQuant" review, manon006.tistory.com/395, §3.1): each K and
+// V row of head_dim values is rotated by the randomised Walsh-Hadamard
+// transform, split into 32-channel groups, given a UE8M0 scale byte from the
+// group absmax times c = 0.156 (§3.3), and coded as E2M1 nibbles, 17 bytes
+// per 32 elements, written into its paged slot.
+//
+// GB300 mapping: one thread owns one row (128 values live in registers, so the
+// whole butterfly needs no shuffles or shared-memory exchange).  Tiles of 64
+// token-head rows of K and of V are brought into shared memory by 2-D TMA
+// copies with the 128-byte swizzle, which makes the per-thread row reads
+// bank-conflict free; a two-stage ring overlaps the next tile's copy with the
+// current tile's arithmetic.  The grid is persistent (a multiple of the SM
+// count).  The kernel is HBM-bound in principle (512 B read and 136 B written
+// per token-head for bf16 input).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "uq_device.cuh"
+#include "uq_internal.h"
+
+namespace {
+
+using namespace uqd;
+
+constexpr int kRows = 64;             // token-head rows per tile
+constexpr int kAppendThreads = 2 * kRows;  // one thread per K row and one per V row
+
+struct AppendParams {
+  const int64_t* slots;
+  int64_t ntok;
+  int hkv;
+  int ps_log2;
+  int64_t num_slots;
+  uint8_t* kc;
+  uint8_t* ks;
+  uint8_t* vc;
+  uint8_t* vs;
+  unsigned int* status;
+  uqh::SignMasks sign;
+};
+
+// Rotation of a register-resident row whose signs were already applied.
+template <int D>
+__device__ __forceinline__ void rotate_regs(float (&u)[D]) {
+  fwht_regs<D>(u);
+  const float c = inv_sqrt_d<D>();
+#pragma unroll
+  for (int i = 0; i < D; i += 2) mul2(u[i], u[i + 1], c);
+}
+
+// Quantiser stage on a rotated row: codes[w] holds bytes 4w..4w+3 of the
+// row's D/2 code bytes, `scales` the D/32 scale bytes (little-endian).
+template <int D>
+__device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D / 8],
+                                              uint32_t& scales) {
+  scales = 0;
+#pragma unroll
+  for (int g = 0; g < D / 32; ++g) {
+    float mx = max_abs_nan(y[32 * g], y[32 * g + 1]);
+#pragma unroll
+    for (int i = 2; i < 32; ++i) mx = max_abs_nan(mx, y[32 * g + i]);
+    const uint32_t byte = scale_byte(fabsf(mx));
+    const float inv = inv_scale(byte == 0xFFu ? 127u : byte);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) mul2(y[32 * g + i], y[32 * g + i + 1], inv);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float* e = &y[32 * g + 8 * w];
+      uint32_t word = cvt_e2m1x2(e[0], e[1]) | (cvt_e2m1x2(e[2], e[3]) << 8) |
+                      (cvt_e2m1x2(e[4], e[5]) << 16) | (cvt_e2m1x2(e[6], e[7]) << 24);
+      codes[4 * g + w] = byte == 0xFFu ? 0u : word;
+    }
+    scales |= byte << (8 * g);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_base, int64_t row,
+                                          const uint32_t (&codes)[D / 8], uint32_t scales) {
+  uint4* cdst = reinterpret_cast<uint4*>(codes_base + row * (D / 2));
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q)
+    cdst[q] = make_uint4(codes[4 * q], codes[4 * q + 1], codes[4 * q + 2], codes[4 * q + 3]);
+  if (D == 128)
+    *reinterpret_cast<uint32_t*>(scales_base + row * 4) = scales;
+  else
+    *reinterpret_cast<uint16_t*>(scales_base + row * 2) = static_cast<uint16_t>(scales);
+}
+
+template <int D, bool F32>
+__global__ void __launch_bounds__(kAppendThreads)
+    fp4_append_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                      const __grid_constant__ AppendParams p) {
+  constexpr int ESZ = F32 ? 4 : 2;
+  constexpr int ROWB = D * ESZ;          // bytes per input row
+  constexpr int NBOX = ROWB / 128;       // 128-byte TMA boxes per row
+  constexpr int BOXE = 128 / ESZ;        // elements per box row
+  constexpr int TILEB = kRows * ROWB;    // one tensor, one stage
+  constexpr int STAGEB = 2 * TILEB;      // K + V
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_flag;
+  // The 128-byte swizzle pattern repeats every 1024 bytes: align the ring.
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int tid = threadIdx.x;
+  const int64_t nrows = p.ntok * p.hkv;
+  const int64_t ntiles = (nrows + kRows - 1) / kRows;
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+
+  auto issue = [&](int64_t tile, int stage) {
+    uint8_t* st = smem + stage * STAGEB;
+    mbar_arrive_expect_tx(&bars[stage], STAGEB);
+    const int y = static_cast<int>(tile * kRows);
+#pragma unroll
+    for (int bx = 0; bx < NBOX; ++bx) {
+      tma_load_2d(st + bx * kRows * 128, &mk, bx * BOXE, y, &bars[stage]);
+      tma_load_2d(st + TILEB + bx * kRows * 128, &mv, bx * BOXE, y, &bars[stage]);
+    }
+  };
+
+  const bool is_v = tid >= kRows;
+  const int row = tid & (kRows - 1);
+  int64_t tile = blockIdx.x;
+  uint32_t it = 0;
+  if (tid == 0 && tile < ntiles) issue(tile, 0);
+  for (; tile < ntiles; tile += gridDim.x, ++it) {
+    const int stage = it & 1;
+    const int64_t next = tile + gridDim.x;
+    if (tid == 0 && next < ntiles) issue(next, stage ^ 1);
+    const bool ok = mbar_wait(&bars[stage], (it >> 1) & 1, kWaitBudget);
+    const int64_t R = tile * kRows + row;
+    if (!ok) {
+      record_error(p.status, kErrTimeout);
+      abort_flag = 1;
+    } else if (R < nrows) {
+      const uint8_t* base = smem + stage * STAGEB + (is_v ? TILEB : 0) + row * 128;
+      float u[D];
+#pragma unroll
+      for (int j = 0; j < ROWB / 16; ++j) {
+        const int bx = j >> 3, cc = j & 7;
+        const uint4 w = *reinterpret_cast<const uint4*>(base + bx * kRows * 128 + ((cc ^ (row & 7)) << 4));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        if (F32) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) u[4 * j + k] = __uint_as_float(ws[k] ^ p.sign.m[4 * j + k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            u[8 * j + 2 * k] = __uint_as_float((ws[k] << 16) ^ p.sign.m[8 * j + 2 * k]);
+            u[8 * j + 2 * k + 1] = __uint_as_float((ws[k] & 0xFFFF0000u) ^ p.sign.m[8 * j + 2 * k + 1]);
+          }
+        }
+      }
+      rotate_regs<D>(u);
+      uint32_t codes[D / 8], scales;
+      quantize_regs<D>(u, codes, scales);
+      const int64_t t = R / p.hkv;
+      const int h = static_cast<int>(R - t * p.hkv);
+      const int64_t slot = p.slots[t];
+      if (slot >= p.num_slots) {
+        record_error(p.status, kErrBounds);
+      } else if (slot >= 0) {
+        const int64_t page = slot >> p.ps_log2;
+        const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
+        store_row<D>(is_v ? p.vc : p.kc, is_v ? p.vs : p.ks, dst, codes, scales);
+      }
+    }
+    __syncthreads();
+    if (abort_flag) {
+      // Let copies that may still be in flight land before the block exits.
+      if (tid == 0) {
+        mbar_wait(&bars[stage], (it >> 1) & 1, kWaitBudget);
+        if (next < ntiles) mbar_wait(&bars[stage ^ 1], ((it + 1) >> 1) & 1, kWaitBudget);
+      }
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------ FP8 / BF16
+struct AnchorParams {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+  int64_t ntok;
+  int hkv;
+  int d;
+  int ps_log2;
+  int64_t num_slots;
+  int fp8;  // 1: e4m3(x / scale), 0: bf16
+  int in_fp32;
+  float k_scale, v_scale;
+  uint8_t* kc;
+  uint8_t* vc;
+  unsigned int* status;
+};
+
+// One thread per 8 consecutive elements of one row of K or V.
+__global__ void __launch_bounds__(256) anchor_append_kernel(const __grid_constant__ AnchorParams p) {
+  const int per_row = p.d / 8;
+  const int64_t nrows = p.ntok * p.hkv;
+  const int64_t total = 2 * nrows * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int is_v = i >= nrows * per_row;
+    const int64_t j = is_v ? i - nrows * per_row : i;
+    const int64_t R = j / per_row;
+    const int chunk = static_cast<int>(j - R * per_row);
+    const int64_t t = R / p.hkv;
+    const int h = static_cast<int>(R - t * p.hkv);
+    const int64_t slot = p.slots[t];
+    if (slot < 0) continue;
+    if (slot >= p.num_slots) {
+      record_error(p.status, kErrBounds);
+      continue;
+    }
+    float x[8];
+    const void* src = is_v ? p.v : p.k;
+    if (p.in_fp32) {
+      const float4* s4 = reinterpret_cast<const float4*>(static_cast<const float*>(src) + R * p.d + chunk * 8);
+      const float4 a = s4[0], b = s4[1];
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+      const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + R * p.d + chunk * 8);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(ws[k] << 16);
+        x[2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+      }
+    }
+    const int64_t page = slot >> p.ps_log2;
+    const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
+    uint8_t* base = is_v ? p.vc : p.kc;
+    if (p.fp8) {
+      const float sc = is_v ? p.v_scale : p.k_scale;
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        lo |= cvt_e4m3x2(__fdiv_rn(x[k], sc), __fdiv_rn(x[k + 1], sc)) << (8 * k);
+        hi |= cvt_e4m3x2(__fdiv_rn(x[4 + k], sc), __fdiv_rn(x[5 + k], sc)) << (8 * k);
+      }
+      *reinterpret_cast<uint2*>(base + dst * p.d + chunk * 8) = make_uint2(lo, hi);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(base + (dst * p.d + chunk * 8) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------ test kernels
+template <int D>
+__global__ void test_rotate_kernel(const float* x, int64_t n, float* y, const __grid_constant__ uqh::SignMasks sm) {
+  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  float u[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) u[i] = __uint_as_float(__float_as_uint(x[r * D + i]) ^ sm.m[i]);
+  rotate_regs<D>(u);
+#pragma unroll
+  for (int i = 0; i < D; ++i) y[r * D + i] = u[i];
+}
+
+template <int D>
+__global__ void test_quantize_kernel(const float* y, int64_t n, uint8_t* codes, uint8_t* scales) {
+  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  float u[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) u[i] = y[r * D + i];
+  uint32_t c[D / 8], s;
+  quantize_regs<D>(u, c, s);
+  store_row<D>(codes, scales, r, c, s);
+}
+
+__global__ void test_cvt_e4m3_kernel(const float* x, int64_t n2, uint16_t* out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i < n2) out[i] = static_cast<uint16_t>(cvt_e4m3x2(x[2 * i], x[2 * i + 1]));
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Rows of `row_elems` elements, boxes of 128 bytes x kRows rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int row_elems, bool f32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kRows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool F32>
+uq_status run_fp4_append(const CUtensorMap& mk, const CUtensorMap& mv, const AppendParams& p, int64_t nrows,
+                         cudaStream_t s) {
+  constexpr int STAGEB = 2 * kRows * D * (F32 ? 4 : 2);
+  constexpr size_t smem = 2 * STAGEB + 1024;
+  auto kern = fp4_append_kernel<D, F32>;
+  static int configured_dev = -1;  // attribute is per device; re-set when the device changes
+  const uqh::DevInfo& di = uqh::dev_info();
+  if (configured_dev != di.device) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return UQ_ERR_CUDA;
+    configured_dev = di.device;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAppendThreads, smem) != cudaSuccess ||
+      per_sm < 1)
+    return UQ_ERR_CUDA;
+  const int64_t ntiles = (nrows + kRows - 1) / kRows;
+  const int64_t grid = std::min<int64_t>(ntiles, (int64_t)di.sms * per_sm);
+  kern<<<(unsigned)grid, kAppendThreads, smem, s>>>(mk, mv, p);
+  return uqh::cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+namespace uqh {
+
+uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t ntok, const int64_t* slots,
+                            const uq_cache& c, cudaStream_t s) {
+  const int64_t nrows = ntok * c.num_kv_heads;
+  if (nrows >= (int64_t(1) << 31) - kRows) return UQ_ERR_UNSUPPORTED;
+  CUtensorMap mk, mv;
+  if (!encode_rows(&mk, k, nrows, c.head_dim, in_fp32) || !encode_rows(&mv, v, nrows, c.head_dim, in_fp32))
+    return UQ_ERR_CUDA;
+  AppendParams p;
+  p.slots = slots;
+  p.ntok = ntok;
+  p.hkv = c.num_kv_heads;
+  p.ps_log2 = ilog2(c.page_size);
+  p.num_slots = (int64_t)c.num_pages * c.page_size;
+  p.kc = static_cast<uint8_t*>(c.k_codes);
+  p.ks = static_cast<uint8_t*>(c.k_scales);
+  p.vc = static_cast<uint8_t*>(c.v_codes);
+  p.vs = static_cast<uint8_t*>(c.v_scales);
+  p.status = status_word();
+  make_sign_masks(c.rot_seed, c.head_dim, &p.sign);
+  if (!p.status) return UQ_ERR_CUDA;
+  if (c.head_dim == 128)
+    return in_fp32 ? run_fp4_append<128, true>(mk, mv, p, nrows, s) : run_fp4_append<128, false>(mk, mv, p, nrows, s);
+  return in_fp32 ? run_fp4_append<64, true>(mk, mv, p, nrows, s) : run_fp4_append<64, false>(mk, mv, p, nrows, s);
+}
+
+uq_status launch_append_anchor(const void* k, const void* v, bool in_fp32, int64_t ntok, const int64_t* slots,
+                               const uq_cache& c, cudaStream_t s) {
+  AnchorParams p;
+  p.k = k;
+  p.v = v;
+  p.slots = slots;
+  p.ntok = ntok;
+  p.hkv = c.num_kv_heads;
+  p.d = c.head_dim;
+  p.ps_log2 = ilog2(c.page_size);
+  p.num_slots = (int64_t)c.num_pages * c.page_size;
+  p.fp8 = c.dtype == UQ_FP8_E4M3;
+  p.in_fp32 = in_fp32;
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.kc = static_cast<uint8_t*>(c.k_codes);
+  p.vc = static_cast<uint8_t*>(c.v_codes);
+  p.status = status_word();
+  if (!p.status) return UQ_ERR_CUDA;
+  const int64_t work = 2 * ntok * c.num_kv_heads * (c.head_dim / 8);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, (int64_t)dev_info().sms * 8));
+  anchor_append_kernel<<<(unsigned)grid, 256, 0, s>>>(p);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y, cudaStream_t s) {
+  SignMasks sm;
+  make_sign_masks(seed, d, &sm);
+  const unsigned grid = (unsigned)((n + 127) / 128);
+  if (d == 128)
+    test_rotate_kernel<128><<<grid, 128, 0, s>>>(x, n, y, sm);
+  else
+    test_rotate_kernel<64><<<grid, 128, 0, s>>>(x, n, y, sm);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s) {
+  const unsigned grid = (unsigned)((n + 127) / 128);
+  if (d == 128)
+    test_quantize_kernel<128><<<grid, 128, 0, s>>>(y, n, codes, scales);
+  else
+    test_quantize_kernel<64><<<grid, 128, 0, s>>>(y, n, codes, scales);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t s) {
+  const int64_t n2 = n / 2;
+  test_cvt_e4m3_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, s>>>(x, n2, reinterpret_cast<uint16_t*>(out));
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace uqh

@@ -1,0 +1,742 @@
+// uq_decode.cu -- decode attention straight from the paged cache.
+//
+// The FP4 path follows "UltraQuant: 4-bit KV Caching for Context-Heavy
+// Agents" (review, manon006.tistory.com/395): §3.2 the query is rotated into
+// the key basis and rounded to FP8 E4M3, keys and values are consumed as
+// E2M1 codes with UE8M0 group scales (value = code * 2^(byte-127)) and are
+// never materialised as BF16 in memory; §4.2 the query is rounded once,
+// outside the key-tile loop.  The output is rotated back (the rotation is
+// orthogonal, "TurboQuant 완전 정리", inner-product preservation).
+//
+// GB300 design
+//   * Work unit = 16 tokens of one (sequence, kv head, block of <= 8 query
+//     heads).  All units of the batch are laid end to end and cut into equal
+//     contiguous ranges, one per block of a persistent grid sized to the SMs,
+//     so mixed sequence lengths stay balanced.  Each block writes one partial
+//     (running max, sum, unnormalised output) per (sequence, kv head) range it
+//     touches; a small merge kernel combines them by log-sum-exp and applies
+//     the inverse rotation.
+//   * Each of the 4 warps of a block streams its own units through a ring of
+//     shared-memory stages filled by 1-D bulk copies (TMA engine) on mbarriers:
+//     one unit = 16 rows of K codes, V codes and their scale bytes
+//     (2176 bytes for head_dim 128), 136 bytes per token-head.
+//   * QK^T and P.V run on the tensor cores with warp-level m16n8k16 f16 MMAs
+//     whose operands are built in registers: E2M1 pairs go through the
+//     hardware e2m1x2 -> f16x2 conversion, group scales 2^(E-R) are applied
+//     with one packed half multiply (R = the largest exponent of the tile, so
+//     every value fits f16), and the accumulators are fp32.  Keeping operands
+//     in registers avoids a second trip through shared memory, which at
+//     n = 8 query heads would otherwise cap the kernel below HBM speed.
+//   * Sums over the head dimension do not depend on the order of channels,
+//     so the channel-to-fragment mapping is chosen to make every thread's
+//     operands contiguous bytes of one 32-channel group.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "uq_device.cuh"
+#include "uq_internal.h"
+
+namespace {
+
+using namespace uqd;
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kHB = 8;  // query heads per block (the MMA's n)
+constexpr int kChunk = 16;  // tokens per work unit (the MMA's m for QK)
+
+enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
+
+template <int KIND, int D>
+struct DC {
+  static constexpr int KROW = KIND == kFP4 ? D / 2 : (KIND == kFP8 ? D : 2 * D);  // bytes/token row
+  static constexpr int SROW = KIND == kFP4 ? D / 32 : 0;                         // scale bytes/token
+  static constexpr int KBYTES = kChunk * KROW;
+  static constexpr int SBYTES = kChunk * SROW;
+  static constexpr int STAGE = 2 * KBYTES + 2 * SBYTES;
+  static constexpr int NST = KIND == kFP4 ? 4 : 3;  // ring depth per warp
+  static constexpr int NMMA = D / 16;               // k-steps of QK, m-blocks of PV
+  static constexpr int CPT = D / 4;                 // QK channels per thread and token
+  static constexpr int VPT = D / 8;                 // PV channels per thread and token
+  static constexpr size_t smem_fixed = (size_t)kWarps * NST * STAGE + (size_t)kWarps * NST * 8 +
+                                       (size_t)kWarps * kHB * 2 * 4 + (size_t)kWarps * kHB * D * 4;
+};
+
+struct DecParams {
+  const uint16_t* q;
+  const uint8_t* kc;
+  const uint8_t* ks;
+  const uint8_t* vc;
+  const uint8_t* vs;
+  float k_scale, v_scale;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int B, Hq, Hkv, G, nhb, ps_log2, num_pages;
+  float sl2e;  // softmax scale * log2(e)
+  float* ws_o;
+  float* ws_ml;
+  int32_t* ws_info;
+  unsigned int* status;
+  uqh::SignMasks sign;
+};
+
+__device__ __forceinline__ float pow2i(int e) {  // 2^e for e in [-149, 127], 0 below
+  if (e >= -126) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  if (e >= -149) return __uint_as_float(1u << (e + 149));
+  return 0.f;
+}
+
+// f16 multiplier for a group scale byte relative to the tile reference R:
+// 2^(byte-R) (<= 1), 0 for masked tokens, NaN for a non-finite group.
+__device__ __forceinline__ float group_mult(uint32_t byte, uint32_t R, bool valid) {
+  if (!valid) return 0.f;
+  if (byte == 0xFFu) return __int_as_float(0x7FC00000);
+  return pow2i(static_cast<int>(byte) - static_cast<int>(R));
+}
+
+__device__ __forceinline__ int clamp_len(const DecParams& p, int b) {
+  const int cap = p.max_pages << p.ps_log2;
+  int L = p.seq_lens[b];
+  if (L < 0 || L > cap) {
+    record_error(p.status, kErrBounds);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+// The rotated E4M3 query of head row `r` of the block, channels
+// [c*CPT, (c+1)*CPT), returned as f16x2 B fragments (FP4) -- the same fp32
+// butterfly as the append path, spread over the 4 threads of a quad: strides
+// below CPT inside a thread, the last two strides across the quad.
+template <int D>
+__device__ __forceinline__ void rotated_query_fp8(const uint16_t* qrow, bool valid, int c, const DecParams& p,
+                                                  uint32_t (&qb)[D / 16][2], uint8_t* bytes_out) {
+  constexpr int CPT = D / 4;
+  float x[CPT];
+#pragma unroll
+  for (int e = 0; e < CPT; e += 2) {
+    uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(qrow + c * CPT + e) : 0u;
+    x[e] = __uint_as_float((w << 16) ^ p.sign.m[c * CPT + e]);
+    x[e + 1] = __uint_as_float((w & 0xFFFF0000u) ^ p.sign.m[c * CPT + e + 1]);
+  }
+  fwht_regs<CPT>(x);
+#pragma unroll
+  for (int k = 1; k <= 2; k <<= 1) {
+    const bool upper = (c & k) != 0;
+#pragma unroll
+    for (int e = 0; e < CPT; ++e) {
+      const float o = __shfl_xor_sync(kFull, x[e], k);
+      x[e] = upper ? (o - x[e]) : (x[e] + o);
+    }
+  }
+  const float s = inv_sqrt_d<D>();
+#pragma unroll
+  for (int e = 0; e < CPT; e += 2) mul2(x[e], x[e + 1], s);
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) {
+    const uint32_t b01 = cvt_e4m3x2(x[4 * m], x[4 * m + 1]);
+    const uint32_t b23 = cvt_e4m3x2(x[4 * m + 2], x[4 * m + 3]);
+    qb[m][0] = e4m3x2_to_f16x2(b01);
+    qb[m][1] = e4m3x2_to_f16x2(b23);
+    if (bytes_out) *reinterpret_cast<uint32_t*>(bytes_out + 4 * m) = b01 | (b23 << 16);
+  }
+}
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DC<KIND, D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * C::NST * C::STAGE);
+  float* comb_ml = reinterpret_cast<float*>(bars + kWarps * C::NST);
+  float* comb_o = comb_ml + kWarps * kHB * 2;
+  int* pre = reinterpret_cast<int*>(comb_o + kWarps * kHB * D);
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, c = lane & 3;
+  const int ps_mask = (1 << p.ps_log2) - 1;
+
+  // Prefix sums of 16-token units per sequence.
+  if (warp == 0) {
+    int run = 0;
+    if (lane == 0) pre[0] = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int x = b < p.B ? (clamp_len(p, b) + kChunk - 1) / kChunk : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < p.B) pre[b + 1] = run + x;
+      run += __shfl_sync(kFull, x, 31);
+    }
+  }
+  uint64_t* mybars = bars + warp * C::NST;
+  uint8_t* myring = ring + warp * C::NST * C::STAGE;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) abort_flag = 0;
+  __syncthreads();
+
+  const int pps = p.Hkv * p.nhb;  // (kv head, head block) pairs per sequence
+  const int64_t U = static_cast<int64_t>(pre[p.B]) * pps;
+  const int64_t lo = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
+  const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+  uint32_t it = 0;  // position in this warp's ring, carried across segments
+
+  for (int64_t u = lo; u < hi;) {
+    // Segment: the units of one (sequence, kv head, head block) inside [u, hi).
+    int lb = 1, hb_ = p.B;  // first index with pre[idx] * pps > u, in [1, B]
+    while (lb < hb_) {
+      const int mid = (lb + hb_) >> 1;
+      if (static_cast<int64_t>(pre[mid]) * pps > u) hb_ = mid; else lb = mid + 1;
+    }
+    const int b = lb - 1;
+    const int nb = pre[b + 1] - pre[b];
+    const int64_t off = u - static_cast<int64_t>(pre[b]) * pps;
+    const int pl = static_cast<int>(off / nb);
+    const int j0 = static_cast<int>(off - static_cast<int64_t>(pl) * nb);
+    const int seg = static_cast<int>((nb - j0) < (hi - u) ? (nb - j0) : (hi - u));
+    const int kvh = pl / p.nhb, hblk = pl - kvh * p.nhb;
+    const int pair = b * pps + pl;
+    const int L = clamp_len(p, b);
+
+    // Query fragments (once per segment, outside the unit loop).
+    uint32_t qb[C::NMMA][2];
+    {
+      const int hloc = hblk * kHB + r;
+      const bool hv = hloc < p.G;
+      const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (hv ? hloc : 0)) * D;
+      if (KIND == kFP4) {
+        rotated_query_fp8<D>(qrow, hv, c, p, qb, nullptr);
+      } else {
+#pragma unroll
+        for (int m = 0; m < C::NMMA; ++m) {
+          const uint32_t w0 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m) : 0u;
+          const uint32_t w1 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m + 2) : 0u;
+          if (KIND == kBF16) {
+            qb[m][0] = w0;
+            qb[m][1] = w1;
+          } else {  // bf16 -> f16 (exact for |q| in the f16 normal range)
+            qb[m][0] = pack_f16x2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+            qb[m][1] = pack_f16x2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+          }
+        }
+      }
+    }
+
+    const int nw = seg > warp ? (seg - warp + kWarps - 1) / kWarps : 0;
+    auto issue = [&](int i, int slot) {
+      const int tok0 = (j0 + warp + i * kWarps) * kChunk;
+      int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + (tok0 >> p.ps_log2)];
+      if (page < 0 || page >= p.num_pages) {
+        record_error(p.status, kErrBounds);
+        page = 0;
+      }
+      const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
+      uint8_t* st = myring + slot * C::STAGE;
+      uint64_t* bar = &mybars[slot];
+      mbar_arrive_expect_tx(bar, C::STAGE);
+      bulk_g2s(st, p.kc + row0 * C::KROW, C::KBYTES, bar);
+      bulk_g2s(st + C::KBYTES, p.vc + row0 * C::KROW, C::KBYTES, bar);
+      if (KIND == kFP4) {
+        bulk_g2s(st + 2 * C::KBYTES, p.ks + row0 * C::SROW, C::SBYTES, bar);
+        bulk_g2s(st + 2 * C::KBYTES + C::SBYTES, p.vs + row0 * C::SROW, C::SBYTES, bar);
+      }
+    };
+    if (lane == 0)
+      for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST);
+
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float O[C::NMMA][4];
+#pragma unroll
+    for (int m = 0; m < C::NMMA; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
+    uint32_t RV = 0;  // FP4: reference exponent byte of the V accumulator
+
+    for (int i = 0; i < nw; ++i, ++it) {
+      const int slot = it % C::NST;
+      const bool ok = __all_sync(kFull, mbar_wait(&mybars[slot], (it / C::NST) & 1, kWaitBudget));
+      if (!ok) {
+        if (lane == 0) {
+          record_error(p.status, kErrTimeout);
+          for (int k = i + 1; k < (nw < i + C::NST ? nw : i + C::NST); ++k)
+            mbar_wait(&mybars[(it + k - i) % C::NST], ((it + k - i) / C::NST) & 1, kWaitBudget);
+        }
+        abort_flag = 1;
+        it += nw - i;
+        break;
+      }
+      const uint8_t* st = myring + slot * C::STAGE;
+      const uint8_t* skc = st;
+      const uint8_t* svc = st + C::KBYTES;
+      const int rem = L - (j0 + warp + i * kWarps) * kChunk;
+      const int nvalid = rem < kChunk ? rem : kChunk;
+      const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+
+      // ---------------------------------------------------------------- QK^T
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      float fac = p.sl2e;
+      if (KIND == kFP4) {
+        constexpr int KB = C::CPT / 2;  // code bytes per thread and token
+        const uint8_t* sks = st + 2 * C::KBYTES;
+        uint32_t kw0[KB / 4], kw1[KB / 4];
+        {
+          const uint32_t* a0 = reinterpret_cast<const uint32_t*>(skc + r * C::KROW + c * KB);
+          const uint32_t* a1 = reinterpret_cast<const uint32_t*>(skc + (r + 8) * C::KROW + c * KB);
+          if (KB == 16) {
+            const uint4 x0 = *reinterpret_cast<const uint4*>(a0), x1 = *reinterpret_cast<const uint4*>(a1);
+            kw0[0] = x0.x; kw0[1] = x0.y; kw0[2] = x0.z; kw0[3] = x0.w;
+            kw1[0] = x1.x; kw1[1] = x1.y; kw1[2] = x1.z; kw1[3] = x1.w;
+          } else {
+            const uint2 x0 = *reinterpret_cast<const uint2*>(a0), x1 = *reinterpret_cast<const uint2*>(a1);
+            kw0[0] = x0.x; kw0[1] = x0.y;
+            kw1[0] = x1.x; kw1[1] = x1.y;
+          }
+        }
+        const int gk = (c * C::CPT) >> 5;
+        const uint32_t kb0 = sks[r * C::SROW + gk], kb1 = sks[(r + 8) * C::SROW + gk];
+        const uint32_t e0 = (v0 && kb0 != 0xFFu) ? kb0 : 0u, e1 = (v1 && kb1 != 0xFFu) ? kb1 : 0u;
+        const uint32_t RK = __reduce_max_sync(kFull, e0 > e1 ? e0 : e1);
+        const float f0 = group_mult(kb0, RK, v0), f1 = group_mult(kb1, RK, v1);
+        const uint32_t mk0 = pack_f16x2(f0, f0), mk1 = pack_f16x2(f1, f1);
+#pragma unroll
+        for (int w = 0; w < KB / 4; ++w) {
+          uint32_t h0[4], h1[4];
+          e2m1x8_to_f16x2(kw0[w], h0);
+          e2m1x8_to_f16x2(kw1[w], h1);
+          mma_f16(sacc, hmul2(h0[0], mk0), hmul2(h1[0], mk1), hmul2(h0[1], mk0), hmul2(h1[1], mk1),
+                  qb[2 * w][0], qb[2 * w][1]);
+          mma_f16(sacc, hmul2(h0[2], mk0), hmul2(h1[2], mk1), hmul2(h0[3], mk0), hmul2(h1[3], mk1),
+                  qb[2 * w + 1][0], qb[2 * w + 1][1]);
+        }
+        fac = __fmul_rn(p.sl2e, pow2i(static_cast<int>(RK) - 127));
+      } else if (KIND == kFP8) {
+        const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT);
+        const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT);
+#pragma unroll
+        for (int q4 = 0; q4 < C::CPT / 16; ++q4) {
+          const uint4 x0 = a0[q4], x1 = a1[q4];
+          const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int m = 4 * q4 + k;
+            mma_f16(sacc, e4m3x2_to_f16x2(w0[k]), e4m3x2_to_f16x2(w1[k]), e4m3x2_to_f16x2(w0[k] >> 16),
+                    e4m3x2_to_f16x2(w1[k] >> 16), qb[m][0], qb[m][1]);
+          }
+        }
+        fac = p.sl2e * p.k_scale;
+      } else {
+        const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT * 2);
+        const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT * 2);
+#pragma unroll
+        for (int q4 = 0; q4 < C::CPT / 8; ++q4) {
+          const uint4 x0 = a0[q4], x1 = a1[q4];
+          mma_bf16(sacc, x0.x, x1.x, x0.y, x1.y, qb[2 * q4][0], qb[2 * q4][1]);
+          mma_bf16(sacc, x0.z, x1.z, x0.w, x1.w, qb[2 * q4 + 1][0], qb[2 * q4 + 1][1]);
+        }
+      }
+      const float s0 = v0 ? sacc[0] * fac : -INFINITY, s1 = v0 ? sacc[1] * fac : -INFINITY;
+      const float s2 = v1 ? sacc[2] * fac : -INFINITY, s3 = v1 ? sacc[3] * fac : -INFINITY;
+
+      // ----------------------------------------------------- online softmax
+      float mc0 = fmaxf(s0, s2), mc1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+        mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+      }
+      if (__any_sync(kFull, mc0 > M0 || mc1 > M1)) {
+        const float n0 = fmaxf(M0, mc0), n1 = fmaxf(M1, mc1);
+        const float a0 = ex2(M0 - n0), a1 = ex2(M1 - n1);
+        M0 = n0;
+        M1 = n1;
+        L0 *= a0;
+        L1 *= a1;
+#pragma unroll
+        for (int m = 0; m < C::NMMA; ++m) {
+          O[m][0] *= a0; O[m][1] *= a1; O[m][2] *= a0; O[m][3] *= a1;
+        }
+      }
+      const float p0 = ex2(s0 - M0), p1 = ex2(s1 - M1), p2 = ex2(s2 - M0), p3 = ex2(s3 - M1);
+      L0 += p0 + p2;
+      L1 += p1 + p3;
+      // P^T fragments: rows = tokens, cols = heads -> transpose to k = tokens.
+      const uint32_t B0 = movmatrix_trans(pack_f16x2(p0, p1));
+      const uint32_t B1 = movmatrix_trans(pack_f16x2(p2, p3));
+
+      // ------------------------------------------------------------- P.V
+      const int t0 = 2 * c, t1 = 2 * c + 1, t8 = 2 * c + 8, t9 = 2 * c + 9;
+      const bool vt0 = t0 < nvalid, vt1 = t1 < nvalid, vt8 = t8 < nvalid, vt9 = t9 < nvalid;
+      if (KIND == kFP4) {
+        constexpr int VB = C::VPT / 2;  // code bytes per thread and token
+        const uint8_t* svs = st + 2 * C::KBYTES + C::SBYTES;
+        uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
+#pragma unroll
+        for (int q4 = 0; q4 < VB / 4; ++q4) {
+          w0[q4] = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
+          w1[q4] = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
+          w8[q4] = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
+          w9[q4] = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
+        }
+        const int gv = (r * C::VPT) >> 5;
+        const uint32_t b0 = svs[t0 * C::SROW + gv], b1 = svs[t1 * C::SROW + gv];
+        const uint32_t b8 = svs[t8 * C::SROW + gv], b9 = svs[t9 * C::SROW + gv];
+        uint32_t ev = 0;
+        ev = (vt0 && b0 != 0xFFu && b0 > ev) ? b0 : ev;
+        ev = (vt1 && b1 != 0xFFu && b1 > ev) ? b1 : ev;
+        ev = (vt8 && b8 != 0xFFu && b8 > ev) ? b8 : ev;
+        ev = (vt9 && b9 != 0xFFu && b9 > ev) ? b9 : ev;
+        const uint32_t RVc = __reduce_max_sync(kFull, ev);
+        if (RVc > RV) {
+          const float f = pow2i(static_cast<int>(RV) - static_cast<int>(RVc));
+#pragma unroll
+          for (int m = 0; m < C::NMMA; ++m) {
+            O[m][0] *= f; O[m][1] *= f; O[m][2] *= f; O[m][3] *= f;
+          }
+          RV = RVc;
+        }
+        const uint32_t mv01 = pack_f16x2(group_mult(b0, RV, vt0), group_mult(b1, RV, vt1));
+        const uint32_t mv89 = pack_f16x2(group_mult(b8, RV, vt8), group_mult(b9, RV, vt9));
+#pragma unroll
+        for (int q4 = 0; q4 < VB / 4; ++q4) {
+          // Pair the same channel of two tokens in one byte (low nibble = lower token).
+          const uint32_t lo01 = (w0[q4] & 0x0F0F0F0Fu) | ((w1[q4] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi01 = ((w0[q4] >> 4) & 0x0F0F0F0Fu) | (w1[q4] & 0xF0F0F0F0u);
+          const uint32_t lo89 = (w8[q4] & 0x0F0F0F0Fu) | ((w9[q4] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi89 = ((w8[q4] >> 4) & 0x0F0F0F0Fu) | (w9[q4] & 0xF0F0F0F0u);
+          uint32_t A0[4], A1[4], A2[4], A3[4];
+          e2m1x8_to_f16x2(lo01, A0);
+          e2m1x8_to_f16x2(hi01, A1);
+          e2m1x8_to_f16x2(lo89, A2);
+          e2m1x8_to_f16x2(hi89, A3);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89),
+                    hmul2(A3[k], mv89), B0, B1);
+        }
+      } else if (KIND == kFP8) {
+        constexpr int VB = C::VPT;  // bytes per thread and token
+        uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
+#pragma unroll
+        for (int q4 = 0; q4 < VB / 4; ++q4) {
+          w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4] : 0u;
+          w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4] : 0u;
+          w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4] : 0u;
+          w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4] : 0u;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < VB / 4; ++q4) {
+          const uint32_t x01 = __byte_perm(w0[q4], w1[q4], 0x5140), y01 = __byte_perm(w0[q4], w1[q4], 0x7362);
+          const uint32_t x89 = __byte_perm(w8[q4], w9[q4], 0x5140), y89 = __byte_perm(w8[q4], w9[q4], 0x7362);
+          mma_f16(O[2 * q4], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(x89),
+                  e4m3x2_to_f16x2(x89 >> 16), B0, B1);
+          mma_f16(O[2 * q4 + 1], e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16), e4m3x2_to_f16x2(y89),
+                  e4m3x2_to_f16x2(y89 >> 16), B0, B1);
+        }
+      } else {
+        constexpr int VW = C::VPT / 2;  // bf16 pairs per thread and token
+        uint32_t w0[VW], w1[VW], w8[VW], w9[VW];
+#pragma unroll
+        for (int q4 = 0; q4 < VW; ++q4) {
+          w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+          w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+          w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+          w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+        }
+        auto bf2h = [](uint32_t w) {  // bf16x2 -> f16x2
+          return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        };
+#pragma unroll
+        for (int m = 0; m < VW; ++m) {
+          mma_f16(O[m], bf2h(__byte_perm(w0[m], w1[m], 0x5410)), bf2h(__byte_perm(w0[m], w1[m], 0x7632)),
+                  bf2h(__byte_perm(w8[m], w9[m], 0x5410)), bf2h(__byte_perm(w8[m], w9[m], 0x7632)), B0, B1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && i + C::NST < nw) {
+        fence_proxy_async();
+        issue(i + C::NST, slot);
+      }
+    }
+
+    // ---------------------------------------------- combine the 4 warps
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      L0 += __shfl_xor_sync(kFull, L0, o);
+      L1 += __shfl_xor_sync(kFull, L1, o);
+    }
+    if (r == 0) {
+      comb_ml[(warp * kHB + 2 * c) * 2] = M0;
+      comb_ml[(warp * kHB + 2 * c) * 2 + 1] = L0;
+      comb_ml[(warp * kHB + 2 * c + 1) * 2] = M1;
+      comb_ml[(warp * kHB + 2 * c + 1) * 2 + 1] = L1;
+    }
+    const float osc = KIND == kFP4 ? pow2i(static_cast<int>(RV) - 127) : (KIND == kFP8 ? p.v_scale : 1.f);
+    {
+      float* co = comb_o + warp * kHB * D;
+#pragma unroll
+      for (int m = 0; m < C::NMMA; ++m) {
+        const int ch0 = r * C::VPT + 2 * m, ch1 = ch0 + 1;
+        co[(2 * c) * D + ch0] = O[m][0] * osc;
+        co[(2 * c + 1) * D + ch0] = O[m][1] * osc;
+        co[(2 * c) * D + ch1] = O[m][2] * osc;
+        co[(2 * c + 1) * D + ch1] = O[m][3] * osc;
+      }
+    }
+    __syncthreads();
+    {
+      const int h = tid >> 4;  // 8 heads x 16 threads
+      constexpr int PER = D / 16;
+      const int ch = (tid & 15) * PER;
+      float Ms = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) Ms = fmaxf(Ms, comb_ml[(w * kHB + h) * 2]);
+      float wt[kWarps], Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        wt[w] = ex2(comb_ml[(w * kHB + h) * 2] - Ms);
+        Ls += wt[w] * comb_ml[(w * kHB + h) * 2 + 1];
+      }
+      const int64_t slot_id = static_cast<int64_t>(blockIdx.x) + pair;
+      float* dst = p.ws_o + (slot_id * kHB + h) * D + ch;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) acc += wt[w] * comb_o[(w * kHB + h) * D + ch + e];
+        dst[e] = acc;
+      }
+      if ((tid & 15) == 0) {
+        p.ws_ml[(slot_id * kHB + h) * 2] = Ms;
+        p.ws_ml[(slot_id * kHB + h) * 2 + 1] = Ls;
+      }
+      if (tid == 0) {
+        if (j0 == 0) p.ws_info[2 * pair] = blockIdx.x;
+        if (j0 + seg == nb) p.ws_info[2 * pair + 1] = blockIdx.x;
+      }
+    }
+    __syncthreads();
+    if (abort_flag) break;
+    u += seg;
+  }
+}
+
+// Log-sum-exp merge of the partials of each (sequence, query head), then the
+// inverse rotation (FP4).  One warp per output row.
+struct MergeParams {
+  const float* ws_o;
+  const float* ws_ml;
+  const int32_t* ws_info;
+  const int32_t* seq_lens;
+  int B, Hq, Hkv, G, nhb, cap, num_ctas;
+  float* out;
+  unsigned int* status;
+  uqh::SignMasks sign;
+};
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= static_cast<int64_t>(p.B) * p.Hq) return;
+  const int b = static_cast<int>(row / p.Hq), h = static_cast<int>(row - static_cast<int64_t>(b) * p.Hq);
+  int L = p.seq_lens[b];
+  L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+  float o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+  if (L > 0) {
+    const int kvh = h / p.G, hl = h - kvh * p.G, hb = hl / kHB, hh = hl - hb * kHB;
+    const int pair = (b * p.Hkv + kvh) * p.nhb + hb;
+    int first = p.ws_info[2 * pair], last = p.ws_info[2 * pair + 1];
+    if (first < 0 || last < first || last >= p.num_ctas) {  // never written: a decode block gave up
+      record_error(p.status, kErrTimeout);
+      first = 1;
+      last = 0;
+    }
+    float Ms = -INFINITY;
+    for (int s = first; s <= last; ++s) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
+    float Ls = 0.f;
+    for (int s = first; s <= last; ++s) {
+      const int64_t id = (int64_t)(s + pair) * kHB + hh;
+      const float w = ex2(p.ws_ml[id * 2] - Ms);
+      Ls += w * p.ws_ml[id * 2 + 1];
+      const float* src = p.ws_o + id * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[e] += w * src[e];
+    }
+    const float inv = 1.f / Ls;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= inv;
+    if (KIND == kFP4) {
+      // inverse rotation: s .* (H o) / sqrt(D); strides below EPL in-thread,
+      // the rest across lanes.
+#pragma unroll
+      for (int hs = 1; hs < EPL; hs <<= 1)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          if ((e & hs) == 0) {
+            const float a = o[e], bb = o[e + hs];
+            o[e] = a + bb;
+            o[e + hs] = a - bb;
+          }
+#pragma unroll
+      for (int k = 1; k < 32; k <<= 1) {
+        const bool upper = (lane & k) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float x = __shfl_xor_sync(kFull, o[e], k);
+          o[e] = upper ? (x - o[e]) : (o[e] + x);
+        }
+      }
+      const float sc = inv_sqrt_d<D>();
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        o[e] = __uint_as_float(__float_as_uint(o[e] * sc) ^ p.sign.m[lane * EPL + e]);
+    }
+  }
+  float* dst = p.out + row * D + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) dst[e] = o[e];
+}
+
+// Test hook: the decode prologue alone.  One warp handles 8 query rows.
+template <int D>
+__global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out, const __grid_constant__ uqh::SignMasks sm) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8 + r;
+  DecParams p;
+  p.sign = sm;
+  uint32_t qb[D / 16][2];
+  uint8_t bytes[D / 4];
+  const bool valid = row < n;
+  rotated_query_fp8<D>(q + (valid ? row : 0) * D, valid, c, p, qb, bytes);
+  if (valid)
+    for (int e = 0; e < D / 4; ++e) out[row * D + c * (D / 4) + e] = bytes[e];
+}
+
+// ------------------------------------------------------------------ host
+size_t ws_slot_bytes(int d) { return static_cast<size_t>(kHB) * (d + 2) * sizeof(float); }
+size_t ws_info_bytes(int pairs) { return ((static_cast<size_t>(pairs) * 2 * sizeof(int32_t)) + 255) & ~size_t(255); }
+
+template <int KIND, int D>
+uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
+  using C = DC<KIND, D>;
+  const uq_cache& c = *a.cache;
+  const int G = a.num_q_heads / c.num_kv_heads;
+  const int pairs = a.batch * c.num_kv_heads * nhb;
+  const size_t smem = C::smem_fixed + (static_cast<size_t>(a.batch) + 1) * sizeof(int);
+  auto kern = decode_kernel<KIND, D>;
+  const uqh::DevInfo& di = uqh::dev_info();
+  if (smem > di.smem_optin) return UQ_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return UQ_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+    return UQ_ERR_CUDA;
+  // Workspace: [pair info][per-slot (m, l) x 8 heads][per-slot O x 8 heads]
+  const size_t info = ws_info_bytes(pairs);
+  if (a.ws_bytes < info) return UQ_ERR_WORKSPACE;
+  const int64_t fit = static_cast<int64_t>((a.ws_bytes - info) / ws_slot_bytes(D)) - pairs;
+  int64_t grid = std::min<int64_t>(static_cast<int64_t>(di.sms) * per_sm, fit);
+  if (grid < 1) return UQ_ERR_WORKSPACE;
+  const int64_t slots = grid + pairs;
+  DecParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.kc = static_cast<const uint8_t*>(c.k_codes);
+  p.ks = static_cast<const uint8_t*>(c.k_scales);
+  p.vc = static_cast<const uint8_t*>(c.v_codes);
+  p.vs = static_cast<const uint8_t*>(c.v_scales);
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.block_table = a.block_table;
+  p.max_pages = a.max_pages;
+  p.seq_lens = a.seq_lens;
+  p.B = a.batch;
+  p.Hq = a.num_q_heads;
+  p.Hkv = c.num_kv_heads;
+  p.G = G;
+  p.nhb = nhb;
+  p.ps_log2 = uqh::ilog2(c.page_size);
+  p.num_pages = c.num_pages;
+  const float sm = a.sm_scale > 0.f ? a.sm_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  p.sl2e = sm * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  p.ws_info = reinterpret_cast<int32_t*>(ws);
+  p.ws_ml = reinterpret_cast<float*>(ws + info);
+  p.ws_o = p.ws_ml + slots * kHB * 2;
+  p.status = uqh::status_word();
+  if (!p.status) return UQ_ERR_CUDA;
+  if (KIND == kFP4) uqh::make_sign_masks(c.rot_seed, D, &p.sign);
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
+
+  MergeParams mp;
+  mp.ws_o = p.ws_o;
+  mp.ws_ml = p.ws_ml;
+  mp.ws_info = p.ws_info;
+  mp.seq_lens = a.seq_lens;
+  mp.B = a.batch;
+  mp.Hq = a.num_q_heads;
+  mp.Hkv = c.num_kv_heads;
+  mp.G = G;
+  mp.nhb = nhb;
+  mp.cap = a.max_pages * c.page_size;
+  mp.num_ctas = static_cast<int>(grid);
+  mp.out = a.out;
+  mp.status = p.status;
+  mp.sign = p.sign;
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads;
+  merge_kernel<KIND, D><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(mp);
+  return uqh::cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+namespace uqh {
+
+int decode_max_ctas() { return dev_info().sms * 8; }
+
+size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas) {
+  const int G = hq / hkv;
+  const int nhb = (G + kHB - 1) / kHB;
+  const int pairs = batch * hkv * nhb;
+  return ws_info_bytes(pairs) + static_cast<size_t>(max_ctas + pairs) * ws_slot_bytes(d);
+}
+
+uq_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const uq_cache& c = *a.cache;
+  const int G = a.num_q_heads / c.num_kv_heads;
+  const int nhb = (G + kHB - 1) / kHB;
+  const int d = c.head_dim;
+  switch (c.dtype) {
+    case UQ_FP4_UE8M0:
+      return d == 128 ? run_decode<kFP4, 128>(a, nhb, s) : run_decode<kFP4, 64>(a, nhb, s);
+    case UQ_FP8_E4M3:
+      return d == 128 ? run_decode<kFP8, 128>(a, nhb, s) : run_decode<kFP8, 64>(a, nhb, s);
+    default:
+      return d == 128 ? run_decode<kBF16, 128>(a, nhb, s) : run_decode<kBF16, 64>(a, nhb, s);
+  }
+}
+
+uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out, cudaStream_t s) {
+  SignMasks sm;
+  make_sign_masks(seed, d, &sm);
+  const int64_t warps = (n + 7) / 8;
+  const unsigned grid = (unsigned)((warps + 3) / 4);
+  if (d == 128)
+    test_query_kernel<128><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+  else
+    test_query_kernel<64><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace uqh

@@ -1,0 +1,73 @@
+// uq_internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI; see include/uq.h for that).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/uq.h"
+
+namespace uqh {
+
+// Per-element XOR masks of the rotation's sign diagonal (0 or 0x80000000),
+// passed to kernels by value so that the library keeps no device state.
+struct SignMasks {
+  uint32_t m[128];
+};
+void make_sign_masks(uint64_t seed, int d, SignMasks* out);
+
+// Device status word of the current device (for in-kernel error records).
+unsigned int* status_word();
+
+// Properties of the current device (cached).
+struct DevInfo {
+  int device = -1;
+  int sms = 0;
+  size_t smem_optin = 0;
+};
+const DevInfo& dev_info();
+
+inline uq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? UQ_OK : UQ_ERR_CUDA; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int ilog2(int v) {
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return l;
+}
+
+// Append launchers (uq_append.cu).
+uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t ntok,
+                            const int64_t* slots, const uq_cache& c, cudaStream_t s);
+uq_status launch_append_anchor(const void* k, const void* v, bool in_fp32, int64_t ntok,
+                               const int64_t* slots, const uq_cache& c, cudaStream_t s);
+uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y,
+                             cudaStream_t s);
+uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s);
+uq_status launch_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+
+// Decode launchers (uq_decode.cu).
+struct DecodeArgs {
+  const void* q;
+  const uq_cache* cache;
+  const int32_t* block_table;
+  int32_t max_pages;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t num_q_heads;
+  float sm_scale;
+  float* out;
+  void* ws;
+  size_t ws_bytes;
+};
+size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas);
+int decode_max_ctas();
+uq_status launch_decode(const DecodeArgs& a, cudaStream_t s);
+uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out,
+                                cudaStream_t s);
+
+}  // namespace uqh
