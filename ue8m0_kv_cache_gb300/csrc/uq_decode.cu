@@ -79,9 +79,32 @@ struct DecParams {
   float* ws_o;
   float* ws_ml;
   int32_t* ws_info;
+  int64_t* ws_units;
   unsigned int* status;
   uqh::SignMasks sign;
 };
+
+// Contiguous range [lo, hi) of the U units that block c of C handles.
+__device__ __forceinline__ void block_range(int64_t c, int64_t U, int64_t C, int64_t& lo, int64_t& hi) {
+  lo = c * U / C;
+  hi = (c + 1) * U / C;
+}
+
+// P.V of one 16-token unit into a fresh accumulator, then added to the fp32
+// running output with IEEE adds.  P arrives as two f16 parts (hi + lo) of
+// p * 2^15, so together they carry ~22 bits; restarting the MMA accumulator
+// every unit keeps its (non-IEEE) accumulation from compounding over
+// thousands of units.
+__device__ __forceinline__ void pv_unit(float (&o)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        const uint32_t (&bp)[4]) {
+  float t[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_f16(t, a0, a1, a2, a3, bp[0], bp[1]);
+  mma_f16(t, a0, a1, a2, a3, bp[2], bp[3]);
+  o[0] += t[0];
+  o[1] += t[1];
+  o[2] += t[2];
+  o[3] += t[3];
+}
 
 __device__ __forceinline__ float pow2i(int e) {  // 2^e for e in [-149, 127], 0 below
   if (e >= -126) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
@@ -187,8 +210,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
   const int pps = p.Hkv * p.nhb;  // (kv head, head block) pairs per sequence
   const int64_t U = static_cast<int64_t>(pre[p.B]) * pps;
-  const int64_t lo = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
-  const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+  int64_t lo, hi;
+  block_range(blockIdx.x, U, gridDim.x, lo, hi);
+  if (blockIdx.x == 0 && tid == 0) *p.ws_units = U;
   uint32_t it = 0;  // position in this warp's ring, carried across segments
 
   for (int64_t u = lo; u < hi;) {
@@ -367,9 +391,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       const float p0 = ex2(s0 - M0), p1 = ex2(s1 - M1), p2 = ex2(s2 - M0), p3 = ex2(s3 - M1);
       L0 += p0 + p2;
       L1 += p1 + p3;
-      // P^T fragments: rows = tokens, cols = heads -> transpose to k = tokens.
-      const uint32_t B0 = movmatrix_trans(pack_f16x2(p0, p1));
-      const uint32_t B1 = movmatrix_trans(pack_f16x2(p2, p3));
+      // P^T fragments (rows = tokens, cols = heads, transposed to k = tokens),
+      // as hi + lo f16 parts of p * 2^15.
+      uint32_t bp[4];
+      {
+        const float q0 = p0 * 32768.f, q1 = p1 * 32768.f, q2 = p2 * 32768.f, q3 = p3 * 32768.f;
+        const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        bp[0] = movmatrix_trans(h01);
+        bp[1] = movmatrix_trans(h23);
+        bp[2] = movmatrix_trans(pack_f16x2(q0 - f01.x, q1 - f01.y));
+        bp[3] = movmatrix_trans(pack_f16x2(q2 - f23.x, q3 - f23.y));
+      }
 
       // ------------------------------------------------------------- P.V
       const int t0 = 2 * c, t1 = 2 * c + 1, t8 = 2 * c + 8, t9 = 2 * c + 9;
@@ -418,8 +452,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
           e2m1x8_to_f16x2(hi89, A3);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89),
-                    hmul2(A3[k], mv89), B0, B1);
+            pv_unit(O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89),
+                    hmul2(A3[k], mv89), bp);
         }
       } else if (KIND == kFP8) {
         constexpr int VB = C::VPT;  // bytes per thread and token
@@ -435,10 +469,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         for (int q4 = 0; q4 < VB / 4; ++q4) {
           const uint32_t x01 = __byte_perm(w0[q4], w1[q4], 0x5140), y01 = __byte_perm(w0[q4], w1[q4], 0x7362);
           const uint32_t x89 = __byte_perm(w8[q4], w9[q4], 0x5140), y89 = __byte_perm(w8[q4], w9[q4], 0x7362);
-          mma_f16(O[2 * q4], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(x89),
-                  e4m3x2_to_f16x2(x89 >> 16), B0, B1);
-          mma_f16(O[2 * q4 + 1], e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16), e4m3x2_to_f16x2(y89),
-                  e4m3x2_to_f16x2(y89 >> 16), B0, B1);
+          pv_unit(O[2 * q4], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(x89),
+                  e4m3x2_to_f16x2(x89 >> 16), bp);
+          pv_unit(O[2 * q4 + 1], e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16), e4m3x2_to_f16x2(y89),
+                  e4m3x2_to_f16x2(y89 >> 16), bp);
         }
       } else {
         constexpr int VW = C::VPT / 2;  // bf16 pairs per thread and token
@@ -455,8 +489,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         };
 #pragma unroll
         for (int m = 0; m < VW; ++m) {
-          mma_f16(O[m], bf2h(__byte_perm(w0[m], w1[m], 0x5410)), bf2h(__byte_perm(w0[m], w1[m], 0x7632)),
-                  bf2h(__byte_perm(w8[m], w9[m], 0x5410)), bf2h(__byte_perm(w8[m], w9[m], 0x7632)), B0, B1);
+          pv_unit(O[m], bf2h(__byte_perm(w0[m], w1[m], 0x5410)), bf2h(__byte_perm(w0[m], w1[m], 0x7632)),
+                  bf2h(__byte_perm(w8[m], w9[m], 0x5410)), bf2h(__byte_perm(w8[m], w9[m], 0x7632)), bp);
         }
       }
       __syncwarp();
@@ -478,7 +512,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       comb_ml[(warp * kHB + 2 * c + 1) * 2] = M1;
       comb_ml[(warp * kHB + 2 * c + 1) * 2 + 1] = L1;
     }
-    const float osc = KIND == kFP4 ? pow2i(static_cast<int>(RV) - 127) : (KIND == kFP8 ? p.v_scale : 1.f);
+    const float osc = (KIND == kFP4 ? pow2i(static_cast<int>(RV) - 127 - 15)
+                                    : (KIND == kFP8 ? p.v_scale * (1.f / 32768.f) : 1.f / 32768.f));
     {
       float* co = comb_o + warp * kHB * D;
 #pragma unroll
@@ -534,6 +569,7 @@ struct MergeParams {
   const float* ws_o;
   const float* ws_ml;
   const int32_t* ws_info;
+  const int64_t* ws_units;
   const int32_t* seq_lens;
   int B, Hq, Hkv, G, nhb, cap, num_ctas;
   float* out;
@@ -562,10 +598,18 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
       first = 1;
       last = 0;
     }
+    const int64_t U = *p.ws_units;
     float Ms = -INFINITY;
-    for (int s = first; s <= last; ++s) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
+    for (int s = first; s <= last; ++s) {
+      int64_t lo, hi;
+      block_range(s, U, p.num_ctas, lo, hi);
+      if (lo < hi) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
+    }
     float Ls = 0.f;
     for (int s = first; s <= last; ++s) {
+      int64_t lo, hi;
+      block_range(s, U, p.num_ctas, lo, hi);
+      if (lo >= hi) continue;  // a block with an empty range wrote no partial
       const int64_t id = (int64_t)(s + pair) * kHB + hh;
       const float w = ex2(p.ws_ml[id * 2] - Ms);
       Ls += w * p.ws_ml[id * 2 + 1];
@@ -625,7 +669,8 @@ __global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out, co
 
 // ------------------------------------------------------------------ host
 size_t ws_slot_bytes(int d) { return static_cast<size_t>(kHB) * (d + 2) * sizeof(float); }
-size_t ws_info_bytes(int pairs) { return ((static_cast<size_t>(pairs) * 2 * sizeof(int32_t)) + 255) & ~size_t(255); }
+// Workspace: [256-byte header: unit count][pair info, 2 x int32][per-slot (m, l) x 8 heads][per-slot O x 8 heads]
+size_t ws_info_bytes(int pairs) { return 256 + (((static_cast<size_t>(pairs) * 2 * sizeof(int32_t)) + 255) & ~size_t(255)); }
 
 template <int KIND, int D>
 uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
@@ -670,7 +715,8 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   const float sm = a.sm_scale > 0.f ? a.sm_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   p.sl2e = sm * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
-  p.ws_info = reinterpret_cast<int32_t*>(ws);
+  p.ws_units = reinterpret_cast<int64_t*>(ws);
+  p.ws_info = reinterpret_cast<int32_t*>(ws + 256);
   p.ws_ml = reinterpret_cast<float*>(ws + info);
   p.ws_o = p.ws_ml + slots * kHB * 2;
   p.status = uqh::status_word();
@@ -683,6 +729,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   mp.ws_o = p.ws_o;
   mp.ws_ml = p.ws_ml;
   mp.ws_info = p.ws_info;
+  mp.ws_units = p.ws_units;
   mp.seq_lens = a.seq_lens;
   mp.B = a.batch;
   mp.Hq = a.num_q_heads;
