@@ -72,8 +72,15 @@ typedef enum uq_in_dtype { UQ_IN_BF16 = 0, UQ_IN_FP32 = 1 } uq_in_dtype;
  * page * page_size + offset (the vLLM convention).
  *
  *   UQ_FP4_UE8M0: k_codes, v_codes : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
- *                   byte j of a row = code(2j) | code(2j+1) << 4, codes of the
- *                   ROTATED vector ([UQ-review] §3.1);
+ *                   codes of the ROTATED vector ([UQ-review] §3.1).  Natural
+ *                   byte j of a row = code(2j) | code(2j+1) << 4, so group g
+ *                   owns natural bytes 16g..16g+15 (words w = 0..3 of 4 bytes).
+ *                   V rows are stored in natural order.  K rows are stored
+ *                   group-interleaved by words: word w of group g sits at word
+ *                   position (head_dim/32)*w + g, so every aligned run of
+ *                   head_dim/8 bytes holds one word of each group (the layout
+ *                   the decode consumes with one load per token; [UQ-review]
+ *                   §4.2 matches the cache layout to the kernel's scale use);
  *                 k_scales, v_scales: uint8 [num_pages][num_kv_heads][page_size][head_dim/32]
  *                   UE8M0 byte of channels 32g..32g+31; value = code * 2^(byte-127)
  *                   ([UQ-review] §3.2); 0xFF marks a non-finite group.

@@ -263,3 +263,11 @@ def scale_bytes(m: np.ndarray, c: float = None, mode: int = ROUND_LOG2) -> np.nd
 def group_mse(y: np.ndarray, c: float, mode: int) -> float:
     y = _c(y, np.float32).reshape(-1)
     return float(_lib.uqo_group_mse(y, y.size // 32, np.float32(c), mode))
+
+_lib.uqo_kbyte_pos.restype = C.c_int
+_lib.uqo_kbyte_pos.argtypes = [C.c_int, C.c_int]
+
+
+def kbyte_pos(j: int, d: int) -> int:
+    """Cache position of natural code byte j of a K row (group-interleaved words)."""
+    return int(_lib.uqo_kbyte_pos(j, d))

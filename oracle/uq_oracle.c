@@ -238,6 +238,22 @@ void uqo_quantize_vectors(const void* x, int in_fp32, int64_t n, int d, uint64_t
 }
 
 /* ------------------------------------------------------------------------- */
+/* Cache byte order of a K row.  A quantised row is a sequence of d/2 code    */
+/* bytes, 16 per 32-channel group (natural order above).  In the cache, the   */
+/* K row's bytes are interleaved by 4-byte words across the groups: word w    */
+/* (bytes 4w..4w+3) of group g is stored at word position (d/32)*w + g, so   */
+/* each aligned run of d/8 bytes holds one word of every group.  V rows are   */
+/* stored in natural order.  (A layout choice of this library, made so that   */
+/* the decode reads the per-group operands with one aligned load; the pages   */
+/* state that the cache layout is matched to how the kernel consumes scales,  */
+/* [UQ-review] 4.2.)                                                          */
+/* ------------------------------------------------------------------------- */
+int uqo_kbyte_pos(int j, int d) {
+  int g = j / 16, b = j % 16, w = b / 4, k = b % 4;
+  return ((d / 32) * w + g) * 4 + k;
+}
+
+/* ------------------------------------------------------------------------- */
 /* R4: FP8 E4M3 (OCP "FN": bias 7, no inf, max 448, 0x7F NaN).                 */
 /* [UQ-review] 3.2: the query is rotated into the key basis, then rounded to   */
 /* FP8 E4M3.  Round to nearest by search over the 127 finite non-negative      */
@@ -300,7 +316,9 @@ void uqo_append_fp4(const void* k, const void* v, int in_fp32, int64_t T, const 
       int64_t src = t * Hkv + h, dst = cache_row(slots[t], h, Hkv, ps);
       const char* kr = (const char*)k + (size_t)src * d * esz;
       const char* vr = (const char*)v + (size_t)src * d * esz;
-      uqo_quantize_vectors(kr, in_fp32, 1, d, seed, kc + dst * (d / 2), ks + dst * (d / 32));
+      uint8_t kn[512];
+      uqo_quantize_vectors(kr, in_fp32, 1, d, seed, kn, ks + dst * (d / 32));
+      for (int j = 0; j < d / 2; ++j) kc[dst * (d / 2) + uqo_kbyte_pos(j, d)] = kn[j];
       uqo_quantize_vectors(vr, in_fp32, 1, d, seed, vc + dst * (d / 2), vs + dst * (d / 32));
     }
   }
@@ -347,10 +365,11 @@ void uqo_append_bf16(const void* k, const void* v, int in_fp32, int64_t T, const
 /* o = sum p v.  For the FP4 cache q is the rotated E4M3 query q~ and the      */
 /* output is rotated back ([UQ-review] 3.2).  kind: 0 = FP4, 1 = FP8, 2 = BF16.*/
 /* ------------------------------------------------------------------------- */
-static double kv_value(int kind, const uint8_t* codes, const uint8_t* scales, int64_t row, int d,
-                       int i, float tensor_scale) {
+static double kv_value(int kind, int is_k, const uint8_t* codes, const uint8_t* scales, int64_t row,
+                       int d, int i, float tensor_scale) {
   if (kind == 0) {
-    int byte = codes[row * (d / 2) + i / 2];
+    int pos = is_k ? uqo_kbyte_pos(i / 2, d) : i / 2;
+    int byte = codes[row * (d / 2) + pos];
     int code = (i & 1) ? (byte >> 4) : (byte & 15);
     return uqo_fp4_value(code, scales[row * (d / 32) + i / 32]);
   }
@@ -384,8 +403,8 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
         int64_t page = block_table[(int64_t)b * max_pages + j / ps];
         int64_t row = (page * Hkv + kvh) * ps + j % ps;
         for (int i = 0; i < d; ++i) {
-          K[(int64_t)j * d + i] = kv_value(kind, kc, ks, row, d, i, k_scale);
-          V[(int64_t)j * d + i] = kv_value(kind, vc, vs, row, d, i, v_scale);
+          K[(int64_t)j * d + i] = kv_value(kind, 1, kc, ks, row, d, i, k_scale);
+          V[(int64_t)j * d + i] = kv_value(kind, 0, vc, vs, row, d, i, v_scale);
         }
       }
       for (int h = kvh * G; h < (kvh + 1) * G; ++h) {

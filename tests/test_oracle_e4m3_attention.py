@@ -75,6 +75,36 @@ def _dequant_dense(codes, scales):
     return vals * np.repeat(2.0 ** (scales.astype(np.float64) - 127), 32, axis=1)
 
 
+def _k_natural(kc):
+    """Undo the cache's group-interleaved word order of K rows (include/uq.h):
+    word w of group g sits at word position (d/32)*w + g."""
+    rows, half = kc.shape
+    ng = half // 16
+    words = kc.reshape(rows, 4, ng, 4)            # [row][w][g][byte]
+    return words.transpose(0, 2, 1, 3).reshape(rows, half)
+
+
+def test_k_row_word_order():
+    """Literal word order of a K row in the cache for head_dim 64 and 128."""
+    want64 = ["g0w0", "g1w0", "g0w1", "g1w1", "g0w2", "g1w2", "g0w3", "g1w3"]
+    want128 = ["g0w0", "g1w0", "g2w0", "g3w0", "g0w1", "g1w1", "g2w1", "g3w1",
+               "g0w2", "g1w2", "g2w2", "g3w2", "g0w3", "g1w3", "g2w3", "g3w3"]
+    for d, want in ((64, want64), (128, want128)):
+        got = [None] * (d // 8)
+        for j in range(0, d // 2, 4):
+            g, w = j // 16, (j % 16) // 4
+            got[oracle.kbyte_pos(j, d) // 4] = "g%dw%d" % (g, w)
+        assert got == want
+        # and a cache row: quantise a vector with distinct codes per word, append, compare
+        rng = np.random.default_rng(d)
+        x = rng.standard_normal((1, 1, d)).astype(np.float32)
+        cache = oracle.Cache(oracle.KIND_FP4, 1, 1, 16, d)
+        cache.append(x, x, np.array([0]))
+        nat, _ = oracle.quantize_vectors(x.reshape(1, d))
+        assert np.array_equal(_k_natural(cache.kc[:1]), nat)
+        assert np.array_equal(cache.vc[:1], nat)
+
+
 def _bf16_bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -97,7 +127,7 @@ def test_attention_matches_dense_brute_force():
     s = oracle.signs(oracle.DEFAULT_SEED, d).astype(np.float64)
     H = _hadamard(d)
     qt = np.vectorize(oracle.e4m3_value)(oracle.query_fp8(q))  # pinned separately
-    K = _dequant_dense(cache.kc, cache.ks)
+    K = _dequant_dense(_k_natural(cache.kc), cache.ks)
     V = _dequant_dense(cache.vc, cache.vs)
     for b in range(w.B):
         L = w.seq_lens[b]

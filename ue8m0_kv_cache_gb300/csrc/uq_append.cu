@@ -78,13 +78,23 @@ __device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D
   }
 }
 
-template <int D>
+// Store one quantised row: codes[4g + w] is word w (bytes 4w..4w+3) of group
+// g in natural order.  K rows (KPERM) are stored group-interleaved by words --
+// word w of group g at word position (D/32)*w + g -- so that the decode can
+// fetch one word of every group with a single aligned load; V rows keep the
+// natural order.
+template <int D, bool KPERM>
 __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_base, int64_t row,
                                           const uint32_t (&codes)[D / 8], uint32_t scales) {
+  constexpr int NG = D / 32;
+  uint32_t out[D / 8];
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) out[KPERM ? NG * w + g : 4 * g + w] = codes[4 * g + w];
   uint4* cdst = reinterpret_cast<uint4*>(codes_base + row * (D / 2));
 #pragma unroll
-  for (int q = 0; q < D / 32; ++q)
-    cdst[q] = make_uint4(codes[4 * q], codes[4 * q + 1], codes[4 * q + 2], codes[4 * q + 3]);
+  for (int q = 0; q < D / 32; ++q) cdst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
   if (D == 128)
     *reinterpret_cast<uint32_t*>(scales_base + row * 4) = scales;
   else
@@ -175,7 +185,10 @@ __global__ void __launch_bounds__(kAppendThreads)
       } else if (slot >= 0) {
         const int64_t page = slot >> p.ps_log2;
         const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
-        store_row<D>(is_v ? p.vc : p.kc, is_v ? p.vs : p.ks, dst, codes, scales);
+        if (is_v)
+          store_row<D, false>(p.vc, p.vs, dst, codes, scales);
+        else
+          store_row<D, true>(p.kc, p.ks, dst, codes, scales);
       }
     }
     __syncthreads();
@@ -288,7 +301,7 @@ __global__ void test_quantize_kernel(const float* y, int64_t n, uint8_t* codes, 
   for (int i = 0; i < D; ++i) u[i] = y[r * D + i];
   uint32_t c[D / 8], s;
   quantize_regs<D>(u, c, s);
-  store_row<D>(codes, scales, r, c, s);
+  store_row<D, false>(codes, scales, r, c, s);
 }
 
 __global__ void test_cvt_e4m3_kernel(const float* x, int64_t n2, uint16_t* out) {

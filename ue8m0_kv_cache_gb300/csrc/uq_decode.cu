@@ -20,16 +20,22 @@
 //     shared-memory stages filled by 1-D bulk copies (TMA engine) on mbarriers:
 //     one unit = 16 rows of K codes, V codes and their scale bytes
 //     (2176 bytes for head_dim 128), 136 bytes per token-head.
-//   * QK^T and P.V run on the tensor cores with warp-level m16n8k16 f16 MMAs
-//     whose operands are built in registers: E2M1 pairs go through the
-//     hardware e2m1x2 -> f16x2 conversion, group scales 2^(E-R) are applied
-//     with one packed half multiply (R = the largest exponent of the tile, so
-//     every value fits f16), and the accumulators are fp32.  Keeping operands
-//     in registers avoids a second trip through shared memory, which at
-//     n = 8 query heads would otherwise cap the kernel below HBM speed.
+//   * QK^T and P.V run on the tensor cores as warp-level m16n8k16 f16 MMAs on
+//     operands built in registers by the hardware e2m1x2 -> f16x2 conversion.
+//     Keeping operands in registers avoids a second pass through shared
+//     memory, which at n = 8 query heads would cap the kernel below HBM speed.
+//   * QK^T runs one 32-channel group at a time into a fresh accumulator; the
+//     group's UE8M0 scale is then applied to the fp32 partial logit, so K
+//     values need no per-element scaling.  The cache stores K rows with the
+//     groups interleaved by 4-byte words, so one 16-byte load gives each
+//     thread one word of every group.
+//   * P.V: V values of a thread all belong to one group, so its scale is one
+//     packed half multiply; P is carried as hi + lo f16 parts (~22 bits) and
+//     each 16-token unit is summed in a fresh accumulator before an IEEE fp32
+//     add, so long contexts do not compound the accumulator's rounding.
 //   * Sums over the head dimension do not depend on the order of channels,
-//     so the channel-to-fragment mapping is chosen to make every thread's
-//     operands contiguous bytes of one 32-channel group.
+//     so channels are assigned to fragment slots wherever the loads are
+//     contiguous; the query and the output use the same assignment.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -44,8 +50,9 @@ using namespace uqd;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kHB = 8;  // query heads per block (the MMA's n)
+constexpr int kHB = 8;      // query heads per block (the MMA's n)
 constexpr int kChunk = 16;  // tokens per work unit (the MMA's m for QK)
+constexpr float kPShift = 15.f;  // p is carried as p * 2^15 (fits f16, keeps the lo part normal)
 
 enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
 
@@ -58,6 +65,7 @@ struct DC {
   static constexpr int STAGE = 2 * KBYTES + 2 * SBYTES;
   static constexpr int NST = KIND == kFP4 ? 4 : 3;  // ring depth per warp
   static constexpr int NMMA = D / 16;               // k-steps of QK, m-blocks of PV
+  static constexpr int NG = D / 32;                 // 32-channel groups
   static constexpr int CPT = D / 4;                 // QK channels per thread and token
   static constexpr int VPT = D / 8;                 // PV channels per thread and token
   static constexpr size_t smem_fixed = (size_t)kWarps * NST * STAGE + (size_t)kWarps * NST * 8 +
@@ -90,34 +98,25 @@ __device__ __forceinline__ void block_range(int64_t c, int64_t U, int64_t C, int
   hi = (c + 1) * U / C;
 }
 
-// P.V of one 16-token unit into a fresh accumulator, then added to the fp32
-// running output with IEEE adds.  P arrives as two f16 parts (hi + lo) of
-// p * 2^15, so together they carry ~22 bits; restarting the MMA accumulator
-// every unit keeps its (non-IEEE) accumulation from compounding over
-// thousands of units.
-__device__ __forceinline__ void pv_unit(float (&o)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        const uint32_t (&bp)[4]) {
-  float t[4] = {0.f, 0.f, 0.f, 0.f};
-  mma_f16(t, a0, a1, a2, a3, bp[0], bp[1]);
-  mma_f16(t, a0, a1, a2, a3, bp[2], bp[3]);
-  o[0] += t[0];
-  o[1] += t[1];
-  o[2] += t[2];
-  o[3] += t[3];
-}
-
 __device__ __forceinline__ float pow2i(int e) {  // 2^e for e in [-149, 127], 0 below
   if (e >= -126) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
   if (e >= -149) return __uint_as_float(1u << (e + 149));
   return 0.f;
 }
 
-// f16 multiplier for a group scale byte relative to the tile reference R:
-// 2^(byte-R) (<= 1), 0 for masked tokens, NaN for a non-finite group.
-__device__ __forceinline__ float group_mult(uint32_t byte, uint32_t R, bool valid) {
-  if (!valid) return 0.f;
-  if (byte == 0xFFu) return __int_as_float(0x7FC00000);
-  return pow2i(static_cast<int>(byte) - static_cast<int>(R));
+// 2^(byte-127) as fp32 for the byte at bit offset 8*g of w: the byte becomes
+// the exponent field.  Byte 0 gives +0 instead of 2^-127 (a group that small
+// contributes nothing representable); byte 0xFF gives +Inf, so a non-finite
+// group poisons the logit.
+template <int G>
+__device__ __forceinline__ float scale_of(uint32_t w) {
+  return G == 3 ? __uint_as_float((w >> 1) & 0x7F800000u)
+                : __uint_as_float((w << (23 - 8 * G)) & 0x7F800000u);
+}
+
+// Non-zero if any byte of w is 0xFF (a non-finite group).
+__device__ __forceinline__ uint32_t has_ff(uint32_t w) {
+  return ((w & 0x7F7F7F7Fu) + 0x01010101u) & w & 0x80808080u;
 }
 
 __device__ __forceinline__ int clamp_len(const DecParams& p, int b) {
@@ -130,20 +129,20 @@ __device__ __forceinline__ int clamp_len(const DecParams& p, int b) {
   return L;
 }
 
-// The rotated E4M3 query of head row `r` of the block, channels
-// [c*CPT, (c+1)*CPT), returned as f16x2 B fragments (FP4) -- the same fp32
-// butterfly as the append path, spread over the 4 threads of a quad: strides
-// below CPT inside a thread, the last two strides across the quad.
+// The rotated E4M3 query of one head, channels [c*D/4, (c+1)*D/4), packed 4
+// bytes per word: the same fp32 butterfly as the append path, spread over
+// the 4 threads of a quad (strides below D/4 inside a thread, the last two
+// across the quad), then E4M3 round to nearest even, saturating.
 template <int D>
-__device__ __forceinline__ void rotated_query_fp8(const uint16_t* qrow, bool valid, int c, const DecParams& p,
-                                                  uint32_t (&qb)[D / 16][2], uint8_t* bytes_out) {
+__device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool valid, int c,
+                                                    const uqh::SignMasks& sign, uint32_t (&out)[D / 16]) {
   constexpr int CPT = D / 4;
   float x[CPT];
 #pragma unroll
   for (int e = 0; e < CPT; e += 2) {
-    uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(qrow + c * CPT + e) : 0u;
-    x[e] = __uint_as_float((w << 16) ^ p.sign.m[c * CPT + e]);
-    x[e + 1] = __uint_as_float((w & 0xFFFF0000u) ^ p.sign.m[c * CPT + e + 1]);
+    const uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(qrow + c * CPT + e) : 0u;
+    x[e] = __uint_as_float((w << 16) ^ sign.m[c * CPT + e]);
+    x[e + 1] = __uint_as_float((w & 0xFFFF0000u) ^ sign.m[c * CPT + e + 1]);
   }
   fwht_regs<CPT>(x);
 #pragma unroll
@@ -159,17 +158,291 @@ __device__ __forceinline__ void rotated_query_fp8(const uint16_t* qrow, bool val
 #pragma unroll
   for (int e = 0; e < CPT; e += 2) mul2(x[e], x[e + 1], s);
 #pragma unroll
-  for (int m = 0; m < D / 16; ++m) {
-    const uint32_t b01 = cvt_e4m3x2(x[4 * m], x[4 * m + 1]);
-    const uint32_t b23 = cvt_e4m3x2(x[4 * m + 2], x[4 * m + 3]);
-    qb[m][0] = e4m3x2_to_f16x2(b01);
-    qb[m][1] = e4m3x2_to_f16x2(b23);
-    if (bytes_out) *reinterpret_cast<uint32_t*>(bytes_out + 4 * m) = b01 | (b23 << 16);
+  for (int m = 0; m < D / 16; ++m)
+    out[m] = cvt_e4m3x2(x[4 * m], x[4 * m + 1]) | (cvt_e4m3x2(x[4 * m + 2], x[4 * m + 3]) << 16);
+}
+
+// Softmax update for one unit: t[] are the log2-domain logits of tokens
+// (r, r+8) x heads (2c, 2c+1).  Updates the running max / sum, rescales O when
+// the max grows, and returns the P^T B fragments as hi/lo f16 parts of
+// p * 2^15.
+template <int NMMA>
+__device__ __forceinline__ void softmax_unit(const float (&t)[4], float& M0, float& M1, float& L0, float& L1,
+                                             float (&O)[NMMA][4], uint32_t (&bp)[4]) {
+  float mc0 = fmaxf(t[0], t[2]), mc1 = fmaxf(t[1], t[3]);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+    mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+  }
+  if (__any_sync(kFull, mc0 > M0 || mc1 > M1)) {
+    const float n0 = fmaxf(M0, mc0), n1 = fmaxf(M1, mc1);
+    const float a0 = ex2(M0 - n0), a1 = ex2(M1 - n1);
+    M0 = n0;
+    M1 = n1;
+    L0 *= a0;
+    L1 *= a1;
+#pragma unroll
+    for (int m = 0; m < NMMA; ++m) {
+      O[m][0] *= a0; O[m][1] *= a1; O[m][2] *= a0; O[m][3] *= a1;
+    }
+  }
+  const float s0 = kPShift - M0, s1 = kPShift - M1;
+  const float p0 = ex2(t[0] + s0), p1 = ex2(t[1] + s1), p2 = ex2(t[2] + s0), p3 = ex2(t[3] + s1);
+  L0 += p0 + p2;
+  L1 += p1 + p3;
+  // hi = p with the low 13 mantissa bits cleared (exact in f16), lo = the rest.
+  const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+  const float h2 = __uint_as_float(__float_as_uint(p2) & 0xFFFFE000u);
+  const float h3 = __uint_as_float(__float_as_uint(p3) & 0xFFFFE000u);
+  // rows = tokens, cols = heads; transposed so that k = tokens.
+  bp[0] = movmatrix_trans(pack_f16x2(h0, h1));
+  bp[1] = movmatrix_trans(pack_f16x2(h2, h3));
+  bp[2] = movmatrix_trans(pack_f16x2(p0 - h0, p1 - h1));
+  bp[3] = movmatrix_trans(pack_f16x2(p2 - h2, p3 - h3));
+}
+
+// P.V of one 16-token unit for one 16-channel block into a fresh
+// accumulator, then an IEEE fp32 add into the running output.
+__device__ __forceinline__ void pv_unit(float (&o)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        const uint32_t (&bp)[4]) {
+  float t[4];
+  mma_f16_zc(t, a0, a1, a2, a3, bp[0], bp[1]);
+  mma_f16(t, a0, a1, a2, a3, bp[2], bp[3]);
+  o[0] += t[0];
+  o[1] += t[1];
+  o[2] += t[2];
+  o[3] += t[3];
+}
+
+// Per-warp running state of one segment.
+template <int NMMA>
+struct WarpState {
+  float M0, M1, L0, L1;
+  float O[NMMA][4];
+  uint32_t RV;   // FP4: reference exponent byte of O
+  uint32_t bad;  // FP4: a non-finite group was seen
+};
+
+// One 16-token unit, FP4 cache.  TAIL: the unit may hold fewer than 16 valid
+// tokens (the last unit of a sequence); masked tokens get logit -inf and
+// value multiplier 0, whatever bytes their slots hold.
+template <int D, bool TAIL>
+__device__ __forceinline__ void unit_fp4(const uint8_t* st, int nvalid, int r, int c,
+                                         const uint32_t (&qb)[D / 16][2], float sl2e,
+                                         WarpState<D / 16>& S) {
+  using C = DC<kFP4, D>;
+  constexpr int NG = C::NG;
+  const uint8_t* skc = st;
+  const uint8_t* svc = st + C::KBYTES;
+  const uint8_t* sks = st + 2 * C::KBYTES;
+  const uint8_t* svs = sks + C::SBYTES;
+
+  // ---- QK^T per group: thread (r, c) holds word c of every group of tokens r, r+8
+  uint32_t kw0[NG], kw1[NG];
+  if (NG == 4) {
+    const uint4 x0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 16);
+    const uint4 x1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 16);
+    kw0[0] = x0.x; kw0[1] = x0.y; kw0[2 % NG] = x0.z; kw0[3 % NG] = x0.w;
+    kw1[0] = x1.x; kw1[1] = x1.y; kw1[2 % NG] = x1.z; kw1[3 % NG] = x1.w;
+  } else {
+    const uint2 x0 = *reinterpret_cast<const uint2*>(skc + r * C::KROW + c * 8);
+    const uint2 x1 = *reinterpret_cast<const uint2*>(skc + (r + 8) * C::KROW + c * 8);
+    kw0[0] = x0.x; kw0[1 % NG] = x0.y;
+    kw1[0] = x1.x; kw1[1 % NG] = x1.y;
+  }
+  uint32_t ksw0, ksw1;  // the token's NG scale bytes
+  if (NG == 4) {
+    ksw0 = *reinterpret_cast<const uint32_t*>(sks + r * 4);
+    ksw1 = *reinterpret_cast<const uint32_t*>(sks + (r + 8) * 4);
+  } else {
+    ksw0 = *reinterpret_cast<const uint16_t*>(sks + r * 2);
+    ksw1 = *reinterpret_cast<const uint16_t*>(sks + (r + 8) * 2);
+  }
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    uint32_t h0[4], h1[4];
+    e2m1x8_to_f16x2(kw0[g], h0);
+    e2m1x8_to_f16x2(kw1[g], h1);
+    float acc[4];
+    mma_f16_zc(acc, h0[0], h1[0], h0[1], h1[1], qb[2 * g][0], qb[2 * g][1]);
+    mma_f16(acc, h0[2], h1[2], h0[3], h1[3], qb[2 * g + 1][0], qb[2 * g + 1][1]);
+    float f0, f1;
+    if (g == 0) { f0 = scale_of<0>(ksw0); f1 = scale_of<0>(ksw1); }
+    else if (g == 1) { f0 = scale_of<1>(ksw0); f1 = scale_of<1>(ksw1); }
+    else if (g == 2) { f0 = scale_of<2>(ksw0); f1 = scale_of<2>(ksw1); }
+    else { f0 = scale_of<3>(ksw0); f1 = scale_of<3>(ksw1); }
+    s[0] = fmaf(acc[0], f0, s[0]);
+    s[1] = fmaf(acc[1], f0, s[1]);
+    s[2] = fmaf(acc[2], f1, s[2]);
+    s[3] = fmaf(acc[3], f1, s[3]);
+  }
+  float t[4] = {s[0] * sl2e, s[1] * sl2e, s[2] * sl2e, s[3] * sl2e};
+  uint32_t kbad;
+  if (TAIL) {
+    const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+    if (!v0) { t[0] = -INFINITY; t[1] = -INFINITY; }
+    if (!v1) { t[2] = -INFINITY; t[3] = -INFINITY; }
+    kbad = (v0 ? has_ff(ksw0) : 0u) | (v1 ? has_ff(ksw1) : 0u);
+  } else {
+    kbad = has_ff(ksw0) | has_ff(ksw1);
+  }
+
+  uint32_t bp[4];
+  softmax_unit<C::NMMA>(t, S.M0, S.M1, S.L0, S.L1, S.O, bp);
+
+  // ---- P.V: thread (r, c) takes channels r*VPT.. of tokens 2c, 2c+1, 2c+8, 2c+9
+  constexpr int VB = C::VPT / 2;  // code bytes per thread and token
+  const int t0 = 2 * c, t1 = t0 + 1, t8 = t0 + 8, t9 = t0 + 9;
+  uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
+#pragma unroll
+  for (int q4 = 0; q4 < VB / 4; ++q4) {
+    w0[q4] = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
+    w1[q4] = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
+    w8[q4] = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
+    w9[q4] = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
+  }
+  const int gv = (r * C::VPT) >> 5;
+  uint32_t b0 = svs[t0 * C::SROW + gv], b1 = svs[t1 * C::SROW + gv];
+  uint32_t b8 = svs[t8 * C::SROW + gv], b9 = svs[t9 * C::SROW + gv];
+  if (TAIL) {
+    if (t0 >= nvalid) b0 = 0;
+    if (t1 >= nvalid) b1 = 0;
+    if (t8 >= nvalid) b8 = 0;
+    if (t9 >= nvalid) b9 = 0;
+  }
+  // Reference exponent RV = running max of the V scale bytes, so that every
+  // multiplier 2^(byte - RV) is <= 1 and fits f16 together with the codes.
+  const uint32_t bmax = max(max(b0, b1), max(b8, b9));
+  const uint32_t vbad = bmax == 0xFFu ? 1u : 0u;
+  const uint32_t RVc = __reduce_max_sync(kFull, bmax);
+  if (RVc > S.RV) {
+    const float f = pow2i(static_cast<int>(S.RV) - static_cast<int>(RVc));
+#pragma unroll
+    for (int m = 0; m < C::NMMA; ++m) {
+      S.O[m][0] *= f; S.O[m][1] *= f; S.O[m][2] *= f; S.O[m][3] *= f;
+    }
+    S.RV = RVc;
+  }
+  // 2^(byte-127) * 2^(127-RV), both factors exact powers of two (byte 0 gives 0).
+  const float rref = pow2i(127 - static_cast<int>(S.RV));
+  float f0 = __uint_as_float(b0 << 23) * rref, f1 = __uint_as_float(b1 << 23) * rref;
+  float f8 = __uint_as_float(b8 << 23) * rref, f9 = __uint_as_float(b9 << 23) * rref;
+  if (TAIL) {
+    if (t0 >= nvalid) f0 = 0.f;
+    if (t1 >= nvalid) f1 = 0.f;
+    if (t8 >= nvalid) f8 = 0.f;
+    if (t9 >= nvalid) f9 = 0.f;
+  }
+  const uint32_t mv01 = pack_f16x2(f0, f1), mv89 = pack_f16x2(f8, f9);
+  S.bad |= kbad | vbad;
+#pragma unroll
+  for (int q4 = 0; q4 < VB / 4; ++q4) {
+    // Pair the same channel of two tokens in one byte (low nibble = lower token).
+    const uint32_t lo01 = (w0[q4] & 0x0F0F0F0Fu) | ((w1[q4] & 0x0F0F0F0Fu) << 4);
+    const uint32_t hi01 = ((w0[q4] >> 4) & 0x0F0F0F0Fu) | (w1[q4] & 0xF0F0F0F0u);
+    const uint32_t lo89 = (w8[q4] & 0x0F0F0F0Fu) | ((w9[q4] & 0x0F0F0F0Fu) << 4);
+    const uint32_t hi89 = ((w8[q4] >> 4) & 0x0F0F0F0Fu) | (w9[q4] & 0xF0F0F0F0u);
+    uint32_t A0[4], A1[4], A2[4], A3[4];
+    e2m1x8_to_f16x2(lo01, A0);
+    e2m1x8_to_f16x2(hi01, A1);
+    e2m1x8_to_f16x2(lo89, A2);
+    e2m1x8_to_f16x2(hi89, A3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      pv_unit(S.O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89), hmul2(A3[k], mv89),
+              bp);
+  }
+}
+
+// One 16-token unit, FP8 or BF16 cache (unrotated, per-tensor scales folded
+// into the logit scale and the final output).
+template <int KIND, int D, bool TAIL>
+__device__ __forceinline__ void unit_anchor(const uint8_t* st, int nvalid, int r, int c,
+                                            const uint32_t (&qb)[D / 16][2], float fac,
+                                            WarpState<D / 16>& S) {
+  using C = DC<KIND, D>;
+  const uint8_t* skc = st;
+  const uint8_t* svc = st + C::KBYTES;
+  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (KIND == kFP8) {
+    const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT);
+    const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT);
+#pragma unroll
+    for (int q4 = 0; q4 < C::CPT / 16; ++q4) {
+      const uint4 x0 = a0[q4], x1 = a1[q4];
+      const uint32_t u0[4] = {x0.x, x0.y, x0.z, x0.w}, u1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int m = 4 * q4 + k;
+        mma_f16(sacc, e4m3x2_to_f16x2(u0[k]), e4m3x2_to_f16x2(u1[k]), e4m3x2_to_f16x2(u0[k] >> 16),
+                e4m3x2_to_f16x2(u1[k] >> 16), qb[m][0], qb[m][1]);
+      }
+    }
+  } else {
+    const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT * 2);
+    const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT * 2);
+#pragma unroll
+    for (int q4 = 0; q4 < C::CPT / 8; ++q4) {
+      const uint4 x0 = a0[q4], x1 = a1[q4];
+      mma_bf16(sacc, x0.x, x1.x, x0.y, x1.y, qb[2 * q4][0], qb[2 * q4][1]);
+      mma_bf16(sacc, x0.z, x1.z, x0.w, x1.w, qb[2 * q4 + 1][0], qb[2 * q4 + 1][1]);
+    }
+  }
+  float t[4] = {sacc[0] * fac, sacc[1] * fac, sacc[2] * fac, sacc[3] * fac};
+  if (TAIL) {
+    if (r >= nvalid) { t[0] = -INFINITY; t[1] = -INFINITY; }
+    if (r + 8 >= nvalid) { t[2] = -INFINITY; t[3] = -INFINITY; }
+  }
+  uint32_t bp[4];
+  softmax_unit<C::NMMA>(t, S.M0, S.M1, S.L0, S.L1, S.O, bp);
+
+  const int t0 = 2 * c, t1 = t0 + 1, t8 = t0 + 8, t9 = t0 + 9;
+  const bool vt0 = !TAIL || t0 < nvalid, vt1 = !TAIL || t1 < nvalid;
+  const bool vt8 = !TAIL || t8 < nvalid, vt9 = !TAIL || t9 < nvalid;
+  if (KIND == kFP8) {
+    constexpr int VB = C::VPT;  // bytes per thread and token
+    uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
+#pragma unroll
+    for (int q4 = 0; q4 < VB / 4; ++q4) {
+      w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4] : 0u;
+      w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4] : 0u;
+      w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4] : 0u;
+      w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4] : 0u;
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < VB / 4; ++q4) {
+      const uint32_t x01 = __byte_perm(w0[q4], w1[q4], 0x5140), y01 = __byte_perm(w0[q4], w1[q4], 0x7362);
+      const uint32_t x89 = __byte_perm(w8[q4], w9[q4], 0x5140), y89 = __byte_perm(w8[q4], w9[q4], 0x7362);
+      pv_unit(S.O[2 * q4], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(x89),
+              e4m3x2_to_f16x2(x89 >> 16), bp);
+      pv_unit(S.O[2 * q4 + 1], e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16), e4m3x2_to_f16x2(y89),
+              e4m3x2_to_f16x2(y89 >> 16), bp);
+    }
+  } else {
+    constexpr int VW = C::VPT / 2;  // bf16 pairs per thread and token
+    uint32_t w0[VW], w1[VW], w8[VW], w9[VW];
+#pragma unroll
+    for (int q4 = 0; q4 < VW; ++q4) {
+      w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+      w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+      w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+      w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * C::VPT * 2)[q4] : 0u;
+    }
+    auto bf2h = [](uint32_t w) {  // bf16x2 -> f16x2
+      return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    };
+#pragma unroll
+    for (int m = 0; m < VW; ++m)
+      pv_unit(S.O[m], bf2h(__byte_perm(w0[m], w1[m], 0x5410)), bf2h(__byte_perm(w0[m], w1[m], 0x7632)),
+              bf2h(__byte_perm(w8[m], w9[m], 0x5410)), bf2h(__byte_perm(w8[m], w9[m], 0x7632)), bp);
   }
 }
 
 template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ DecParams p) {
   using C = DC<KIND, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -239,27 +512,45 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       const bool hv = hloc < p.G;
       const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (hv ? hloc : 0)) * D;
       if (KIND == kFP4) {
-        rotated_query_fp8<D>(qrow, hv, c, p, qb, nullptr);
+        // Rotate and round on the quad, then regroup through this warp's slice
+        // of the combine buffer: thread c needs bytes 32g + 8c .. +7 of its
+        // head for every group g (the fragment order of the QK^T loop).
+        uint32_t qbytes[D / 16];
+        rotated_query_bytes<D>(qrow, hv, c, p.sign, qbytes);
+        uint8_t* qs = reinterpret_cast<uint8_t*>(comb_o + warp * kHB * D);
+#pragma unroll
+        for (int e = 0; e < D / 16; ++e) *reinterpret_cast<uint32_t*>(qs + r * D + c * (D / 4) + 4 * e) = qbytes[e];
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < C::NG; ++g) {
+          const uint2 w = *reinterpret_cast<const uint2*>(qs + r * D + 32 * g + 8 * c);
+          qb[2 * g][0] = e4m3x2_to_f16x2(w.x);
+          qb[2 * g][1] = e4m3x2_to_f16x2(w.x >> 16);
+          qb[2 * g + 1][0] = e4m3x2_to_f16x2(w.y);
+          qb[2 * g + 1][1] = e4m3x2_to_f16x2(w.y >> 16);
+        }
+        __syncwarp();
       } else {
 #pragma unroll
         for (int m = 0; m < C::NMMA; ++m) {
-          const uint32_t w0 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m) : 0u;
-          const uint32_t w1 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m + 2) : 0u;
+          const uint32_t x0 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m) : 0u;
+          const uint32_t x1 = hv ? *reinterpret_cast<const uint32_t*>(qrow + c * C::CPT + 4 * m + 2) : 0u;
           if (KIND == kBF16) {
-            qb[m][0] = w0;
-            qb[m][1] = w1;
+            qb[m][0] = x0;
+            qb[m][1] = x1;
           } else {  // bf16 -> f16 (exact for |q| in the f16 normal range)
-            qb[m][0] = pack_f16x2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
-            qb[m][1] = pack_f16x2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+            qb[m][0] = pack_f16x2(__uint_as_float(x0 << 16), __uint_as_float(x0 & 0xFFFF0000u));
+            qb[m][1] = pack_f16x2(__uint_as_float(x1 << 16), __uint_as_float(x1 & 0xFFFF0000u));
           }
         }
       }
     }
 
     const int nw = seg > warp ? (seg - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
     auto issue = [&](int i, int slot) {
       const int tok0 = (j0 + warp + i * kWarps) * kChunk;
-      int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + (tok0 >> p.ps_log2)];
+      int page = bt_row[tok0 >> p.ps_log2];
       if (page < 0 || page >= p.num_pages) {
         record_error(p.status, kErrBounds);
         page = 0;
@@ -278,11 +569,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (lane == 0)
       for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST);
 
-    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-    float O[C::NMMA][4];
+    WarpState<C::NMMA> S;
+    S.M0 = S.M1 = -INFINITY;
+    S.L0 = S.L1 = 0.f;
+    S.RV = 0;
+    S.bad = 0;
 #pragma unroll
-    for (int m = 0; m < C::NMMA; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
-    uint32_t RV = 0;  // FP4: reference exponent byte of the V accumulator
+    for (int m = 0; m < C::NMMA; ++m) S.O[m][0] = S.O[m][1] = S.O[m][2] = S.O[m][3] = 0.f;
+    const float fac = KIND == kFP8 ? p.sl2e * p.k_scale : p.sl2e;
 
     for (int i = 0; i < nw; ++i, ++it) {
       const int slot = it % C::NST;
@@ -298,200 +592,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         break;
       }
       const uint8_t* st = myring + slot * C::STAGE;
-      const uint8_t* skc = st;
-      const uint8_t* svc = st + C::KBYTES;
-      const int rem = L - (j0 + warp + i * kWarps) * kChunk;
-      const int nvalid = rem < kChunk ? rem : kChunk;
-      const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
-
-      // ---------------------------------------------------------------- QK^T
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      float fac = p.sl2e;
-      if (KIND == kFP4) {
-        constexpr int KB = C::CPT / 2;  // code bytes per thread and token
-        const uint8_t* sks = st + 2 * C::KBYTES;
-        uint32_t kw0[KB / 4], kw1[KB / 4];
-        {
-          const uint32_t* a0 = reinterpret_cast<const uint32_t*>(skc + r * C::KROW + c * KB);
-          const uint32_t* a1 = reinterpret_cast<const uint32_t*>(skc + (r + 8) * C::KROW + c * KB);
-          if (KB == 16) {
-            const uint4 x0 = *reinterpret_cast<const uint4*>(a0), x1 = *reinterpret_cast<const uint4*>(a1);
-            kw0[0] = x0.x; kw0[1] = x0.y; kw0[2] = x0.z; kw0[3] = x0.w;
-            kw1[0] = x1.x; kw1[1] = x1.y; kw1[2] = x1.z; kw1[3] = x1.w;
-          } else {
-            const uint2 x0 = *reinterpret_cast<const uint2*>(a0), x1 = *reinterpret_cast<const uint2*>(a1);
-            kw0[0] = x0.x; kw0[1] = x0.y;
-            kw1[0] = x1.x; kw1[1] = x1.y;
-          }
-        }
-        const int gk = (c * C::CPT) >> 5;
-        const uint32_t kb0 = sks[r * C::SROW + gk], kb1 = sks[(r + 8) * C::SROW + gk];
-        const uint32_t e0 = (v0 && kb0 != 0xFFu) ? kb0 : 0u, e1 = (v1 && kb1 != 0xFFu) ? kb1 : 0u;
-        const uint32_t RK = __reduce_max_sync(kFull, e0 > e1 ? e0 : e1);
-        const float f0 = group_mult(kb0, RK, v0), f1 = group_mult(kb1, RK, v1);
-        const uint32_t mk0 = pack_f16x2(f0, f0), mk1 = pack_f16x2(f1, f1);
-#pragma unroll
-        for (int w = 0; w < KB / 4; ++w) {
-          uint32_t h0[4], h1[4];
-          e2m1x8_to_f16x2(kw0[w], h0);
-          e2m1x8_to_f16x2(kw1[w], h1);
-          mma_f16(sacc, hmul2(h0[0], mk0), hmul2(h1[0], mk1), hmul2(h0[1], mk0), hmul2(h1[1], mk1),
-                  qb[2 * w][0], qb[2 * w][1]);
-          mma_f16(sacc, hmul2(h0[2], mk0), hmul2(h1[2], mk1), hmul2(h0[3], mk0), hmul2(h1[3], mk1),
-                  qb[2 * w + 1][0], qb[2 * w + 1][1]);
-        }
-        fac = __fmul_rn(p.sl2e, pow2i(static_cast<int>(RK) - 127));
-      } else if (KIND == kFP8) {
-        const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT);
-        const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT);
-#pragma unroll
-        for (int q4 = 0; q4 < C::CPT / 16; ++q4) {
-          const uint4 x0 = a0[q4], x1 = a1[q4];
-          const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int m = 4 * q4 + k;
-            mma_f16(sacc, e4m3x2_to_f16x2(w0[k]), e4m3x2_to_f16x2(w1[k]), e4m3x2_to_f16x2(w0[k] >> 16),
-                    e4m3x2_to_f16x2(w1[k] >> 16), qb[m][0], qb[m][1]);
-          }
-        }
-        fac = p.sl2e * p.k_scale;
+      const int nvalid = L - (j0 + warp + i * kWarps) * kChunk;
+      if (nvalid >= kChunk) {
+        if (KIND == kFP4) unit_fp4<D, false>(st, kChunk, r, c, qb, fac, S);
+        else unit_anchor<KIND, D, false>(st, kChunk, r, c, qb, fac, S);
       } else {
-        const uint4* a0 = reinterpret_cast<const uint4*>(skc + r * C::KROW + c * C::CPT * 2);
-        const uint4* a1 = reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * C::CPT * 2);
-#pragma unroll
-        for (int q4 = 0; q4 < C::CPT / 8; ++q4) {
-          const uint4 x0 = a0[q4], x1 = a1[q4];
-          mma_bf16(sacc, x0.x, x1.x, x0.y, x1.y, qb[2 * q4][0], qb[2 * q4][1]);
-          mma_bf16(sacc, x0.z, x1.z, x0.w, x1.w, qb[2 * q4 + 1][0], qb[2 * q4 + 1][1]);
-        }
-      }
-      const float s0 = v0 ? sacc[0] * fac : -INFINITY, s1 = v0 ? sacc[1] * fac : -INFINITY;
-      const float s2 = v1 ? sacc[2] * fac : -INFINITY, s3 = v1 ? sacc[3] * fac : -INFINITY;
-
-      // ----------------------------------------------------- online softmax
-      float mc0 = fmaxf(s0, s2), mc1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
-        mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
-      }
-      if (__any_sync(kFull, mc0 > M0 || mc1 > M1)) {
-        const float n0 = fmaxf(M0, mc0), n1 = fmaxf(M1, mc1);
-        const float a0 = ex2(M0 - n0), a1 = ex2(M1 - n1);
-        M0 = n0;
-        M1 = n1;
-        L0 *= a0;
-        L1 *= a1;
-#pragma unroll
-        for (int m = 0; m < C::NMMA; ++m) {
-          O[m][0] *= a0; O[m][1] *= a1; O[m][2] *= a0; O[m][3] *= a1;
-        }
-      }
-      const float p0 = ex2(s0 - M0), p1 = ex2(s1 - M1), p2 = ex2(s2 - M0), p3 = ex2(s3 - M1);
-      L0 += p0 + p2;
-      L1 += p1 + p3;
-      // P^T fragments (rows = tokens, cols = heads, transposed to k = tokens),
-      // as hi + lo f16 parts of p * 2^15.
-      uint32_t bp[4];
-      {
-        const float q0 = p0 * 32768.f, q1 = p1 * 32768.f, q2 = p2 * 32768.f, q3 = p3 * 32768.f;
-        const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-        bp[0] = movmatrix_trans(h01);
-        bp[1] = movmatrix_trans(h23);
-        bp[2] = movmatrix_trans(pack_f16x2(q0 - f01.x, q1 - f01.y));
-        bp[3] = movmatrix_trans(pack_f16x2(q2 - f23.x, q3 - f23.y));
-      }
-
-      // ------------------------------------------------------------- P.V
-      const int t0 = 2 * c, t1 = 2 * c + 1, t8 = 2 * c + 8, t9 = 2 * c + 9;
-      const bool vt0 = t0 < nvalid, vt1 = t1 < nvalid, vt8 = t8 < nvalid, vt9 = t9 < nvalid;
-      if (KIND == kFP4) {
-        constexpr int VB = C::VPT / 2;  // code bytes per thread and token
-        const uint8_t* svs = st + 2 * C::KBYTES + C::SBYTES;
-        uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
-#pragma unroll
-        for (int q4 = 0; q4 < VB / 4; ++q4) {
-          w0[q4] = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
-          w1[q4] = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
-          w8[q4] = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
-          w9[q4] = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
-        }
-        const int gv = (r * C::VPT) >> 5;
-        const uint32_t b0 = svs[t0 * C::SROW + gv], b1 = svs[t1 * C::SROW + gv];
-        const uint32_t b8 = svs[t8 * C::SROW + gv], b9 = svs[t9 * C::SROW + gv];
-        uint32_t ev = 0;
-        ev = (vt0 && b0 != 0xFFu && b0 > ev) ? b0 : ev;
-        ev = (vt1 && b1 != 0xFFu && b1 > ev) ? b1 : ev;
-        ev = (vt8 && b8 != 0xFFu && b8 > ev) ? b8 : ev;
-        ev = (vt9 && b9 != 0xFFu && b9 > ev) ? b9 : ev;
-        const uint32_t RVc = __reduce_max_sync(kFull, ev);
-        if (RVc > RV) {
-          const float f = pow2i(static_cast<int>(RV) - static_cast<int>(RVc));
-#pragma unroll
-          for (int m = 0; m < C::NMMA; ++m) {
-            O[m][0] *= f; O[m][1] *= f; O[m][2] *= f; O[m][3] *= f;
-          }
-          RV = RVc;
-        }
-        const uint32_t mv01 = pack_f16x2(group_mult(b0, RV, vt0), group_mult(b1, RV, vt1));
-        const uint32_t mv89 = pack_f16x2(group_mult(b8, RV, vt8), group_mult(b9, RV, vt9));
-#pragma unroll
-        for (int q4 = 0; q4 < VB / 4; ++q4) {
-          // Pair the same channel of two tokens in one byte (low nibble = lower token).
-          const uint32_t lo01 = (w0[q4] & 0x0F0F0F0Fu) | ((w1[q4] & 0x0F0F0F0Fu) << 4);
-          const uint32_t hi01 = ((w0[q4] >> 4) & 0x0F0F0F0Fu) | (w1[q4] & 0xF0F0F0F0u);
-          const uint32_t lo89 = (w8[q4] & 0x0F0F0F0Fu) | ((w9[q4] & 0x0F0F0F0Fu) << 4);
-          const uint32_t hi89 = ((w8[q4] >> 4) & 0x0F0F0F0Fu) | (w9[q4] & 0xF0F0F0F0u);
-          uint32_t A0[4], A1[4], A2[4], A3[4];
-          e2m1x8_to_f16x2(lo01, A0);
-          e2m1x8_to_f16x2(hi01, A1);
-          e2m1x8_to_f16x2(lo89, A2);
-          e2m1x8_to_f16x2(hi89, A3);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            pv_unit(O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89),
-                    hmul2(A3[k], mv89), bp);
-        }
-      } else if (KIND == kFP8) {
-        constexpr int VB = C::VPT;  // bytes per thread and token
-        uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
-#pragma unroll
-        for (int q4 = 0; q4 < VB / 4; ++q4) {
-          w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4] : 0u;
-          w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4] : 0u;
-          w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4] : 0u;
-          w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4] : 0u;
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < VB / 4; ++q4) {
-          const uint32_t x01 = __byte_perm(w0[q4], w1[q4], 0x5140), y01 = __byte_perm(w0[q4], w1[q4], 0x7362);
-          const uint32_t x89 = __byte_perm(w8[q4], w9[q4], 0x5140), y89 = __byte_perm(w8[q4], w9[q4], 0x7362);
-          pv_unit(O[2 * q4], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(x89),
-                  e4m3x2_to_f16x2(x89 >> 16), bp);
-          pv_unit(O[2 * q4 + 1], e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16), e4m3x2_to_f16x2(y89),
-                  e4m3x2_to_f16x2(y89 >> 16), bp);
-        }
-      } else {
-        constexpr int VW = C::VPT / 2;  // bf16 pairs per thread and token
-        uint32_t w0[VW], w1[VW], w8[VW], w9[VW];
-#pragma unroll
-        for (int q4 = 0; q4 < VW; ++q4) {
-          w0[q4] = vt0 ? reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * C::VPT * 2)[q4] : 0u;
-          w1[q4] = vt1 ? reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * C::VPT * 2)[q4] : 0u;
-          w8[q4] = vt8 ? reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * C::VPT * 2)[q4] : 0u;
-          w9[q4] = vt9 ? reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * C::VPT * 2)[q4] : 0u;
-        }
-        auto bf2h = [](uint32_t w) {  // bf16x2 -> f16x2
-          return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-        };
-#pragma unroll
-        for (int m = 0; m < VW; ++m) {
-          pv_unit(O[m], bf2h(__byte_perm(w0[m], w1[m], 0x5410)), bf2h(__byte_perm(w0[m], w1[m], 0x7632)),
-                  bf2h(__byte_perm(w8[m], w9[m], 0x5410)), bf2h(__byte_perm(w8[m], w9[m], 0x7632)), bp);
-        }
+        if (KIND == kFP4) unit_fp4<D, true>(st, nvalid, r, c, qb, fac, S);
+        else unit_anchor<KIND, D, true>(st, nvalid, r, c, qb, fac, S);
       }
       __syncwarp();
       if (lane == 0 && i + C::NST < nw) {
@@ -503,26 +610,26 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     // ---------------------------------------------- combine the 4 warps
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      L0 += __shfl_xor_sync(kFull, L0, o);
-      L1 += __shfl_xor_sync(kFull, L1, o);
+      S.L0 += __shfl_xor_sync(kFull, S.L0, o);
+      S.L1 += __shfl_xor_sync(kFull, S.L1, o);
     }
+    if (KIND == kFP4 && __any_sync(kFull, S.bad != 0)) S.L0 = S.L1 = __int_as_float(0x7FC00000);
     if (r == 0) {
-      comb_ml[(warp * kHB + 2 * c) * 2] = M0;
-      comb_ml[(warp * kHB + 2 * c) * 2 + 1] = L0;
-      comb_ml[(warp * kHB + 2 * c + 1) * 2] = M1;
-      comb_ml[(warp * kHB + 2 * c + 1) * 2 + 1] = L1;
+      comb_ml[(warp * kHB + 2 * c) * 2] = S.M0;
+      comb_ml[(warp * kHB + 2 * c) * 2 + 1] = S.L0;
+      comb_ml[(warp * kHB + 2 * c + 1) * 2] = S.M1;
+      comb_ml[(warp * kHB + 2 * c + 1) * 2 + 1] = S.L1;
     }
-    const float osc = (KIND == kFP4 ? pow2i(static_cast<int>(RV) - 127 - 15)
-                                    : (KIND == kFP8 ? p.v_scale * (1.f / 32768.f) : 1.f / 32768.f));
+    const float osc = KIND == kFP4 ? pow2i(static_cast<int>(S.RV) - 127) : (KIND == kFP8 ? p.v_scale : 1.f);
     {
       float* co = comb_o + warp * kHB * D;
 #pragma unroll
       for (int m = 0; m < C::NMMA; ++m) {
         const int ch0 = r * C::VPT + 2 * m, ch1 = ch0 + 1;
-        co[(2 * c) * D + ch0] = O[m][0] * osc;
-        co[(2 * c + 1) * D + ch0] = O[m][1] * osc;
-        co[(2 * c) * D + ch1] = O[m][2] * osc;
-        co[(2 * c + 1) * D + ch1] = O[m][3] * osc;
+        co[(2 * c) * D + ch0] = S.O[m][0] * osc;
+        co[(2 * c + 1) * D + ch0] = S.O[m][1] * osc;
+        co[(2 * c) * D + ch1] = S.O[m][2] * osc;
+        co[(2 * c + 1) * D + ch1] = S.O[m][3] * osc;
       }
     }
     __syncthreads();
@@ -654,17 +761,16 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
 
 // Test hook: the decode prologue alone.  One warp handles 8 query rows.
 template <int D>
-__global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out, const __grid_constant__ uqh::SignMasks sm) {
+__global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out,
+                                  const __grid_constant__ uqh::SignMasks sm) {
   const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8 + r;
-  DecParams p;
-  p.sign = sm;
-  uint32_t qb[D / 16][2];
-  uint8_t bytes[D / 4];
   const bool valid = row < n;
-  rotated_query_fp8<D>(q + (valid ? row : 0) * D, valid, c, p, qb, bytes);
+  uint32_t bytes[D / 16];
+  rotated_query_bytes<D>(q + (valid ? row : 0) * D, valid, c, sm, bytes);
   if (valid)
-    for (int e = 0; e < D / 4; ++e) out[row * D + c * (D / 4) + e] = bytes[e];
+    for (int e = 0; e < D / 16; ++e)
+      *reinterpret_cast<uint32_t*>(out + row * D + c * (D / 4) + 4 * e) = bytes[e];
 }
 
 // ------------------------------------------------------------------ host
