@@ -187,6 +187,31 @@ uq_status uq_decode_attention_bf16(const void* q, const uq_cache* cache,
                                    float sm_scale, float* out, void* workspace,
                                    size_t workspace_bytes, cudaStream_t stream);
 
+/* The same decode attention for callers that cannot allocate device memory
+ * (no counterpart on the pages; a deployment convenience of this library).
+ * Some callers cannot provide the workspace: their device memory belongs to
+ * another allocator (a framework's caching allocator or a fixed arena) that
+ * they may not draw from here, and they may not call cudaMalloc either.  This
+ * entry point takes no workspace and allocates nothing: it uses an 8 MiB
+ * scratch array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   - Arguments, results and errors are those of uq_decode_attention.
+ *   - Batch shapes whose smallest workspace exceeds 8 MiB (roughly more than
+ *     2000 (sequence, kv head) pairs at head_dim 128) return UQ_ERR_WORKSPACE
+ *     before anything is enqueued; use uq_decode_attention for those.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one scratch array, and it keeps the last
+ *     call's contents.  Nothing in it needs to start at zero: every entry a
+ *     call reads was written earlier in the same call.  Calls that overlap on
+ *     the GPU (different streams, no ordering between them) race on the
+ *     scratch and give wrong results; order them on one stream or with
+ *     events. */
+uq_status uq_decode_attention_noalloc(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                      int32_t num_q_heads, float sm_scale, float* out, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns UQ_OK, UQ_ERR_DEVICE_TIMEOUT or UQ_ERR_DEVICE_BOUNDS (the
  * first error recorded since the last call), or UQ_ERR_CUDA. */

@@ -50,6 +50,7 @@ _sig = {
     "uq_decode_attention": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_fp8": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_bf16": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_decode_attention_noalloc": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp]),
     "uq_check_device_status": (C.c_int, [_vp]),
     "uq_status_string": (C.c_char_p, [C.c_int]),
     "uq_rotation_signs": (None, [C.c_uint64, _i32, _vp]),
