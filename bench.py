@@ -347,6 +347,54 @@ def run_uq(args):
     print(json.dumps(line), flush=True)
 
 
+def run_decode_only(args):
+    """Decode of one of the other workloads (tiny, gqa8k, mixed, prefix128k):
+    the cache is filled untimed, then each step decodes one query token per
+    sequence.  Used for per-workload numbers and for profiling."""
+    ws, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import ue8m0_kv_cache_gb300 as uq
+    import workloads
+    w = workloads.make(args.workload)
+    cache = uq.KVCache(uq.FP4_UE8M0, w.num_pages, w.Hkv, w.ps, w.D, device=dev)
+    for b in range(w.B):
+        start = w.shared_prefix if (b > 0 and w.shared_prefix) else 0
+        for t0 in range(start, w.seq_lens[b], 8192):
+            n = min(8192, w.seq_lens[b] - t0)
+            k, v = w.kv(b, t0, n, device=dev)
+            uq.uq_quantize_append(k, v, torch.from_numpy(w.slots(b, t0, n)).to(dev), cache)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+    q = w.q(0, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    wsp = uq.workspace(w.B, w.Hq, w.Hkv, w.D, dev)
+    for _ in range(args.warmup):
+        uq.uq_decode_attention(q, cache, bt, sl, out=out, workspace=wsp)
+    torch.cuda.synchronize()
+    t0, t1 = _event_pair()
+    stream = torch.cuda.current_stream()
+    t0.record(stream)
+    for _ in range(args.steps):
+        uq.uq_decode_attention(q, cache, bt, sl, out=out, workspace=wsp)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert uq.uq_check_device_status() == 0
+    dt = t0.elapsed_time(t1) * 1e-3 / args.steps
+    logical = sum(w.seq_lens) * w.Hkv * FP4_BYTES_PER_TOKEN_HEAD
+    unique_tokens = sum(w.seq_lens) - (w.B - 1) * w.shared_prefix
+    hbm, kind = _peaks()
+    line = {"metric": "decode tokens/s (one attention layer)", "value": w.B / dt, "unit": "decode tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "dtype": "e2m1/ue8m0 cache", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "tokens": sum(w.seq_lens)},
+            "kv_GB_per_s_logical": logical / dt / 1e9,
+            "kv_GB_per_s_unique": unique_tokens * w.Hkv * FP4_BYTES_PER_TOKEN_HEAD / dt / 1e9,
+            "frac_of_peak_logical": logical / dt / 1e9 / hbm, "peak": hbm, "peak_kind": kind,
+            "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -355,10 +403,14 @@ def main():
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--no-anchors", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="append64k",
+                    choices=["append64k", "tiny", "gqa8k", "mixed", "prefix128k"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "append64k":
+        run_decode_only(args)
     else:
         run_uq(args)
 

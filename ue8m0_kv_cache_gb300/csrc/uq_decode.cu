@@ -52,7 +52,11 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHB = 8;      // query heads per block (the MMA's n)
 constexpr int kChunk = 16;  // tokens per work unit (the MMA's m for QK)
-constexpr float kPShift = 15.f;  // p is carried as p * 2^15 (fits f16, keeps the lo part normal)
+// The running max M is only raised when a logit exceeds it by more than
+// kSlack (log2 units); p = 2^(t - M) may then reach 2^kSlack.  p is carried as
+// p * 2^kPShift, so the largest value is 2^(kSlack + kPShift) = 2^15, inside f16.
+constexpr float kSlack = 8.f;
+constexpr float kPShift = 7.f;
 
 enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
 
@@ -169,13 +173,17 @@ __device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool v
 template <int NMMA>
 __device__ __forceinline__ void softmax_unit(const float (&t)[4], float& M0, float& M1, float& L0, float& L1,
                                              float (&O)[NMMA][4], uint32_t (&bp)[4]) {
+  // M does not have to be the exact max: p = 2^(t - M) stays exact for any M,
+  // and the same M scales O and L.  It is raised (with a reduction of the
+  // unit max across the 8 token rows and a rescale of O) only when some logit
+  // exceeds it by more than kSlack, which after the first units is rare.
   float mc0 = fmaxf(t[0], t[2]), mc1 = fmaxf(t[1], t[3]);
+  if (__any_sync(kFull, mc0 > M0 + kSlack || mc1 > M1 + kSlack)) {
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
-    mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
-  }
-  if (__any_sync(kFull, mc0 > M0 || mc1 > M1)) {
+    for (int o = 4; o < 32; o <<= 1) {
+      mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+      mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+    }
     const float n0 = fmaxf(M0, mc0), n1 = fmaxf(M1, mc1);
     const float a0 = ex2(M0 - n0), a1 = ex2(M1 - n1);
     M0 = n0;
@@ -210,10 +218,8 @@ __device__ __forceinline__ void pv_unit(float (&o)[4], uint32_t a0, uint32_t a1,
   float t[4];
   mma_f16_zc(t, a0, a1, a2, a3, bp[0], bp[1]);
   mma_f16(t, a0, a1, a2, a3, bp[2], bp[3]);
-  o[0] += t[0];
-  o[1] += t[1];
-  o[2] += t[2];
-  o[3] += t[3];
+  add2(o[0], o[1], t[0], t[1]);
+  add2(o[2], o[3], t[2], t[3]);
 }
 
 // Per-warp running state of one segment.
@@ -222,6 +228,7 @@ struct WarpState {
   float M0, M1, L0, L1;
   float O[NMMA][4];
   uint32_t RV;   // FP4: reference exponent byte of O
+  float rref;    // FP4: 2^(127 - RV)
   uint32_t bad;  // FP4: a non-finite group was seen
 };
 
@@ -274,10 +281,8 @@ __device__ __forceinline__ void unit_fp4(const uint8_t* st, int nvalid, int r, i
     else if (g == 1) { f0 = scale_of<1>(ksw0); f1 = scale_of<1>(ksw1); }
     else if (g == 2) { f0 = scale_of<2>(ksw0); f1 = scale_of<2>(ksw1); }
     else { f0 = scale_of<3>(ksw0); f1 = scale_of<3>(ksw1); }
-    s[0] = fmaf(acc[0], f0, s[0]);
-    s[1] = fmaf(acc[1], f0, s[1]);
-    s[2] = fmaf(acc[2], f1, s[2]);
-    s[3] = fmaf(acc[3], f1, s[3]);
+    fma2(s[0], s[1], acc[0], acc[1], f0);
+    fma2(s[2], s[3], acc[2], acc[3], f1);
   }
   float t[4] = {s[0] * sl2e, s[1] * sl2e, s[2] * sl2e, s[3] * sl2e};
   uint32_t kbad;
@@ -325,9 +330,10 @@ __device__ __forceinline__ void unit_fp4(const uint8_t* st, int nvalid, int r, i
       S.O[m][0] *= f; S.O[m][1] *= f; S.O[m][2] *= f; S.O[m][3] *= f;
     }
     S.RV = RVc;
+    S.rref = pow2i(127 - static_cast<int>(RVc));
   }
   // 2^(byte-127) * 2^(127-RV), both factors exact powers of two (byte 0 gives 0).
-  const float rref = pow2i(127 - static_cast<int>(S.RV));
+  const float rref = S.rref;
   float f0 = __uint_as_float(b0 << 23) * rref, f1 = __uint_as_float(b1 << 23) * rref;
   float f8 = __uint_as_float(b8 << 23) * rref, f9 = __uint_as_float(b9 << 23) * rref;
   if (TAIL) {
@@ -548,31 +554,53 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
 
     const int nw = seg > warp ? (seg - warp + kWarps - 1) / kWarps : 0;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
-    auto issue = [&](int i, int slot) {
-      const int tok0 = (j0 + warp + i * kWarps) * kChunk;
-      int page = bt_row[tok0 >> p.ps_log2];
-      if (page < 0 || page >= p.num_pages) {
-        record_error(p.status, kErrBounds);
-        page = 0;
+    // Lane l holds the page of this warp's unit (32*k + l); refreshed every 32
+    // units, so the copy issue never waits on a dependent global load.
+    auto page_of_lane = [&](int i) {
+      int page = 0;
+      if (i < nw) {
+        page = bt_row[((j0 + warp + i * kWarps) * kChunk) >> p.ps_log2];
+        if (page < 0 || page >= p.num_pages) {
+          record_error(p.status, kErrBounds);
+          page = 0;
+        }
       }
-      const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
-      uint8_t* st = myring + slot * C::STAGE;
-      uint64_t* bar = &mybars[slot];
-      mbar_arrive_expect_tx(bar, C::STAGE);
-      bulk_g2s(st, p.kc + row0 * C::KROW, C::KBYTES, bar);
-      bulk_g2s(st + C::KBYTES, p.vc + row0 * C::KROW, C::KBYTES, bar);
-      if (KIND == kFP4) {
-        bulk_g2s(st + 2 * C::KBYTES, p.ks + row0 * C::SROW, C::SBYTES, bar);
-        bulk_g2s(st + 2 * C::KBYTES + C::SBYTES, p.vs + row0 * C::SROW, C::SBYTES, bar);
-      }
+      return page;
     };
-    if (lane == 0)
-      for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST);
+    int pf = page_of_lane(lane);
+    // Lanes 0..3 issue the unit's four bulk copies (K codes, V codes, K
+    // scales, V scales) in one pass; lane-specific source bases, row sizes and
+    // stage offsets are fixed for the segment.
+    const uint8_t* cp_base = p.kc;
+    uint32_t cp_row = C::KROW, cp_off = 0, cp_bytes = C::KBYTES;
+    if (lane == 1) { cp_base = p.vc; cp_off = C::KBYTES; }
+    if (KIND == kFP4 && lane == 2) { cp_base = p.ks; cp_row = C::SROW; cp_off = 2 * C::KBYTES; cp_bytes = C::SBYTES; }
+    if (KIND == kFP4 && lane == 3) {
+      cp_base = p.vs; cp_row = C::SROW; cp_off = 2 * C::KBYTES + C::SBYTES; cp_bytes = C::SBYTES;
+    }
+    constexpr int kCopies = KIND == kFP4 ? 4 : 2;
+    const uint32_t ring_u32 = smem_u32(myring), bars_u32 = smem_u32(mybars);
+    auto issue = [&](int i, int slot, int page) {
+      const int tok0 = (j0 + warp + i * kWarps) * kChunk;
+      const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
+      const uint32_t bar = bars_u32 + 8u * slot;
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(uint32_t(C::STAGE))
+                     : "memory");
+      if (lane < kCopies)
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                ring_u32 + slot * uint32_t(C::STAGE) + cp_off),
+            "l"(cp_base + row0 * cp_row), "r"(cp_bytes), "r"(bar)
+            : "memory");
+    };
+    for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST, __shfl_sync(kFull, pf, i));
 
     WarpState<C::NMMA> S;
     S.M0 = S.M1 = -INFINITY;
     S.L0 = S.L1 = 0.f;
     S.RV = 0;
+    S.rref = pow2i(127);
     S.bad = 0;
 #pragma unroll
     for (int m = 0; m < C::NMMA; ++m) S.O[m][0] = S.O[m][1] = S.O[m][2] = S.O[m][3] = 0.f;
@@ -600,10 +628,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         if (KIND == kFP4) unit_fp4<D, true>(st, nvalid, r, c, qb, fac, S);
         else unit_anchor<KIND, D, true>(st, nvalid, r, c, qb, fac, S);
       }
-      __syncwarp();
-      if (lane == 0 && i + C::NST < nw) {
+      const int nx = i + C::NST;  // warp-uniform
+      if (nx < nw) {
+        if ((nx & 31) == 0) pf = page_of_lane(nx + lane);
+        const int page = __shfl_sync(kFull, pf, nx & 31);
+        __syncwarp();
         fence_proxy_async();
-        issue(i + C::NST, slot);
+        issue(nx, slot, page);
       }
     }
 

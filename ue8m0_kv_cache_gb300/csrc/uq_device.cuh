@@ -36,6 +36,20 @@ __device__ __forceinline__ void bfly2(float& a0, float& a1, float& b0, float& b1
       : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
 }
 
+// (a0, a1) += (b0, b1), round to nearest (one packed instruction).
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 A, B;\n\tmov.b64 A, {%0, %1};\n\tmov.b64 B, {%2, %3};\n\t"
+      "add.rn.f32x2 A, A, B;\n\tmov.b64 {%0, %1}, A;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+
+// (a0, a1) = (b0, b1) * (s, s) + (a0, a1), round to nearest once.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, float s) {
+  asm("{\n\t.reg .b64 A, B, S;\n\tmov.b64 A, {%0, %1};\n\tmov.b64 B, {%2, %3};\n\t"
+      "mov.b64 S, {%4, %4};\n\tfma.rn.f32x2 A, B, S, A;\n\tmov.b64 {%0, %1}, A;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1), "f"(s));
+}
+
 // (a0, a1) * (s, s), round to nearest.
 __device__ __forceinline__ void mul2(float& a0, float& a1, float s) {
   asm("{\n\t.reg .b64 A, S;\n\tmov.b64 A, {%0, %1};\n\tmov.b64 S, {%2, %2};\n\t"
@@ -204,13 +218,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One try_wait.  The suspend-time hint (in ns) lets the hardware park the
+// thread until the phase completes (or the hint runs out) instead of having it
+// spin on the barrier, which would take issue slots from the warps that work.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
