@@ -60,6 +60,10 @@ constexpr float kPShift = 7.f;
 
 enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
 
+#ifndef UQ_FP4_MINB
+#define UQ_FP4_MINB 3  // resident blocks per SM the FP4 decode is compiled for
+#endif
+
 template <int KIND, int D>
 struct DC {
   static constexpr int KROW = KIND == kFP4 ? D / 2 : (KIND == kFP8 ? D : 2 * D);  // bytes/token row
@@ -232,96 +236,136 @@ struct WarpState {
   uint32_t bad;  // FP4: a non-finite group was seen
 };
 
-// One 16-token unit, FP4 cache.  TAIL: the unit may hold fewer than 16 valid
-// tokens (the last unit of a sequence); masked tokens get logit -inf and
-// value multiplier 0, whatever bytes their slots hold.
-template <int D, bool TAIL>
-__device__ __forceinline__ void unit_fp4(const uint8_t* st, int nvalid, int r, int c,
-                                         const uint32_t (&qb)[D / 16][2], float sl2e,
-                                         WarpState<D / 16>& S) {
+// NU consecutive units of this warp, FP4 cache, processed together: their
+// QK^T chains are independent, the softmax bookkeeping (vote, rare reduction)
+// is shared, and P.V accumulates all of them into one fresh accumulator per
+// 16-channel block before the fp32 add.  TAIL: the last of the NU units may
+// hold fewer than 16 valid tokens (a sequence's last unit); its masked tokens
+// get logit -inf and value multiplier 0, whatever bytes their slots hold.
+template <int D, int NU, bool TAIL>
+__device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nvalid_last, int r, int c,
+                                          const uint32_t (&qb)[D / 16][2], float sl2e, WarpState<D / 16>& S) {
   using C = DC<kFP4, D>;
   constexpr int NG = C::NG;
-  const uint8_t* skc = st;
-  const uint8_t* svc = st + C::KBYTES;
-  const uint8_t* sks = st + 2 * C::KBYTES;
-  const uint8_t* svs = sks + C::SBYTES;
+  constexpr int VB = C::VPT / 2;  // V code bytes per thread and token
+  const int t0 = 2 * c, t1 = t0 + 1, t8 = t0 + 8, t9 = t0 + 9;
 
   // ---- QK^T per group: thread (r, c) holds word c of every group of tokens r, r+8
-  uint32_t kw0[NG], kw1[NG];
-  if (NG == 4) {
-    const uint4 x0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 16);
-    const uint4 x1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 16);
-    kw0[0] = x0.x; kw0[1] = x0.y; kw0[2 % NG] = x0.z; kw0[3 % NG] = x0.w;
-    kw1[0] = x1.x; kw1[1] = x1.y; kw1[2 % NG] = x1.z; kw1[3 % NG] = x1.w;
-  } else {
-    const uint2 x0 = *reinterpret_cast<const uint2*>(skc + r * C::KROW + c * 8);
-    const uint2 x1 = *reinterpret_cast<const uint2*>(skc + (r + 8) * C::KROW + c * 8);
-    kw0[0] = x0.x; kw0[1 % NG] = x0.y;
-    kw1[0] = x1.x; kw1[1 % NG] = x1.y;
-  }
-  uint32_t ksw0, ksw1;  // the token's NG scale bytes
-  if (NG == 4) {
-    ksw0 = *reinterpret_cast<const uint32_t*>(sks + r * 4);
-    ksw1 = *reinterpret_cast<const uint32_t*>(sks + (r + 8) * 4);
-  } else {
-    ksw0 = *reinterpret_cast<const uint16_t*>(sks + r * 2);
-    ksw1 = *reinterpret_cast<const uint16_t*>(sks + (r + 8) * 2);
-  }
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  float t[NU][4];
+  uint32_t kbad = 0;
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    uint32_t h0[4], h1[4];
-    e2m1x8_to_f16x2(kw0[g], h0);
-    e2m1x8_to_f16x2(kw1[g], h1);
-    float acc[4];
-    mma_f16_zc(acc, h0[0], h1[0], h0[1], h1[1], qb[2 * g][0], qb[2 * g][1]);
-    mma_f16(acc, h0[2], h1[2], h0[3], h1[3], qb[2 * g + 1][0], qb[2 * g + 1][1]);
-    float f0, f1;
-    if (g == 0) { f0 = scale_of<0>(ksw0); f1 = scale_of<0>(ksw1); }
-    else if (g == 1) { f0 = scale_of<1>(ksw0); f1 = scale_of<1>(ksw1); }
-    else if (g == 2) { f0 = scale_of<2>(ksw0); f1 = scale_of<2>(ksw1); }
-    else { f0 = scale_of<3>(ksw0); f1 = scale_of<3>(ksw1); }
-    fma2(s[0], s[1], acc[0], acc[1], f0);
-    fma2(s[2], s[3], acc[2], acc[3], f1);
-  }
-  float t[4] = {s[0] * sl2e, s[1] * sl2e, s[2] * sl2e, s[3] * sl2e};
-  uint32_t kbad;
-  if (TAIL) {
-    const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
-    if (!v0) { t[0] = -INFINITY; t[1] = -INFINITY; }
-    if (!v1) { t[2] = -INFINITY; t[3] = -INFINITY; }
-    kbad = (v0 ? has_ff(ksw0) : 0u) | (v1 ? has_ff(ksw1) : 0u);
-  } else {
-    kbad = has_ff(ksw0) | has_ff(ksw1);
+  for (int u = 0; u < NU; ++u) {
+    const uint8_t* skc = st[u];
+    const uint8_t* sks = st[u] + 2 * C::KBYTES;
+    uint32_t kw0[NG], kw1[NG], ksw0, ksw1;
+    if (NG == 4) {
+      const uint4 x0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 16);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 16);
+      kw0[0] = x0.x; kw0[1] = x0.y; kw0[2 % NG] = x0.z; kw0[3 % NG] = x0.w;
+      kw1[0] = x1.x; kw1[1] = x1.y; kw1[2 % NG] = x1.z; kw1[3 % NG] = x1.w;
+      ksw0 = *reinterpret_cast<const uint32_t*>(sks + r * 4);
+      ksw1 = *reinterpret_cast<const uint32_t*>(sks + (r + 8) * 4);
+    } else {
+      const uint2 x0 = *reinterpret_cast<const uint2*>(skc + r * C::KROW + c * 8);
+      const uint2 x1 = *reinterpret_cast<const uint2*>(skc + (r + 8) * C::KROW + c * 8);
+      kw0[0] = x0.x; kw0[1 % NG] = x0.y;
+      kw1[0] = x1.x; kw1[1 % NG] = x1.y;
+      ksw0 = *reinterpret_cast<const uint16_t*>(sks + r * 2);
+      ksw1 = *reinterpret_cast<const uint16_t*>(sks + (r + 8) * 2);
+    }
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      uint32_t h0[4], h1[4];
+      e2m1x8_to_f16x2(kw0[g], h0);
+      e2m1x8_to_f16x2(kw1[g], h1);
+      float acc[4];
+      mma_f16_zc(acc, h0[0], h1[0], h0[1], h1[1], qb[2 * g][0], qb[2 * g][1]);
+      mma_f16(acc, h0[2], h1[2], h0[3], h1[3], qb[2 * g + 1][0], qb[2 * g + 1][1]);
+      float f0, f1;
+      if (g == 0) { f0 = scale_of<0>(ksw0); f1 = scale_of<0>(ksw1); }
+      else if (g == 1) { f0 = scale_of<1>(ksw0); f1 = scale_of<1>(ksw1); }
+      else if (g == 2) { f0 = scale_of<2>(ksw0); f1 = scale_of<2>(ksw1); }
+      else { f0 = scale_of<3>(ksw0); f1 = scale_of<3>(ksw1); }
+      fma2(sa[0], sa[1], acc[0], acc[1], f0);
+      fma2(sa[2], sa[3], acc[2], acc[3], f1);
+    }
+    t[u][0] = sa[0] * sl2e; t[u][1] = sa[1] * sl2e; t[u][2] = sa[2] * sl2e; t[u][3] = sa[3] * sl2e;
+    if (TAIL && u == NU - 1) {
+      const bool v0 = r < nvalid_last, v1 = r + 8 < nvalid_last;
+      if (!v0) { t[u][0] = -INFINITY; t[u][1] = -INFINITY; }
+      if (!v1) { t[u][2] = -INFINITY; t[u][3] = -INFINITY; }
+      kbad |= (v0 ? has_ff(ksw0) : 0u) | (v1 ? has_ff(ksw1) : 0u);
+    } else {
+      kbad |= has_ff(ksw0) | has_ff(ksw1);
+    }
   }
 
-  uint32_t bp[4];
-  softmax_unit<C::NMMA>(t, S.M0, S.M1, S.L0, S.L1, S.O, bp);
+  // ---- softmax over the NU units
+  float mc0 = -INFINITY, mc1 = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    mc0 = fmaxf(mc0, fmaxf(t[u][0], t[u][2]));
+    mc1 = fmaxf(mc1, fmaxf(t[u][1], t[u][3]));
+  }
+  if (__any_sync(kFull, mc0 > S.M0 + kSlack || mc1 > S.M1 + kSlack)) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+      mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+    }
+    const float n0 = fmaxf(S.M0, mc0), n1 = fmaxf(S.M1, mc1);
+    const float a0 = ex2(S.M0 - n0), a1 = ex2(S.M1 - n1);
+    S.M0 = n0;
+    S.M1 = n1;
+    S.L0 *= a0;
+    S.L1 *= a1;
+#pragma unroll
+    for (int m = 0; m < C::NMMA; ++m) {
+      S.O[m][0] *= a0; S.O[m][1] *= a1; S.O[m][2] *= a0; S.O[m][3] *= a1;
+    }
+  }
+  uint32_t bp[NU][4];
+  {
+    const float s0 = kPShift - S.M0, s1 = kPShift - S.M1;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const float p0 = ex2(t[u][0] + s0), p1 = ex2(t[u][1] + s1), p2 = ex2(t[u][2] + s0), p3 = ex2(t[u][3] + s1);
+      S.L0 += p0 + p2;
+      S.L1 += p1 + p3;
+      const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+      const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+      const float h2 = __uint_as_float(__float_as_uint(p2) & 0xFFFFE000u);
+      const float h3 = __uint_as_float(__float_as_uint(p3) & 0xFFFFE000u);
+      bp[u][0] = movmatrix_trans(pack_f16x2(h0, h1));
+      bp[u][1] = movmatrix_trans(pack_f16x2(h2, h3));
+      bp[u][2] = movmatrix_trans(pack_f16x2(p0 - h0, p1 - h1));
+      bp[u][3] = movmatrix_trans(pack_f16x2(p2 - h2, p3 - h3));
+    }
+  }
 
   // ---- P.V: thread (r, c) takes channels r*VPT.. of tokens 2c, 2c+1, 2c+8, 2c+9
-  constexpr int VB = C::VPT / 2;  // code bytes per thread and token
-  const int t0 = 2 * c, t1 = t0 + 1, t8 = t0 + 8, t9 = t0 + 9;
-  uint32_t w0[VB / 4], w1[VB / 4], w8[VB / 4], w9[VB / 4];
-#pragma unroll
-  for (int q4 = 0; q4 < VB / 4; ++q4) {
-    w0[q4] = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
-    w1[q4] = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
-    w8[q4] = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
-    w9[q4] = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
-  }
   const int gv = (r * C::VPT) >> 5;
-  uint32_t b0 = svs[t0 * C::SROW + gv], b1 = svs[t1 * C::SROW + gv];
-  uint32_t b8 = svs[t8 * C::SROW + gv], b9 = svs[t9 * C::SROW + gv];
-  if (TAIL) {
-    if (t0 >= nvalid) b0 = 0;
-    if (t1 >= nvalid) b1 = 0;
-    if (t8 >= nvalid) b8 = 0;
-    if (t9 >= nvalid) b9 = 0;
+  uint32_t vb[NU][4];
+  uint32_t bmax = 0;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const uint8_t* svs = st[u] + 2 * C::KBYTES + C::SBYTES;
+    vb[u][0] = svs[t0 * C::SROW + gv];
+    vb[u][1] = svs[t1 * C::SROW + gv];
+    vb[u][2] = svs[t8 * C::SROW + gv];
+    vb[u][3] = svs[t9 * C::SROW + gv];
+    if (TAIL && u == NU - 1) {
+      if (t0 >= nvalid_last) vb[u][0] = 0;
+      if (t1 >= nvalid_last) vb[u][1] = 0;
+      if (t8 >= nvalid_last) vb[u][2] = 0;
+      if (t9 >= nvalid_last) vb[u][3] = 0;
+    }
+    bmax = max(bmax, max(max(vb[u][0], vb[u][1]), max(vb[u][2], vb[u][3])));
   }
   // Reference exponent RV = running max of the V scale bytes, so that every
   // multiplier 2^(byte - RV) is <= 1 and fits f16 together with the codes.
-  const uint32_t bmax = max(max(b0, b1), max(b8, b9));
-  const uint32_t vbad = bmax == 0xFFu ? 1u : 0u;
+  S.bad |= kbad | (bmax == 0xFFu ? 1u : 0u);
   const uint32_t RVc = __reduce_max_sync(kFull, bmax);
   if (RVc > S.RV) {
     const float f = pow2i(static_cast<int>(S.RV) - static_cast<int>(RVc));
@@ -332,34 +376,51 @@ __device__ __forceinline__ void unit_fp4(const uint8_t* st, int nvalid, int r, i
     S.RV = RVc;
     S.rref = pow2i(127 - static_cast<int>(RVc));
   }
-  // 2^(byte-127) * 2^(127-RV), both factors exact powers of two (byte 0 gives 0).
-  const float rref = S.rref;
-  float f0 = __uint_as_float(b0 << 23) * rref, f1 = __uint_as_float(b1 << 23) * rref;
-  float f8 = __uint_as_float(b8 << 23) * rref, f9 = __uint_as_float(b9 << 23) * rref;
-  if (TAIL) {
-    if (t0 >= nvalid) f0 = 0.f;
-    if (t1 >= nvalid) f1 = 0.f;
-    if (t8 >= nvalid) f8 = 0.f;
-    if (t9 >= nvalid) f9 = 0.f;
+  uint32_t mv01[NU], mv89[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    // 2^(byte-127) * 2^(127-RV), both exact powers of two (byte 0 gives 0).
+    float f0 = __uint_as_float(vb[u][0] << 23) * S.rref, f1 = __uint_as_float(vb[u][1] << 23) * S.rref;
+    float f8 = __uint_as_float(vb[u][2] << 23) * S.rref, f9 = __uint_as_float(vb[u][3] << 23) * S.rref;
+    if (TAIL && u == NU - 1) {
+      if (t0 >= nvalid_last) f0 = 0.f;
+      if (t1 >= nvalid_last) f1 = 0.f;
+      if (t8 >= nvalid_last) f8 = 0.f;
+      if (t9 >= nvalid_last) f9 = 0.f;
+    }
+    mv01[u] = pack_f16x2(f0, f1);
+    mv89[u] = pack_f16x2(f8, f9);
   }
-  const uint32_t mv01 = pack_f16x2(f0, f1), mv89 = pack_f16x2(f8, f9);
-  S.bad |= kbad | vbad;
 #pragma unroll
   for (int q4 = 0; q4 < VB / 4; ++q4) {
-    // Pair the same channel of two tokens in one byte (low nibble = lower token).
-    const uint32_t lo01 = (w0[q4] & 0x0F0F0F0Fu) | ((w1[q4] & 0x0F0F0F0Fu) << 4);
-    const uint32_t hi01 = ((w0[q4] >> 4) & 0x0F0F0F0Fu) | (w1[q4] & 0xF0F0F0F0u);
-    const uint32_t lo89 = (w8[q4] & 0x0F0F0F0Fu) | ((w9[q4] & 0x0F0F0F0Fu) << 4);
-    const uint32_t hi89 = ((w8[q4] >> 4) & 0x0F0F0F0Fu) | (w9[q4] & 0xF0F0F0F0u);
-    uint32_t A0[4], A1[4], A2[4], A3[4];
-    e2m1x8_to_f16x2(lo01, A0);
-    e2m1x8_to_f16x2(hi01, A1);
-    e2m1x8_to_f16x2(lo89, A2);
-    e2m1x8_to_f16x2(hi89, A3);
+    uint32_t A[NU][4][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      pv_unit(S.O[4 * q4 + k], hmul2(A0[k], mv01), hmul2(A1[k], mv01), hmul2(A2[k], mv89), hmul2(A3[k], mv89),
-              bp);
+    for (int u = 0; u < NU; ++u) {
+      const uint8_t* svc = st[u] + C::KBYTES;
+      const uint32_t w0 = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
+      const uint32_t w1 = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
+      const uint32_t w8 = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
+      const uint32_t w9 = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
+      // Pair the same channel of two tokens in one byte (low nibble = lower token).
+      e2m1x8_to_f16x2((w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4), A[u][0]);
+      e2m1x8_to_f16x2(((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u), A[u][1]);
+      e2m1x8_to_f16x2((w8 & 0x0F0F0F0Fu) | ((w9 & 0x0F0F0F0Fu) << 4), A[u][2]);
+      e2m1x8_to_f16x2(((w8 >> 4) & 0x0F0F0F0Fu) | (w9 & 0xF0F0F0F0u), A[u][3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float acc[4];
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const uint32_t a0 = hmul2(A[u][0][k], mv01[u]), a1 = hmul2(A[u][1][k], mv01[u]);
+        const uint32_t a2 = hmul2(A[u][2][k], mv89[u]), a3 = hmul2(A[u][3][k], mv89[u]);
+        if (u == 0) mma_f16_zc(acc, a0, a1, a2, a3, bp[u][0], bp[u][1]);
+        else mma_f16(acc, a0, a1, a2, a3, bp[u][0], bp[u][1]);
+        mma_f16(acc, a0, a1, a2, a3, bp[u][2], bp[u][3]);
+      }
+      add2(S.O[4 * q4 + k][0], S.O[4 * q4 + k][1], acc[0], acc[1]);
+      add2(S.O[4 * q4 + k][2], S.O[4 * q4 + k][3], acc[2], acc[3]);
+    }
   }
 }
 
@@ -448,7 +509,7 @@ __device__ __forceinline__ void unit_anchor(const uint8_t* st, int nvalid, int r
 }
 
 template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) decode_kernel(const __grid_constant__ DecParams p) {
   using C = DC<KIND, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -606,36 +667,50 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     for (int m = 0; m < C::NMMA; ++m) S.O[m][0] = S.O[m][1] = S.O[m][2] = S.O[m][3] = 0.f;
     const float fac = KIND == kFP8 ? p.sl2e * p.k_scale : p.sl2e;
 
-    for (int i = 0; i < nw; ++i, ++it) {
-      const int slot = it % C::NST;
-      const bool ok = __all_sync(kFull, mbar_wait(&mybars[slot], (it / C::NST) & 1, kWaitBudget));
-      if (!ok) {
+    for (int i = 0; i < nw;) {
+      // FP4 takes two units per step (independent work for the scheduler);
+      // the anchors, and an odd last unit, take one.
+      const int nu = (KIND == kFP4 && i + 1 < nw) ? 2 : 1;  // warp-uniform
+      bool ok = mbar_wait(&mybars[it % C::NST], (it / C::NST) & 1, kWaitBudget);
+      if (nu == 2) ok = ok && mbar_wait(&mybars[(it + 1) % C::NST], ((it + 1) / C::NST) & 1, kWaitBudget);
+      if (!__all_sync(kFull, ok)) {
         if (lane == 0) {
           record_error(p.status, kErrTimeout);
-          for (int k = i + 1; k < (nw < i + C::NST ? nw : i + C::NST); ++k)
+          for (int k = i; k < (nw < i + C::NST ? nw : i + C::NST); ++k)
             mbar_wait(&mybars[(it + k - i) % C::NST], ((it + k - i) / C::NST) & 1, kWaitBudget);
         }
         abort_flag = 1;
         it += nw - i;
         break;
       }
-      const uint8_t* st = myring + slot * C::STAGE;
-      const int nvalid = L - (j0 + warp + i * kWarps) * kChunk;
-      if (nvalid >= kChunk) {
-        if (KIND == kFP4) unit_fp4<D, false>(st, kChunk, r, c, qb, fac, S);
-        else unit_anchor<KIND, D, false>(st, kChunk, r, c, qb, fac, S);
+      const uint8_t* st0 = myring + (it % C::NST) * C::STAGE;
+      const int nvalid = L - (j0 + warp + (i + nu - 1) * kWarps) * kChunk;  // of the last unit taken
+      if (KIND == kFP4) {
+        if (nu == 2) {
+          const uint8_t* const sts[2] = {st0, myring + ((it + 1) % C::NST) * C::STAGE};
+          if (nvalid >= kChunk) units_fp4<D, 2, false>(sts, kChunk, r, c, qb, fac, S);
+          else units_fp4<D, 2, true>(sts, nvalid, r, c, qb, fac, S);
+        } else {
+          const uint8_t* const sts[1] = {st0};
+          if (nvalid >= kChunk) units_fp4<D, 1, false>(sts, kChunk, r, c, qb, fac, S);
+          else units_fp4<D, 1, true>(sts, nvalid, r, c, qb, fac, S);
+        }
       } else {
-        if (KIND == kFP4) unit_fp4<D, true>(st, nvalid, r, c, qb, fac, S);
-        else unit_anchor<KIND, D, true>(st, nvalid, r, c, qb, fac, S);
+        if (nvalid >= kChunk) unit_anchor<KIND, D, false>(st0, kChunk, r, c, qb, fac, S);
+        else unit_anchor<KIND, D, true>(st0, nvalid, r, c, qb, fac, S);
       }
-      const int nx = i + C::NST;  // warp-uniform
-      if (nx < nw) {
-        if ((nx & 31) == 0) pf = page_of_lane(nx + lane);
-        const int page = __shfl_sync(kFull, pf, nx & 31);
-        __syncwarp();
-        fence_proxy_async();
-        issue(nx, slot, page);
+      __syncwarp();
+      for (int k = 0; k < nu; ++k) {
+        const int nx = i + k + C::NST;  // warp-uniform
+        if (nx < nw) {
+          if ((nx & 31) == 0) pf = page_of_lane(nx + lane);
+          const int page = __shfl_sync(kFull, pf, nx & 31);
+          fence_proxy_async();
+          issue(nx, (it + k) % C::NST, page);
+        }
       }
+      i += nu;
+      it += nu;
     }
 
     // ---------------------------------------------- combine the 4 warps
