@@ -278,14 +278,8 @@ def run_uq(args):
     ms_per_step = total / steps * 1e3
     value = ws * B * steps / total
     achieved = kv_bytes / dec_t / 1e9
-    prof = {}
-    try:
-        with open(os.path.join(ROOT, "profiles", "decode_fp4_traffic.json")) as f:
-            prof = json.load(f)
-    except Exception:
-        pass
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": prof.get("traffic_bytes_per_launch"), "peak_kind": peak_kind,
+                "traffic": _captured_traffic(B * HKV * ctx_mean), "peak_kind": peak_kind,
                 "kernel": "uq_decode_attention (decode + merge launches), FP4 cache",
                 "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_t * 1e3,
                 "frac_of_nominal_8TBps": achieved / 8000.0}
@@ -345,6 +339,24 @@ def run_uq(args):
             "kv_GB_per_s": achieved, "quantize": quantize, "anchors": anchors, "roofline": roofline,
             "clocks": clk, "e2e": e2e, "gpu_launches": 3 * steps, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
+
+
+def _captured_traffic(token_heads):
+    """DRAM bytes (read + write) of one FP4 decode launch over `token_heads`
+    token-heads, scaled from the ncu capture summarised in
+    profiles/decode_fp4_traffic.json.  None when that capture is missing or was
+    taken on a different version of the decode source."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_fp4_traffic.json")) as f:
+            prof = json.load(f)
+        with open(os.path.join(ROOT, "ue8m0_kv_cache_gb300", "csrc", "uq_decode.cu"), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    if prof.get("source_sha256_16") != sha:
+        return None
+    return float(prof["dram_bytes_per_token_head"]) * token_heads
 
 
 def run_decode_only(args):
