@@ -27,6 +27,7 @@ namespace {
 using namespace uqd;
 
 constexpr int kRows = 64;             // token-head rows per tile
+constexpr int64_t kSmallAppendRows = 1024;  // token-head rows up to which the direct-load kernel is used
 constexpr int kAppendThreads = 2 * kRows;  // one thread per K row and one per V row
 
 struct AppendParams {
@@ -203,6 +204,60 @@ __global__ void __launch_bounds__(kAppendThreads)
   }
 }
 
+// Small appends (a decode step's new tokens): one thread per K or V row read
+// straight from global memory, no tensor maps -- the per-call host work of the
+// tiled kernel would cost more than the copy.
+template <int D, bool F32>
+__global__ void __launch_bounds__(128) fp4_append_small_kernel(const void* k, const void* v,
+                                                               const __grid_constant__ AppendParams p) {
+  pdl_wait();
+  const int64_t nrows = p.ntok * p.hkv;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= 2 * nrows) return;
+  const bool is_v = gid >= nrows;
+  const int64_t R = is_v ? gid - nrows : gid;
+  float u[D];
+  if (F32) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(is_v ? v : k) + R * D);
+#pragma unroll
+    for (int j = 0; j < D / 4; ++j) {
+      const uint4 w = src[j];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) u[4 * j + e] = __uint_as_float(ws[e] ^ p.sign.m[4 * j + e]);
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(is_v ? v : k) + R * D);
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      const uint4 w = src[j];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        u[8 * j + 2 * e] = __uint_as_float((ws[e] << 16) ^ p.sign.m[8 * j + 2 * e]);
+        u[8 * j + 2 * e + 1] = __uint_as_float((ws[e] & 0xFFFF0000u) ^ p.sign.m[8 * j + 2 * e + 1]);
+      }
+    }
+  }
+  rotate_regs<D>(u);
+  uint32_t codes[D / 8], scales;
+  quantize_regs<D>(u, codes, scales);
+  const int64_t t = R / p.hkv;
+  const int h = static_cast<int>(R - t * p.hkv);
+  const int64_t slot = p.slots[t];
+  if (slot >= p.num_slots) {
+    record_error(p.status, kErrBounds);
+  } else if (slot >= 0) {
+    const int64_t page = slot >> p.ps_log2;
+    const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
+    if (is_v)
+      store_row<D, false>(p.vc, p.vs, dst, codes, scales);
+    else
+      store_row<D, true>(p.kc, p.ks, dst, codes, scales);
+  }
+  pdl_trigger();
+}
+
 // ------------------------------------------------------------ FP8 / BF16
 struct AnchorParams {
   const void* k;
@@ -373,9 +428,6 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
                             const uq_cache& c, cudaStream_t s) {
   const int64_t nrows = ntok * c.num_kv_heads;
   if (nrows >= (int64_t(1) << 31) - kRows) return UQ_ERR_UNSUPPORTED;
-  CUtensorMap mk, mv;
-  if (!encode_rows(&mk, k, nrows, c.head_dim, in_fp32) || !encode_rows(&mv, v, nrows, c.head_dim, in_fp32))
-    return UQ_ERR_CUDA;
   AppendParams p;
   p.slots = slots;
   p.ntok = ntok;
@@ -389,6 +441,20 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
   p.status = status_word();
   make_sign_masks(c.rot_seed, c.head_dim, &p.sign);
   if (!p.status) return UQ_ERR_CUDA;
+  if (nrows <= kSmallAppendRows) {
+    const unsigned grid = static_cast<unsigned>((2 * nrows + 127) / 128);
+    cudaError_t e;
+    if (c.head_dim == 128)
+      e = in_fp32 ? launch_pdl(fp4_append_small_kernel<128, true>, grid, 128, 0, s, k, v, p)
+                  : launch_pdl(fp4_append_small_kernel<128, false>, grid, 128, 0, s, k, v, p);
+    else
+      e = in_fp32 ? launch_pdl(fp4_append_small_kernel<64, true>, grid, 128, 0, s, k, v, p)
+                  : launch_pdl(fp4_append_small_kernel<64, false>, grid, 128, 0, s, k, v, p);
+    return cuda_status(e);
+  }
+  CUtensorMap mk, mv;
+  if (!encode_rows(&mk, k, nrows, c.head_dim, in_fp32) || !encode_rows(&mv, v, nrows, c.head_dim, in_fp32))
+    return UQ_ERR_CUDA;
   if (c.head_dim == 128)
     return in_fp32 ? run_fp4_append<128, true>(mk, mv, p, nrows, s) : run_fp4_append<128, false>(mk, mv, p, nrows, s);
   return in_fp32 ? run_fp4_append<64, true>(mk, mv, p, nrows, s) : run_fp4_append<64, false>(mk, mv, p, nrows, s);

@@ -521,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, c = lane & 3;
   const int ps_mask = (1 << p.ps_log2) - 1;
+  pdl_wait();  // the cache, query and block table are written by earlier kernels
 
   // Prefix sums of 16-token units per sequence.
   if (warp == 0) {
@@ -774,6 +775,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
     if (abort_flag) break;
     u += seg;
   }
+  pdl_trigger();  // the merge may now be scheduled; it still waits for the whole grid
 }
 
 // Log-sum-exp merge of the partials of each (sequence, query head), then the
@@ -794,6 +796,7 @@ template <int KIND, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int EPL = D / 32;
   const int lane = threadIdx.x & 31;
+  pdl_wait();  // the partials come from the decode kernel
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= static_cast<int64_t>(p.B) * p.Hq) return;
   const int b = static_cast<int>(row / p.Hq), h = static_cast<int>(row - static_cast<int64_t>(b) * p.Hq);
@@ -863,6 +866,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
   float* dst = p.out + row * D + lane * EPL;
 #pragma unroll
   for (int e = 0; e < EPL; ++e) dst[e] = o[e];
+  pdl_trigger();
 }
 
 // Test hook: the decode prologue alone.  One warp handles 8 query rows.
@@ -894,16 +898,34 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   auto kern = decode_kernel<KIND, D>;
   const uqh::DevInfo& di = uqh::dev_info();
   if (smem > di.smem_optin) return UQ_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return UQ_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
-    return UQ_ERR_CUDA;
+  // The attribute is per device; it is raised to the largest size seen so far.
+  static int cfg_dev = -1;
+  static size_t cfg_smem = 0;
+  static int per_sm = 0;
+  if (cfg_dev != di.device || smem > cfg_smem) {
+    const size_t want = smem > cfg_smem || cfg_dev != di.device ? smem : cfg_smem;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)want) != cudaSuccess)
+      return UQ_ERR_CUDA;
+    // occupancy is set by registers and the fixed part of shared memory
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::smem_fixed) != cudaSuccess ||
+        per_sm < 1)
+      return UQ_ERR_CUDA;
+    cfg_dev = di.device;
+    cfg_smem = want;
+  }
   // Workspace: [pair info][per-slot (m, l) x 8 heads][per-slot O x 8 heads]
   const size_t info = ws_info_bytes(pairs);
   if (a.ws_bytes < info) return UQ_ERR_WORKSPACE;
   const int64_t fit = static_cast<int64_t>((a.ws_bytes - info) / ws_slot_bytes(D)) - pairs;
+  // At least kMinUnitsPerBlock of the batch's largest possible number of
+  // 16-token units per block: every block's partial is one more step of the
+  // merge, which for a small batch costs more than the parallelism gains.
+  constexpr int64_t kMinUnitsPerBlock = 4;
+  const int64_t max_units =
+      static_cast<int64_t>(a.batch) * ((static_cast<int64_t>(a.max_pages) * c.page_size + kChunk - 1) / kChunk) *
+      c.num_kv_heads * nhb;
   int64_t grid = std::min<int64_t>(static_cast<int64_t>(di.sms) * per_sm, fit);
+  grid = std::min<int64_t>(grid, std::max<int64_t>(1, max_units / kMinUnitsPerBlock));
   if (grid < 1) return UQ_ERR_WORKSPACE;
   const int64_t slots = grid + pairs;
   DecParams p;
@@ -934,8 +956,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.status = uqh::status_word();
   if (!p.status) return UQ_ERR_CUDA;
   if (KIND == kFP4) uqh::make_sign_masks(c.rot_seed, D, &p.sign);
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
+  if (uqh::launch_pdl(kern, (unsigned)grid, kThreads, smem, s, p) != cudaSuccess) return UQ_ERR_CUDA;
 
   MergeParams mp;
   mp.ws_o = p.ws_o;
@@ -954,8 +975,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   mp.status = p.status;
   mp.sign = p.sign;
   const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads;
-  merge_kernel<KIND, D><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(mp);
-  return uqh::cuda_status(cudaGetLastError());
+  return uqh::cuda_status(uqh::launch_pdl(merge_kernel<KIND, D>, (unsigned)((rows + 3) / 4), 128, 0, s, mp));
 }
 
 }  // namespace

@@ -262,6 +262,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while the previous kernel in the
+// stream is still running; it must wait for that kernel (and its memory) before
+// touching global memory.  Without the attribute the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled (it still waits for this one to finish).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Record the first device-side error (1-based uq_status value) in the status word.
 __device__ __forceinline__ void record_error(unsigned int* status, unsigned int code) {
   if (status) atomicCAS(status, 0u, code);
