@@ -175,6 +175,32 @@ uq_status uq_decode_attention(const void* q, const uq_cache* cache, const int32_
                               int32_t num_q_heads, float sm_scale, float* out, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * One decode step with the step's new tokens appended in the same launch
+ * (FP4 cache only): for each sequence b with new_slots[b] >= 0, the token
+ * k_new[b], v_new[b] is quantised exactly as uq_quantize_append would and
+ * written to slot new_slots[b]; then the attention of uq_decode_attention is
+ * computed over seq_lens[b] tokens, which include the new token as the last
+ * one.  The pages describe the cache as written once per token and read by
+ * the decode kernel ([UQ-review] §4.2); doing both in one launch saves the
+ * separate append kernel of every decode step.
+ * k_new, v_new : device [batch][num_kv_heads][head_dim], bf16 or fp32 as
+ *                in_dtype says, 16-byte aligned.
+ * new_slots    : device int64 [batch], 8-byte aligned; the physical slot of
+ *                sequence b's new token, which must be where block_table
+ *                places its logical position seq_lens[b] - 1 (a mismatch is
+ *                recorded as UQ_ERR_DEVICE_BOUNDS and that token is not
+ *                written); -1 = no new token (seq_lens[b] must then not
+ *                count one).
+ * Other arguments and errors as uq_decode_attention.  UQ_ERR_UNSUPPORTED for
+ * FP8 / BF16 caches.
+ */
+uq_status uq_decode_attention_append(const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
+                                     const int64_t* new_slots, const uq_cache* cache, const int32_t* block_table,
+                                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                     int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
+
 /* The anchors: identical to uq_decode_attention but require cache->dtype to be
  * UQ_FP8_E4M3 (resp. UQ_BF16) and return UQ_ERR_INVALID_ARG otherwise. */
 uq_status uq_decode_attention_fp8(const void* q, const uq_cache* cache, const int32_t* block_table,

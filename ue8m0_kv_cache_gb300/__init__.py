@@ -51,6 +51,8 @@ _sig = {
     "uq_decode_attention_fp8": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_bf16": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_noalloc": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp]),
+    "uq_decode_attention_append": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
+                                             _vp, _sz, _vp]),
     "uq_check_device_status": (C.c_int, [_vp]),
     "uq_status_string": (C.c_char_p, [C.c_int]),
     "uq_rotation_signs": (None, [C.c_uint64, _i32, _vp]),
@@ -174,6 +176,33 @@ def uq_decode_attention(q, cache, block_table, seq_lens, out=None, workspace=Non
     """Decode attention of q [B][Hq][D] bf16 over `cache`; returns fp32 [B][Hq][D]."""
     return _decode(_lib.uq_decode_attention, "uq_decode_attention", q, cache, block_table, seq_lens, out,
                    workspace, sm_scale, stream)
+
+
+def uq_decode_attention_append(q, k_new, v_new, new_slots, cache, block_table, seq_lens, out=None, workspace=None,
+                               sm_scale=0.0, stream=None):
+    """One decode step: append each sequence's new token (k_new, v_new [B][Hkv][D], bf16 or fp32) at
+    new_slots [B] (int64, -1 = none), then decode attention over seq_lens (which count the new token)."""
+    if k_new.dtype not in (torch.bfloat16, torch.float32) or v_new.dtype != k_new.dtype:
+        raise ValueError("k_new, v_new must both be bf16 or fp32")
+    _need(k_new, k_new.dtype, "k_new")
+    _need(v_new, k_new.dtype, "v_new")
+    _need(new_slots, torch.int64, "new_slots")
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    if (tuple(k_new.shape) != (B, cache.num_kv_heads, cache.head_dim) or v_new.shape != k_new.shape
+            or new_slots.numel() != B or D != cache.head_dim or block_table.shape[0] != B or seq_lens.numel() != B):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    ws = workspace if workspace is not None else globals()["workspace"](B, Hq, cache.num_kv_heads, D, q.device)
+    _check(_lib.uq_decode_attention_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), IN_FP32 if k_new.dtype == torch.float32 else IN_BF16, _ptr(new_slots),
+        C.byref(cache.struct), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, float(sm_scale),
+        _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "uq_decode_attention_append")
+    return out
 
 
 def uq_decode_attention_fp8(q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0, stream=None):

@@ -98,7 +98,9 @@ uq_status check_cache(const uq_cache* c) {
 
 uq_status decode_common(const void* q, const uq_cache* cache, const int32_t* block_table, int32_t max_pages,
                         const int32_t* seq_lens, int32_t batch, int32_t hq, float sm_scale, float* out,
-                        void* ws, size_t ws_bytes, cudaStream_t stream, int want_dtype) {
+                        void* ws, size_t ws_bytes, cudaStream_t stream, int want_dtype,
+                        const void* k_new = nullptr, const void* v_new = nullptr,
+                        const int64_t* new_slots = nullptr, int new_f32 = 0) {
   uq_status st = check_cache(cache);
   if (st != UQ_OK) return st;
   if (want_dtype >= 0 && cache->dtype != want_dtype) return UQ_ERR_INVALID_ARG;
@@ -111,6 +113,10 @@ uq_status decode_common(const void* q, const uq_cache* cache, const int32_t* blo
   if ((int64_t)max_pages * cache->page_size >= (int64_t(1) << 31)) return UQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return UQ_ERR_ALIGNMENT;
   uqh::DecodeArgs a{q, cache, block_table, max_pages, seq_lens, batch, hq, sm_scale, out, ws, ws_bytes};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_slots = new_slots;
+  a.new_f32 = new_f32;
   return uqh::launch_decode(a, stream);
 }
 
@@ -166,6 +172,22 @@ uq_status uq_decode_attention(const void* q, const uq_cache* cache, const int32_
                               size_t workspace_bytes, cudaStream_t stream) {
   return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
                        workspace, workspace_bytes, stream, -1);
+}
+
+uq_status uq_decode_attention_append(const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
+                                     const int64_t* new_slots, const uq_cache* cache, const int32_t* block_table,
+                                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                     int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  if (!cache) return UQ_ERR_INVALID_ARG;
+  if (cache->dtype != UQ_FP4_UE8M0) return UQ_ERR_UNSUPPORTED;
+  if (in_dtype != UQ_IN_BF16 && in_dtype != UQ_IN_FP32) return UQ_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new || !new_slots)) return UQ_ERR_INVALID_ARG;
+  if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return UQ_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(new_slots) & 7u) != 0) return UQ_ERR_ALIGNMENT;
+  return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                       workspace, workspace_bytes, stream, UQ_FP4_UE8M0, k_new, v_new, new_slots,
+                       in_dtype == UQ_IN_FP32 ? 1 : 0);
 }
 
 uq_status uq_decode_attention_fp8(const void* q, const uq_cache* cache, const int32_t* block_table,

@@ -98,6 +98,17 @@ struct DecParams {
   int64_t* ws_units;
   unsigned int* status;
   uqh::SignMasks sign;
+  // Fused append (FP4): new token of sequence b at physical slot new_slots[b]
+  // (-1: none), rows k_new/v_new [B][Hkv][D] (bf16, or fp32 if new_f32).
+  const void* k_new;
+  const void* v_new;
+  const int64_t* new_slots;
+  int new_f32;
+  int64_t num_slots;
+  uint8_t* wkc;
+  uint8_t* wks;
+  uint8_t* wvc;
+  uint8_t* wvs;
 };
 
 // Contiguous range [lo, hi) of the U units that block c of C handles.
@@ -137,20 +148,28 @@ __device__ __forceinline__ int clamp_len(const DecParams& p, int b) {
   return L;
 }
 
-// The rotated E4M3 query of one head, channels [c*D/4, (c+1)*D/4), packed 4
-// bytes per word: the same fp32 butterfly as the append path, spread over
-// the 4 threads of a quad (strides below D/4 inside a thread, the last two
-// across the quad), then E4M3 round to nearest even, saturating.
-template <int D>
-__device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool valid, int c,
-                                                    const uqh::SignMasks& sign, uint32_t (&out)[D / 16]) {
+// R1 rotation of one row of D values spread over the 4 threads of a quad:
+// thread c ends with rotated channels [c*D/4, (c+1)*D/4) in fp32.  The same
+// fp32 butterfly as the append path (strides below D/4 inside a thread, the
+// last two across the quad, ascending), then the 1/sqrt(D) factor.  Every
+// lane of the warp must call it (the cross-quad steps are warp shuffles).
+template <int D, bool F32>
+__device__ __forceinline__ void rotate_quad(const void* row, bool valid, int c, const uqh::SignMasks& sign,
+                                            float (&x)[D / 4]) {
   constexpr int CPT = D / 4;
-  float x[CPT];
+  if (F32) {
 #pragma unroll
-  for (int e = 0; e < CPT; e += 2) {
-    const uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(qrow + c * CPT + e) : 0u;
-    x[e] = __uint_as_float((w << 16) ^ sign.m[c * CPT + e]);
-    x[e + 1] = __uint_as_float((w & 0xFFFF0000u) ^ sign.m[c * CPT + e + 1]);
+    for (int e = 0; e < CPT; ++e) {
+      const uint32_t w = valid ? reinterpret_cast<const uint32_t*>(row)[c * CPT + e] : 0u;
+      x[e] = __uint_as_float(w ^ sign.m[c * CPT + e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < CPT; e += 2) {
+      const uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(row) + c * CPT + e) : 0u;
+      x[e] = __uint_as_float((w << 16) ^ sign.m[c * CPT + e]);
+      x[e + 1] = __uint_as_float((w & 0xFFFF0000u) ^ sign.m[c * CPT + e + 1]);
+    }
   }
   fwht_regs<CPT>(x);
 #pragma unroll
@@ -165,9 +184,42 @@ __device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool v
   const float s = inv_sqrt_d<D>();
 #pragma unroll
   for (int e = 0; e < CPT; e += 2) mul2(x[e], x[e + 1], s);
+}
+
+// The rotated E4M3 query of one head, channels [c*D/4, (c+1)*D/4), packed 4
+// bytes per word, E4M3 round to nearest even, saturating.
+template <int D>
+__device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool valid, int c,
+                                                    const uqh::SignMasks& sign, uint32_t (&out)[D / 16]) {
+  float x[D / 4];
+  rotate_quad<D, false>(qrow, valid, c, sign, x);
 #pragma unroll
   for (int m = 0; m < D / 16; ++m)
     out[m] = cvt_e4m3x2(x[4 * m], x[4 * m + 1]) | (cvt_e4m3x2(x[4 * m + 2], x[4 * m + 3]) << 16);
+}
+
+// R2 + R3 on the rotated channels a quad thread holds (32 for D = 128, one
+// group; 16 for D = 64, half a group shared with the neighbouring thread):
+// the group's UE8M0 byte and the E2M1 codes of this thread's channels, with
+// the same arithmetic as the append path.  All lanes must call it.
+template <int D>
+__device__ __forceinline__ void quantize_quad(float (&x)[D / 4], uint32_t (&codes)[D / 32], uint32_t& byte) {
+  constexpr int CPT = D / 4;
+  float mx = max_abs_nan(x[0], x[1]);
+#pragma unroll
+  for (int i = 2; i < CPT; ++i) mx = max_abs_nan(mx, x[i]);
+  if (CPT < 32) mx = max_abs_nan(mx, __shfl_xor_sync(kFull, mx, 1));
+  byte = scale_byte(fabsf(mx));
+  const float inv = inv_scale(byte == 0xFFu ? 127u : byte);
+#pragma unroll
+  for (int i = 0; i < CPT; i += 2) mul2(x[i], x[i + 1], inv);
+#pragma unroll
+  for (int w = 0; w < CPT / 8; ++w) {
+    const float* e = &x[8 * w];
+    const uint32_t word = cvt_e2m1x2(e[0], e[1]) | (cvt_e2m1x2(e[2], e[3]) << 8) |
+                          (cvt_e2m1x2(e[4], e[5]) << 16) | (cvt_e2m1x2(e[6], e[7]) << 24);
+    codes[w] = byte == 0xFFu ? 0u : word;
+  }
 }
 
 // Softmax update for one unit: t[] are the log2-domain logits of tokens
@@ -508,6 +560,77 @@ __device__ __forceinline__ void unit_anchor(const uint8_t* st, int nvalid, int r
   }
 }
 
+// Fused append: the warp that will take a sequence's last unit quantises that
+// sequence's new token (position L - 1, physical slot new_slots[b]) itself --
+// lanes 0-3 the K row, lanes 4-7 the V row of this kv head, with the append
+// path's arithmetic -- and writes both rows to the cache and, in the stage's
+// own layout, to a scratch row in shared memory.  It runs at the start of the
+// segment, while the first copies are in flight; when the last unit's stage
+// lands (its copy of that slot may predate the write), patch_stage puts the
+// scratch row over the token's row.  So no separate append launch precedes
+// the decode.  A slot that disagrees with the block table's position for the
+// token is an error (recorded; nothing written, returns false).
+template <int D>
+__device__ __noinline__ bool fused_append(const DecParams& p, uint8_t* scratch, int b, int kvh, int L,
+                                          const int32_t* bt_row, int lane) {
+  using C = DC<kFP4, D>;
+  constexpr int CPT = D / 4, NG = D / 32, NW = CPT / 8;  // channels, groups, code words per thread
+  const int64_t slot = p.new_slots[b];
+  if (slot < 0) return false;
+  const int tok = L - 1;
+  const int ps_mask = (1 << p.ps_log2) - 1;
+  const int64_t bslot = tok < 0 ? -1 : (static_cast<int64_t>(bt_row[tok >> p.ps_log2]) << p.ps_log2) + (tok & ps_mask);
+  if (slot != bslot || slot >= p.num_slots) {
+    if (lane == 0) record_error(p.status, kErrBounds);
+    return false;
+  }
+  const int quad = lane >> 2, c = lane & 3;
+  const bool is_v = quad == 1, active = quad < 2;
+  const size_t esz = p.new_f32 ? 4 : 2;
+  const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) +
+                       (static_cast<int64_t>(b) * p.Hkv + kvh) * D * esz;
+  float x[CPT];
+  if (p.new_f32) rotate_quad<D, true>(src, active, c, p.sign, x);
+  else rotate_quad<D, false>(src, active, c, p.sign, x);
+  uint32_t codes[NW], byte;
+  quantize_quad<D>(x, codes, byte);
+  if (active) {
+    const int64_t dst = (((slot >> p.ps_log2) * p.Hkv + kvh) << p.ps_log2) + (slot & ps_mask);
+    uint8_t* gcodes = (is_v ? p.wvc : p.wkc) + dst * C::KROW;
+    uint8_t* scodes = scratch + (is_v ? C::KROW : 0);
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      const int nw = c * NW + k;                           // natural word index in the row
+      const int pos = is_v ? nw : NG * (nw & 3) + (nw >> 2);  // K rows: group-interleaved words
+      *reinterpret_cast<uint32_t*>(gcodes + 4 * pos) = codes[k];
+      *reinterpret_cast<uint32_t*>(scodes + 4 * pos) = codes[k];
+    }
+    if (CPT == 32 || (c & 1) == 0) {
+      const int g = c * CPT / 32;
+      (is_v ? p.wvs : p.wks)[dst * NG + g] = static_cast<uint8_t>(byte);
+      scratch[2 * C::KROW + (is_v ? C::SROW : 0) + g] = static_cast<uint8_t>(byte);
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
+// Copies the scratch row written by fused_append over row r of a landed stage.
+template <int D>
+__device__ __forceinline__ void patch_stage(const uint8_t* scratch, uint8_t* st, int r, int lane) {
+  using C = DC<kFP4, D>;
+  constexpr int KW = C::KROW / 4;  // code words per row
+  if (lane < 2 * KW) {
+    const int v = lane >= KW, wd = lane - (v ? KW : 0);
+    *reinterpret_cast<uint32_t*>(st + (v ? C::KBYTES : 0) + r * C::KROW + 4 * wd) =
+        *reinterpret_cast<const uint32_t*>(scratch + (v ? C::KROW : 0) + 4 * wd);
+  }
+  if (lane < 2 * C::SROW) {
+    const int v = lane >= C::SROW, g = lane - (v ? C::SROW : 0);
+    st[2 * C::KBYTES + (v ? C::SBYTES : 0) + r * C::SROW + g] = scratch[2 * C::KROW + (v ? C::SROW : 0) + g];
+  }
+}
+
 template <int KIND, int D>
 __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) decode_kernel(const __grid_constant__ DecParams p) {
   using C = DC<KIND, D>;
@@ -657,6 +780,13 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
             : "memory");
     };
     for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST, __shfl_sync(kFull, pf, i));
+    // The new token (fused append) is quantised while those copies fly; its
+    // scratch row sits in this warp's slice of the combine buffer, past the
+    // query bytes, which is free until the combine.
+    int fa_unit = -1;  // index of the unit whose stage takes the scratch row
+    uint8_t* fa_scratch = reinterpret_cast<uint8_t*>(comb_o + warp * kHB * D) + kHB * D;
+    if (KIND == kFP4 && p.new_slots != nullptr && nw > 0 && j0 + warp + (nw - 1) * kWarps == nb - 1)
+      if (fused_append<D>(p, fa_scratch, b, kvh, L, bt_row, lane)) fa_unit = nw - 1;
 
     WarpState<C::NMMA> S;
     S.M0 = S.M1 = -INFINITY;
@@ -683,6 +813,11 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
         abort_flag = 1;
         it += nw - i;
         break;
+      }
+      if (KIND == kFP4 && fa_unit >= 0 && fa_unit - i < nu) {
+        patch_stage<D>(fa_scratch, myring + ((it + fa_unit - i) % C::NST) * C::STAGE, (L - 1) & (kChunk - 1), lane);
+        fa_unit = -1;
+        __syncwarp();
       }
       const uint8_t* st0 = myring + (it % C::NST) * C::STAGE;
       const int nvalid = L - (j0 + warp + (i + nu - 1) * kWarps) * kChunk;  // of the last unit taken
@@ -956,6 +1091,15 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.status = uqh::status_word();
   if (!p.status) return UQ_ERR_CUDA;
   if (KIND == kFP4) uqh::make_sign_masks(c.rot_seed, D, &p.sign);
+  p.k_new = a.k_new;
+  p.v_new = a.v_new;
+  p.new_slots = a.new_slots;
+  p.new_f32 = a.new_f32;
+  p.num_slots = static_cast<int64_t>(c.num_pages) * c.page_size;
+  p.wkc = static_cast<uint8_t*>(c.k_codes);
+  p.wks = static_cast<uint8_t*>(c.k_scales);
+  p.wvc = static_cast<uint8_t*>(c.v_codes);
+  p.wvs = static_cast<uint8_t*>(c.v_scales);
   if (uqh::launch_pdl(kern, (unsigned)grid, kThreads, smem, s, p) != cudaSuccess) return UQ_ERR_CUDA;
 
   MergeParams mp;

@@ -82,6 +82,11 @@ struct DecodeArgs {
   float* out;
   void* ws;
   size_t ws_bytes;
+  // fused append of one new token per sequence (FP4; new_slots == nullptr: none)
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* new_slots = nullptr;
+  int new_f32 = 0;
 };
 size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas);
 int decode_max_ctas();
