@@ -52,16 +52,63 @@ def _peaks():
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region."""
+    """SM clock and clock-event-reason sampler for the timed region.
+
+    Polls NVML (libnvidia-ml, read-only queries) from a thread every 2 ms, so
+    a timed region of a few tens of milliseconds still gets a dozen samples;
+    falls back to `nvidia-smi -lms 100` where the library cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock event reason bits of the NVML API
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, pci_bus_id=None):
         self.gpu = gpu_index
         self.p = None
+        self.nv = None
+        self.samples = []
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                # NVML numbers all GPUs of the machine; the PCI bus id names the one CUDA uses
+                ok = pci_bus_id is not None and \
+                    nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) == 0
+                if ok or nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(h)) == 0:
+                    self.nv, self.h, self.ct = nv, h, ctypes
+        except Exception:
+            self.nv = None
+
+    def _read(self):
+        ct, nv = self.ct, self.nv
+        mhz, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:  # 1 = SM clock
+            return None
+        nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self.h, ct.byref(rs))
+        return mhz.value, mx.value, rs.value
 
     def start(self):
+        self.samples = []
+        if self.nv is not None:
+            import threading
+            self.stop_ev = threading.Event()
+
+            def run():
+                while not self.stop_ev.is_set():
+                    r = self._read()
+                    if r is not None:
+                        self.samples.append(r)
+                    time.sleep(0.002)
+            self.th = threading.Thread(target=run, daemon=True)
+            self.th.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 1.0:
+                time.sleep(0.001)
+            return
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
                                        "--format=csv,noheader,nounits", "-lms", "100"],
@@ -70,6 +117,14 @@ class Clocks:
             self.p = None
 
     def stop(self):
+        if self.nv is not None:
+            self.stop_ev.set()
+            self.th.join(timeout=5)
+            sm = [s[0] for s in self.samples]
+            reasons = sorted(n for n, bit in self.BITS.items() if any(s[2] & bit for s in self.samples))
+            return {"sm_mhz": float(np.median(sm)) if sm else None,
+                    "sm_max_mhz": float(self.samples[-1][1]) if sm else None, "reasons": reasons,
+                    "samples": len(sm), "source": "nvml, 2 ms"}
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         self.p.terminate()
@@ -93,7 +148,16 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 100 ms"}
+
+
+def _pci_bus_id(dev):
+    """'dddddddd:bb:dd.0' of a CUDA device, or None where torch does not report it."""
+    pr = torch.cuda.get_device_properties(dev)
+    try:
+        return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except AttributeError:
+        return None
 
 
 def _cpu_baseline(w, seconds_hint=True):
@@ -270,7 +334,7 @@ def run_uq(args):
         dec = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e-3
         return total, dec, (clk if clocks else None)
 
-    clocks = Clocks(local if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0)
+    clocks = Clocks(local if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0, _pci_bus_id(dev))
     total, dec_t, clk = timed("fp4", clocks)
     assert uq.uq_check_device_status() == 0
     if ws > 1:

@@ -739,8 +739,9 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
 
     const int nw = seg > warp ? (seg - warp + kWarps - 1) / kWarps : 0;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
-    // Lane l holds the page of this warp's unit (32*k + l); refreshed every 32
-    // units, so the copy issue never waits on a dependent global load.
+    // Lane l holds the page of this warp's unit (32*k + l) in pf and of unit
+    // (32*(k+1) + l) in pf_next; pf_next is loaded 32 units before it is
+    // needed, so the copy issue never waits on a dependent global load.
     auto page_of_lane = [&](int i) {
       int page = 0;
       if (i < nw) {
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
       }
       return page;
     };
-    int pf = page_of_lane(lane);
+    int pf = page_of_lane(lane), pf_next = page_of_lane(32 + lane);
     // Lanes 0..3 issue the unit's four bulk copies (K codes, V codes, K
     // scales, V scales) in one pass; lane-specific source bases, row sizes and
     // stage offsets are fixed for the segment.
@@ -839,7 +840,10 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
       for (int k = 0; k < nu; ++k) {
         const int nx = i + k + C::NST;  // warp-uniform
         if (nx < nw) {
-          if ((nx & 31) == 0) pf = page_of_lane(nx + lane);
+          if ((nx & 31) == 0) {
+            pf = pf_next;
+            pf_next = page_of_lane(nx + 32 + lane);
+          }
           const int page = __shfl_sync(kFull, pf, nx & 31);
           fence_proxy_async();
           issue(nx, (it + k) % C::NST, page);
@@ -913,6 +917,12 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
   pdl_trigger();  // the merge may now be scheduled; it still waits for the whole grid
 }
 
+// N consecutive floats, aligned for one vector load.
+template <int N>
+struct alignas(4 * N) VecF {
+  float x[N];
+};
+
 // Log-sum-exp merge of the partials of each (sequence, query head), then the
 // inverse rotation (FP4).  One warp per output row.
 struct MergeParams {
@@ -950,24 +960,59 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
       last = 0;
     }
     const int64_t U = *p.ws_units;
+    // The partials of this row are slots first..last (those with an empty
+    // unit range wrote nothing).  Their (m, l) are read lane-parallel, 32 at a
+    // time; the O rows are then summed in slot order, four loads in flight.
     float Ms = -INFINITY;
-    for (int s = first; s <= last; ++s) {
-      int64_t lo, hi;
-      block_range(s, U, p.num_ctas, lo, hi);
+    for (int base = first; base <= last; base += 32) {
+      const int s = base + lane;
+      int64_t lo = 0, hi = 0;
+      if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
       if (lo < hi) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
     }
-    float Ls = 0.f;
-    for (int s = first; s <= last; ++s) {
-      int64_t lo, hi;
-      block_range(s, U, p.num_ctas, lo, hi);
-      if (lo >= hi) continue;  // a block with an empty range wrote no partial
-      const int64_t id = (int64_t)(s + pair) * kHB + hh;
-      const float w = ex2(p.ws_ml[id * 2] - Ms);
-      Ls += w * p.ws_ml[id * 2 + 1];
-      const float* src = p.ws_o + id * D + lane * EPL;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) o[e] += w * src[e];
+    for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
+    float Ls = 0.f;
+    for (int base = first; base <= last; base += 32) {
+      const int s = base + lane;
+      int64_t lo = 0, hi = 0;
+      if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
+      float w = 0.f;
+      if (lo < hi) {
+        const int64_t id = (int64_t)(s + pair) * kHB + hh;
+        w = ex2(p.ws_ml[id * 2] - Ms);
+        Ls += w * p.ws_ml[id * 2 + 1];
+      }
+      const unsigned valid = __ballot_sync(kFull, lo < hi);
+      const int n = last - base + 1 < 32 ? last - base + 1 : 32;
+      int j = 0;
+      for (; j + 4 <= n; j += 4) {
+        VecF<EPL> v[4];
+        float wj[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          wj[t] = __shfl_sync(kFull, w, j + t);
+          if ((valid >> (j + t)) & 1u)
+            v[t] = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + t + pair) * kHB + hh) * D + lane * EPL);
+          else
+            v[t] = VecF<EPL>{};
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[e] += wj[t] * v[t].x[e];
+      }
+      for (; j < n; ++j) {
+        const float wj = __shfl_sync(kFull, w, j);
+        if ((valid >> j) & 1u) {
+          const VecF<EPL> v = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + pair) * kHB + hh) * D + lane * EPL);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
+        }
+      }
     }
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) Ls += __shfl_xor_sync(kFull, Ls, k);
     const float inv = 1.f / Ls;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= inv;
