@@ -353,6 +353,31 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
     }
   }
 
+  // ---- V scale bytes of the NU units (independent of QK^T; read before the
+  // shared rare branch so that the branch splits the body only once)
+  const int gv = (r * C::VPT) >> 5;
+  uint32_t vb[NU][4];
+  uint32_t bmax = 0;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const uint8_t* svs = st[u] + 2 * C::KBYTES + C::SBYTES;
+    vb[u][0] = svs[t0 * C::SROW + gv];
+    vb[u][1] = svs[t1 * C::SROW + gv];
+    vb[u][2] = svs[t8 * C::SROW + gv];
+    vb[u][3] = svs[t9 * C::SROW + gv];
+    if (TAIL && u == NU - 1) {
+      if (t0 >= nvalid_last) vb[u][0] = 0;
+      if (t1 >= nvalid_last) vb[u][1] = 0;
+      if (t8 >= nvalid_last) vb[u][2] = 0;
+      if (t9 >= nvalid_last) vb[u][3] = 0;
+    }
+    bmax = max(bmax, max(max(vb[u][0], vb[u][1]), max(vb[u][2], vb[u][3])));
+  }
+  S.bad |= kbad | (bmax == 0xFFu ? 1u : 0u);
+  // Reference exponent RV = running max of the V scale bytes, so that every
+  // multiplier 2^(byte - RV) is <= 1 and fits f16 together with the codes.
+  const uint32_t RVc = __reduce_max_sync(kFull, bmax);
+
   // ---- softmax over the NU units
   float mc0 = -INFINITY, mc1 = -INFINITY;
 #pragma unroll
@@ -360,18 +385,33 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
     mc0 = fmaxf(mc0, fmaxf(t[u][0], t[u][2]));
     mc1 = fmaxf(mc1, fmaxf(t[u][1], t[u][3]));
   }
-  if (__any_sync(kFull, mc0 > S.M0 + kSlack || mc1 > S.M1 + kSlack)) {
+  // One rare branch for both rescales of O: the running max M grew by more
+  // than kSlack (after the first units, rare), or the V reference exponent
+  // grew (rarer).  RVc and S.RV are warp-uniform.
+  const bool grow_m = __any_sync(kFull, mc0 > S.M0 + kSlack || mc1 > S.M1 + kSlack);
+  if (grow_m || RVc > S.RV) {
+    float a0 = 1.f, a1 = 1.f, f = 1.f;
+    if (grow_m) {
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
-      mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+      for (int o = 4; o < 32; o <<= 1) {
+        mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+        mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+      }
+      const float n0 = fmaxf(S.M0, mc0), n1 = fmaxf(S.M1, mc1);
+      a0 = ex2(S.M0 - n0);
+      a1 = ex2(S.M1 - n1);
+      S.M0 = n0;
+      S.M1 = n1;
+      S.L0 *= a0;
+      S.L1 *= a1;
     }
-    const float n0 = fmaxf(S.M0, mc0), n1 = fmaxf(S.M1, mc1);
-    const float a0 = ex2(S.M0 - n0), a1 = ex2(S.M1 - n1);
-    S.M0 = n0;
-    S.M1 = n1;
-    S.L0 *= a0;
-    S.L1 *= a1;
+    if (RVc > S.RV) {
+      f = pow2i(static_cast<int>(S.RV) - static_cast<int>(RVc));
+      S.RV = RVc;
+      S.rref = pow2i(127 - static_cast<int>(RVc));
+    }
+    a0 *= f;  // exact: f is a power of two
+    a1 *= f;
 #pragma unroll
     for (int m = 0; m < C::NMMA; ++m) {
       S.O[m][0] *= a0; S.O[m][1] *= a1; S.O[m][2] *= a0; S.O[m][3] *= a1;
@@ -397,37 +437,6 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
   }
 
   // ---- P.V: thread (r, c) takes channels r*VPT.. of tokens 2c, 2c+1, 2c+8, 2c+9
-  const int gv = (r * C::VPT) >> 5;
-  uint32_t vb[NU][4];
-  uint32_t bmax = 0;
-#pragma unroll
-  for (int u = 0; u < NU; ++u) {
-    const uint8_t* svs = st[u] + 2 * C::KBYTES + C::SBYTES;
-    vb[u][0] = svs[t0 * C::SROW + gv];
-    vb[u][1] = svs[t1 * C::SROW + gv];
-    vb[u][2] = svs[t8 * C::SROW + gv];
-    vb[u][3] = svs[t9 * C::SROW + gv];
-    if (TAIL && u == NU - 1) {
-      if (t0 >= nvalid_last) vb[u][0] = 0;
-      if (t1 >= nvalid_last) vb[u][1] = 0;
-      if (t8 >= nvalid_last) vb[u][2] = 0;
-      if (t9 >= nvalid_last) vb[u][3] = 0;
-    }
-    bmax = max(bmax, max(max(vb[u][0], vb[u][1]), max(vb[u][2], vb[u][3])));
-  }
-  // Reference exponent RV = running max of the V scale bytes, so that every
-  // multiplier 2^(byte - RV) is <= 1 and fits f16 together with the codes.
-  S.bad |= kbad | (bmax == 0xFFu ? 1u : 0u);
-  const uint32_t RVc = __reduce_max_sync(kFull, bmax);
-  if (RVc > S.RV) {
-    const float f = pow2i(static_cast<int>(S.RV) - static_cast<int>(RVc));
-#pragma unroll
-    for (int m = 0; m < C::NMMA; ++m) {
-      S.O[m][0] *= f; S.O[m][1] *= f; S.O[m][2] *= f; S.O[m][3] *= f;
-    }
-    S.RV = RVc;
-    S.rref = pow2i(127 - static_cast<int>(RVc));
-  }
   uint32_t mv01[NU], mv89[NU];
 #pragma unroll
   for (int u = 0; u < NU; ++u) {
