@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
   uint8_t* myring = ring + warp * C::NST * C::STAGE;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], 1);
+    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], KIND == kFP4 ? 1 + 32 : 1);  // see the copy issue
     fence_mbar_init();
   }
   if (tid == 0) abort_flag = 0;
@@ -763,31 +763,38 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
       return page;
     };
     int pf = page_of_lane(lane), pf_next = page_of_lane(32 + lane);
-    // Lanes 0..3 issue the unit's four bulk copies (K codes, V codes, K
-    // scales, V scales) in one pass; lane-specific source bases, row sizes and
-    // stage offsets are fixed for the segment.
-    const uint8_t* cp_base = p.kc;
-    uint32_t cp_row = C::KROW, cp_off = 0, cp_bytes = C::KBYTES;
-    if (lane == 1) { cp_base = p.vc; cp_off = C::KBYTES; }
-    if (KIND == kFP4 && lane == 2) { cp_base = p.ks; cp_row = C::SROW; cp_off = 2 * C::KBYTES; cp_bytes = C::SBYTES; }
-    if (KIND == kFP4 && lane == 3) {
-      cp_base = p.vs; cp_row = C::SROW; cp_off = 2 * C::KBYTES + C::SBYTES; cp_bytes = C::SBYTES;
-    }
-    constexpr int kCopies = KIND == kFP4 ? 4 : 2;
+    // Lanes 0 and 1 issue the unit's two bulk copies (K codes, V codes); the
+    // FP4 scale rows (64 + 64 bytes at D = 128) are fetched by per-lane 4-byte
+    // cp.async, which costs less than two more bulk-copy requests.  Both
+    // complete on the stage's mbarrier: the copies by their byte count, the
+    // cp.async of every lane by one no-increment arrival each, so an FP4
+    // stage barrier expects 1 + 32 arrivals.
+    const uint8_t* cp_base = lane == 1 ? p.vc : p.kc;
+    const uint32_t cp_off = lane == 1 ? C::KBYTES : 0;
     const uint32_t ring_u32 = smem_u32(myring), bars_u32 = smem_u32(mybars);
     auto issue = [&](int i, int slot, int page) {
       const int tok0 = (j0 + warp + i * kWarps) * kChunk;
       const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
       const uint32_t bar = bars_u32 + 8u * slot;
       if (lane == 0)
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(uint32_t(C::STAGE))
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(uint32_t(2 * C::KBYTES))
                      : "memory");
-      if (lane < kCopies)
+      if (lane < 2)
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 ring_u32 + slot * uint32_t(C::STAGE) + cp_off),
-            "l"(cp_base + row0 * cp_row), "r"(cp_bytes), "r"(bar)
+            "l"(cp_base + row0 * C::KROW), "r"(uint32_t(C::KBYTES)), "r"(bar)
             : "memory");
+      if (KIND == kFP4) {
+        constexpr int SW = C::SBYTES / 4;  // scale words per array and unit
+#pragma unroll
+        for (int w = lane; w < 2 * SW; w += 32) {
+          const uint8_t* g = (w < SW ? p.ks : p.vs) + row0 * C::SROW + 4 * (w < SW ? w : w - SW);
+          const uint32_t d = ring_u32 + slot * uint32_t(C::STAGE) + 2 * C::KBYTES + 4 * w;
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(g) : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+      }
     };
     for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST, __shfl_sync(kFull, pf, i));
     // The new token (fused append) is quantised while those copies fly; its
