@@ -60,7 +60,23 @@ _lib.uqo_decode.argtypes = [C.c_int, _u16p, C.c_int, C.c_int, C.c_int, C.c_int, 
                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_float, C.c_float,
                             _i32p, C.c_int, _i32p, C.c_double, C.c_uint64, _f64p]
 
-KIND_FP4, KIND_FP8, KIND_BF16 = 0, 1, 2
+_lib.uqo_decode_ex.argtypes = [C.c_int, _u16p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_float, C.c_float,
+                               _i32p, C.c_int, _i32p, C.c_double, C.c_uint64, C.c_void_p, _f64p]
+_lib.uqo_f16_round.restype = C.c_double
+_lib.uqo_f16_round.argtypes = [C.c_float]
+_lib.uqo_tq_norm.restype = C.c_float
+_lib.uqo_tq_norm.argtypes = [_f32p, C.c_int]
+_lib.uqo_tq_code.restype = C.c_int
+_lib.uqo_tq_code.argtypes = [C.c_float, _f32p]
+_lib.uqo_tq_value.restype = C.c_double
+_lib.uqo_tq_value.argtypes = [C.c_int, _f64p]
+_lib.uqo_tq_quantize_row.argtypes = [_f32p, C.c_int, _i8p, _f32p, _u8p, _f32p]
+_lib.uqo_append_tq4.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
+                                C.c_int, C.c_uint64, _f32p, _u8p, _f32p, _u8p, _f32p]
+_lib.uqo_query_f16.argtypes = [_u16p, C.c_int, C.c_uint64, _f64p]
+
+KIND_FP4, KIND_FP8, KIND_BF16, KIND_TQ4 = 0, 1, 2, 3
 DEFAULT_SEED = 42
 C_CONSTANT = float(_lib.uqo_c_constant())
 ROUND_LOG2, ROUND_LINEAR, ROUND_FLOOR, ROUND_CEIL = 0, 1, 2, 3
@@ -194,6 +210,12 @@ class Cache:
             self.vc = np.zeros((rows, head_dim // 2), np.uint8)
             self.ks = np.zeros((rows, head_dim // 32), np.uint8)
             self.vs = np.zeros((rows, head_dim // 32), np.uint8)
+        elif kind == KIND_TQ4:
+            self.kc = np.zeros((rows, head_dim // 2), np.uint8)
+            self.vc = np.zeros((rows, head_dim // 2), np.uint8)
+            self.ks = np.zeros(rows, np.float32)  # norms
+            self.vs = np.zeros(rows, np.float32)
+            self.mags, self.tau = tq_codebook(head_dim)
         elif kind == KIND_FP8:
             self.kc = np.zeros((rows, head_dim), np.uint8)
             self.vc = np.zeros((rows, head_dim), np.uint8)
@@ -212,6 +234,8 @@ class Cache:
         args = (ka.ctypes.data, va.ctypes.data, f32, T, slots, self.Hkv, self.ps, self.d)
         if self.kind == KIND_FP4:
             _lib.uqo_append_fp4(*args, self.seed, self.kc, self.ks, self.vc, self.vs)
+        elif self.kind == KIND_TQ4:
+            _lib.uqo_append_tq4(*args, self.seed, _c(self.tau[8:], np.float32), self.kc, self.ks, self.vc, self.vs)
         elif self.kind == KIND_FP8:
             _lib.uqo_append_fp8(*args, np.float32(self.k_scale), np.float32(self.v_scale), self.kc, self.vc)
         else:
@@ -225,9 +249,11 @@ class Cache:
         sl = _c(seq_lens, np.int32)
         out = np.empty((B, Hq, d), np.float64)
         ptr = lambda a: None if a is None else a.ctypes.data
-        _lib.uqo_decode(self.kind, q.reshape(-1), B, Hq, self.Hkv, d, self.ps, ptr(self.kc), ptr(self.ks),
-                        ptr(self.vc), ptr(self.vs), np.float32(self.k_scale), np.float32(self.v_scale),
-                        bt.reshape(-1), bt.shape[1], sl, float(sm_scale), self.seed, out.reshape(-1))
+        mags = _c(self.mags, np.float64) if self.kind == KIND_TQ4 else None
+        _lib.uqo_decode_ex(self.kind, q.reshape(-1), B, Hq, self.Hkv, d, self.ps, ptr(self.kc), ptr(self.ks),
+                           ptr(self.vc), ptr(self.vs), np.float32(self.k_scale), np.float32(self.v_scale),
+                           bt.reshape(-1), bt.shape[1], sl, float(sm_scale), self.seed, ptr(mags),
+                           out.reshape(-1))
         return out
 
 
@@ -271,3 +297,63 @@ _lib.uqo_kbyte_pos.argtypes = [C.c_int, C.c_int]
 def kbyte_pos(j: int, d: int) -> int:
     """Cache position of natural code byte j of a K row (group-interleaved words)."""
     return int(_lib.uqo_kbyte_pos(j, d))
+
+
+# ---------------------------------------------------------------- TQ4 (TurboQuant codebook variant)
+_TQ_BOOKS = {}
+
+
+def tq_codebook(d: int, bits: int = 4):
+    """(f16 magnitudes c_8..c_15 as float64, fp32 thresholds tau_0..tau_14)
+    of the Lloyd-Max codebook for head_dim d (oracle/tq.py), cached."""
+    from . import tq
+    key = (d, bits)
+    if key not in _TQ_BOOKS:
+        _TQ_BOOKS[key] = tq.codebook(d, bits)
+    return _TQ_BOOKS[key]
+
+
+def f16_round(x: float) -> float:
+    return float(_lib.uqo_f16_round(np.float32(x)))
+
+
+def tq_norm(y: np.ndarray) -> np.float32:
+    y = _c(y, np.float32)
+    return np.float32(_lib.uqo_tq_norm(y, y.size))
+
+
+def tq_code(y: float, t_pos: np.ndarray) -> int:
+    return int(_lib.uqo_tq_code(np.float32(y), _c(t_pos, np.float32)))
+
+
+def tq_value(code: int, mags: np.ndarray) -> float:
+    return float(_lib.uqo_tq_value(code, _c(mags, np.float64)))
+
+
+def tq_quantize_rows(x: np.ndarray, seed: int = DEFAULT_SEED):
+    """Rotate + TQ4-quantise rows of x (fp32 or bf16 bits): (codes [n][d/2]
+    natural byte order, norms [n] fp32)."""
+    xa, f32 = _rows(x)
+    d = xa.shape[-1]
+    flat = xa.reshape(-1, d)
+    if not f32:
+        flat = (flat.astype(np.uint32) << 16).view(np.float32)
+    flat = _c(flat, np.float32)
+    _, tau = tq_codebook(d)
+    s = signs(seed, d)
+    codes = np.empty((flat.shape[0], d // 2), np.uint8)
+    norms = np.empty(flat.shape[0], np.float32)
+    for r in range(flat.shape[0]):
+        _lib.uqo_tq_quantize_row(flat[r], d, s, _c(tau[8:], np.float32), codes[r], norms[r:r + 1])
+    return codes, norms
+
+
+def query_f16(q_bf16: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """T5: f16-rounded rotated query (as float64) for each bf16 row."""
+    q = _c(q_bf16, np.uint16)
+    d = q.shape[-1]
+    flat = q.reshape(-1, d)
+    out = np.empty(flat.shape, np.float64)
+    for r in range(flat.shape[0]):
+        _lib.uqo_query_f16(flat[r], d, seed, out[r])
+    return out.reshape(q.shape)

@@ -358,19 +358,125 @@ void uqo_append_bf16(const void* k, const void* v, int in_fp32, int64_t T, const
 }
 
 /* ------------------------------------------------------------------------- */
+/* TQ4: the TurboQuant Q_mse codebook variant ([TQ-guide] "Lloyd-Max 스칼라    */
+/* 양자화 (Q_mse)" and "직교성을 이용한 내적 보존").  A row is rotated with R1,  */
+/* its L2 norm is stored, and every coordinate of the unit vector y / n is     */
+/* replaced by the index of its nearest Lloyd-Max centroid.  The codebook     */
+/* (computed from the pdf in oracle/tq.py) comes in as two tables: the f16    */
+/* reconstruction magnitudes c_8..c_15 of the non-negative half and the fp32   */
+/* decision thresholds tau_8..tau_14 between them (the negative half mirrors). */
+/* Readings:                                                       */
+/*   T3  n = fl32(sqrt(S)), S the fp32 pairwise-tree sum of fl32(y_i^2) with   */
+/*       strides d/2, d/4, ..., 1; non-finite n: norm NaN, zero codes.         */
+/*   T4  with t_k = fl32(n * tau_k): y >= 0 -> code m = #{k : y >= t_k};       */
+/*       y < 0 -> code 8 | #{k : |y| > t_k}.  This is "index of the first     */
+/*       threshold above y/n" written without a division, on the sign-        */
+/*       magnitude code (bit 3 = negative, bits 0..2 = magnitude rank).        */
+/*   T5  q~ = f16(R1 q), round to nearest even.                                */
+/* ------------------------------------------------------------------------- */
+double uqo_f16_round(float x) {
+  if (isnan(x)) return NAN;
+  double a = fabs((double)x), r;
+  if (a >= 65520.0) {
+    r = INFINITY;  /* at and above the midpoint 65504 + 16 ties go to 2^16 */
+  } else if (a < ldexp(1.0, -14)) {
+    r = nearbyint(a * ldexp(1.0, 24)) * ldexp(1.0, -24);  /* subnormal quantum 2^-24 */
+  } else {
+    int e;
+    frexp(a, &e);                       /* a in [2^(e-1), 2^e) */
+    double quantum = ldexp(1.0, e - 11); /* 10 fraction bits */
+    r = nearbyint(a / quantum) * quantum;
+  }
+  return signbit(x) ? -r : r;
+}
+
+float uqo_tq_norm(const float* y, int d) {
+  float sq[1024];
+  for (int i = 0; i < d; ++i) sq[i] = y[i] * y[i];
+  for (int h = d / 2; h >= 1; h /= 2)
+    for (int i = 0; i < h; ++i) sq[i] = sq[i] + sq[i + h];
+  return sqrtf(sq[0]);
+}
+
+int uqo_tq_code(float y, const float* t) {
+  int m = 0;
+  if (y >= 0.0f) {
+    for (int k = 0; k < 7; ++k) m += (y >= t[k]);
+    return m;
+  }
+  for (int k = 0; k < 7; ++k) m += (-y > t[k]);
+  return 8 | m;
+}
+
+double uqo_tq_value(int code, const double* mags) {
+  double v = mags[code & 7];
+  return (code & 8) ? -v : v;
+}
+
+/* Rotate + quantise one row (fp32 values): d/2 code bytes in natural order   */
+/* (byte j = code(2j) | code(2j+1) << 4) and the fp32 norm.                    */
+void uqo_tq_quantize_row(const float* xr, int d, const int8_t* s, const float* tau_pos,
+                         uint8_t* codes, float* norm) {
+  float y[1024], t[7];
+  uqo_rotate_fp32(xr, d, s, y);
+  float n = uqo_tq_norm(y, d);
+  if (!isfinite(n)) {
+    memset(codes, 0, (size_t)d / 2);
+    *norm = NAN;
+    return;
+  }
+  for (int k = 0; k < 7; ++k) t[k] = n * tau_pos[k];
+  for (int j = 0; j < d / 2; ++j)
+    codes[j] = (uint8_t)(uqo_tq_code(y[2 * j], t) | (uqo_tq_code(y[2 * j + 1], t) << 4));
+  *norm = n;
+}
+
+void uqo_append_tq4(const void* k, const void* v, int in_fp32, int64_t T, const int64_t* slots,
+                    int Hkv, int ps, int d, uint64_t seed, const float* tau_pos, uint8_t* kc,
+                    float* kn, uint8_t* vc, float* vn) {
+  int8_t s[1024];
+  float xr[1024];
+  uint8_t row[512];
+  uqo_signs(seed, d, s);
+  for (int64_t t = 0; t < T; ++t) {
+    if (slots[t] < 0) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      int64_t src = t * Hkv + h, dst = cache_row(slots[t], h, Hkv, ps);
+      load_row(k, in_fp32, src, d, xr);
+      uqo_tq_quantize_row(xr, d, s, tau_pos, row, kn + dst);
+      for (int j = 0; j < d / 2; ++j) kc[dst * (d / 2) + uqo_kbyte_pos(j, d)] = row[j];
+      load_row(v, in_fp32, src, d, xr);
+      uqo_tq_quantize_row(xr, d, s, tau_pos, vc + dst * (d / 2), vn + dst);
+    }
+  }
+}
+
+/* T5: rotated query rounded to f16, as fp64 values. */
+void uqo_query_f16(const uint16_t* q, int d, uint64_t seed, double* out) {
+  int8_t s[1024];
+  float xr[1024], y[1024];
+  uqo_signs(seed, d, s);
+  for (int i = 0; i < d; ++i) xr[i] = bf16_to_f32(q[i]);
+  uqo_rotate_fp32(xr, d, s, y);
+  for (int i = 0; i < d; ++i) out[i] = uqo_f16_round(y[i]);
+}
+
+/* ------------------------------------------------------------------------- */
 /* R5: decode attention in fp64 on the dequantised cache.                      */
 /* One query token per sequence; q head h reads kv head h / (Hq/Hkv).          */
 /* Logical token j of sequence b lives in page block_table[b][j/ps], slot      */
 /* offset j % ps.  logits = sm_scale * <q, k>, softmax with max subtraction,   */
 /* o = sum p v.  For the FP4 cache q is the rotated E4M3 query q~ and the      */
-/* output is rotated back ([UQ-review] 3.2).  kind: 0 = FP4, 1 = FP8, 2 = BF16.*/
+/* output is rotated back ([UQ-review] 3.2).  kind: 0 = FP4, 1 = FP8, 2 = BF16,*/
+/* 3 = TQ4 (q~ = f16(R1 q), values = codebook value x stored norm, rotated). */
 /* ------------------------------------------------------------------------- */
 static double kv_value(int kind, int is_k, const uint8_t* codes, const uint8_t* scales, int64_t row,
-                       int d, int i, float tensor_scale) {
-  if (kind == 0) {
+                       int d, int i, float tensor_scale, const double* tq_mags) {
+  if (kind == 0 || kind == 3) {
     int pos = is_k ? uqo_kbyte_pos(i / 2, d) : i / 2;
     int byte = codes[row * (d / 2) + pos];
     int code = (i & 1) ? (byte >> 4) : (byte & 15);
+    if (kind == 3) return uqo_tq_value(code, tq_mags) * (double)((const float*)scales)[row];
     return uqo_fp4_value(code, scales[row * (d / 32) + i / 32]);
   }
   if (kind == 1) return uqo_e4m3_value(codes[row * d + i]) * (double)tensor_scale;
@@ -378,10 +484,11 @@ static double kv_value(int kind, int is_k, const uint8_t* codes, const uint8_t* 
   return (double)bf16_to_f32(b[row * d + i]);
 }
 
-void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int ps,
-                const uint8_t* kc, const uint8_t* ks, const uint8_t* vc, const uint8_t* vs,
-                float k_scale, float v_scale, const int32_t* block_table, int max_pages,
-                const int32_t* seq_lens, double sm_scale, uint64_t seed, double* out) {
+void uqo_decode_ex(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int ps,
+                   const uint8_t* kc, const uint8_t* ks, const uint8_t* vc, const uint8_t* vs,
+                   float k_scale, float v_scale, const int32_t* block_table, int max_pages,
+                   const int32_t* seq_lens, double sm_scale, uint64_t seed, const double* tq_mags,
+                   double* out) {
   int G = Hq / Hkv;
   if (sm_scale <= 0.0) sm_scale = 1.0 / sqrt((double)d);
   int8_t s[1024];
@@ -403,8 +510,8 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
         int64_t page = block_table[(int64_t)b * max_pages + j / ps];
         int64_t row = (page * Hkv + kvh) * ps + j % ps;
         for (int i = 0; i < d; ++i) {
-          K[(int64_t)j * d + i] = kv_value(kind, 1, kc, ks, row, d, i, k_scale);
-          V[(int64_t)j * d + i] = kv_value(kind, 0, vc, vs, row, d, i, v_scale);
+          K[(int64_t)j * d + i] = kv_value(kind, 1, kc, ks, row, d, i, k_scale, tq_mags);
+          V[(int64_t)j * d + i] = kv_value(kind, 0, vc, vs, row, d, i, v_scale, tq_mags);
         }
       }
       for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
@@ -414,6 +521,8 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
           uint8_t q8[1024];
           uqo_query_fp8(qrow, d, seed, q8);
           for (int i = 0; i < d; ++i) qd[i] = uqo_e4m3_value(q8[i]);
+        } else if (kind == 3) {
+          uqo_query_f16(qrow, d, seed, qd);
         } else {
           for (int i = 0; i < d; ++i) qd[i] = (double)bf16_to_f32(qrow[i]);
         }
@@ -432,7 +541,7 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
           for (int i = 0; i < d; ++i) o[i] += p * V[(int64_t)j * d + i];
         }
         for (int i = 0; i < d; ++i) o[i] /= lsum;
-        if (kind == 0) uqo_inverse_rotate_f64(o, d, s, ob);
+        if (kind == 0 || kind == 3) uqo_inverse_rotate_f64(o, d, s, ob);
         else memcpy(ob, o, sizeof(double) * (size_t)d);
       }
       free(K);
@@ -440,6 +549,14 @@ void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int 
       free(logit);
     }
   }
+}
+
+void uqo_decode(int kind, const uint16_t* q, int B, int Hq, int Hkv, int d, int ps,
+                const uint8_t* kc, const uint8_t* ks, const uint8_t* vc, const uint8_t* vs,
+                float k_scale, float v_scale, const int32_t* block_table, int max_pages,
+                const int32_t* seq_lens, double sm_scale, uint64_t seed, double* out) {
+  uqo_decode_ex(kind, q, B, Hq, Hkv, d, ps, kc, ks, vc, vs, k_scale, v_scale, block_table, max_pages,
+                seq_lens, sm_scale, seed, NULL, out);
 }
 
 /* ------------------------------------------------------------------------- */
