@@ -60,7 +60,8 @@ typedef enum uq_status {
 typedef enum uq_kv_dtype {
   UQ_FP4_UE8M0 = 0, /* rotated FP4 E2M1 codes + UE8M0 group scales, 4.25 bit/elem */
   UQ_FP8_E4M3 = 1,  /* unrotated E4M3 with one per-tensor scale for K and one for V */
-  UQ_BF16 = 2       /* unrotated bf16 */
+  UQ_BF16 = 2,      /* unrotated bf16 */
+  UQ_TQ4 = 3        /* rotated TurboQuant Q_mse: 4-bit Lloyd-Max codebook indices + fp32 row norm */
 } uq_kv_dtype;
 
 typedef enum uq_in_dtype { UQ_IN_BF16 = 0, UQ_IN_FP32 = 1 } uq_in_dtype;
@@ -88,9 +89,23 @@ typedef enum uq_in_dtype { UQ_IN_BF16 = 0, UQ_IN_FP32 = 1 } uq_in_dtype;
  *   UQ_FP8_E4M3:  k_codes, v_codes : uint8 [num_pages][num_kv_heads][page_size][head_dim],
  *                   element = e4m3(x / k_scale) (resp. v_scale); scales unused (NULL).
  *   UQ_BF16:      k_codes, v_codes : bf16  [num_pages][num_kv_heads][page_size][head_dim]; scales unused.
+ *   UQ_TQ4:       the TurboQuant Q_mse codebook variant ([TQ-guide] "Lloyd-Max
+ *                 스칼라 양자화 (Q_mse)"), a quality anchor for the FP4 format.
+ *                 k_codes, v_codes : uint8, laid out exactly as for UQ_FP4_UE8M0
+ *                   (K rows group-interleaved by words, V rows natural), each
+ *                   nibble a sign-magnitude codebook index of one coordinate
+ *                   of the ROTATED row divided by its norm: bit 3 = negative,
+ *                   bits 0..2 = rank m of the magnitude, value = +-c_m with
+ *                   c_0 < ... < c_7 the non-negative half of the 16-level
+ *                   Lloyd-Max codebook of one coordinate of a random unit
+ *                   vector in R^head_dim, stored as f16 (see uq_tq_codebook);
+ *                 k_scales, v_scales: fp32 [num_pages][num_kv_heads][page_size]
+ *                   the row's L2 norm n (NaN for a non-finite row, whose codes
+ *                   are 0).  Element value = +-c_m * n.
+ *                 4.25 bits per element at head_dim 128 (64 + 4 bytes per row).
  *
- * rot_seed seeds the ±1 diagonal of the randomised Hadamard rotation (FP4
- * only); one sign vector serves K, V, the query and every head.  The same
+ * rot_seed seeds the ±1 diagonal of the randomised Hadamard rotation (FP4 and
+ * TQ4); one sign vector serves K, V, the query and every head.  The same
  * seed must be used for append and decode.
  */
 typedef struct uq_cache {
@@ -105,7 +120,7 @@ typedef struct uq_cache {
   void* v_scales;
   float k_scale;        /* FP8 only (1.0 if unused) */
   float v_scale;        /* FP8 only (1.0 if unused) */
-  uint64_t rot_seed;    /* FP4 only */
+  uint64_t rot_seed;    /* FP4 and TQ4 */
 } uq_cache;
 
 /* Byte size of array `which` of the cache (0 = k_codes, 1 = k_scales,
@@ -124,6 +139,14 @@ size_t uq_cache_bytes(const uq_cache* cache, int32_t which);
  *         E2M1(y * 2^-E) rounded to nearest, ties to even, saturating at 6.
  *   FP8:  e4m3(x / k_scale), round to nearest even, saturating at 448.
  *   BF16: x rounded to bf16 (exact copy for bf16 input).
+ *   TQ4:  y = the FP4 rotation of x; S = fp32 pairwise sum of fl32(y_i^2)
+ *         (balanced binary tree over adjacent elements: left half + right
+ *         half, recursively); n = fl32(sqrt(S)); with the codebook's fp32
+ *         thresholds tau_0 < ... < tau_6 between c_0..c_7 and t_k =
+ *         fl32(n * tau_k): y_i >= 0 gets code #{k : y_i >= t_k}, y_i < 0 gets
+ *         8 | #{k : |y_i| > t_k} (the nearest codebook value of y_i / n,
+ *         decided without a division).  A non-finite n stores NaN and zero
+ *         codes.
  * k, v         : device, [num_tokens][num_kv_heads][head_dim], bf16 or fp32
  *                per in_dtype, 16-byte aligned rows (contiguous).
  * slot_mapping : device int64 [num_tokens]; negative = skip the token.
@@ -202,7 +225,11 @@ uq_status uq_decode_attention_append(const void* q, const void* k_new, const voi
                                      size_t workspace_bytes, cudaStream_t stream);
 
 /* The anchors: identical to uq_decode_attention but require cache->dtype to be
- * UQ_FP8_E4M3 (resp. UQ_BF16) and return UQ_ERR_INVALID_ARG otherwise. */
+ * UQ_FP8_E4M3 (resp. UQ_BF16, UQ_TQ4) and return UQ_ERR_INVALID_ARG otherwise.
+ * TQ4 ([TQ-guide] "직교성을 이용한 내적 보존"): q~ = f16(R q) (rotation as in
+ * append, round to nearest even), logits_j = sm_scale * n^K_j * <q~, c(k_j)>,
+ * softmax, o = sum_j p_j n^V_j c(v_j), out = R^T o; the codebook values
+ * c(.) are the f16 values uq_tq_codebook returns. */
 uq_status uq_decode_attention_fp8(const void* q, const uq_cache* cache, const int32_t* block_table,
                                   int32_t max_pages_per_seq, const int32_t* seq_lens,
                                   int32_t batch, int32_t num_q_heads, float sm_scale, float* out,
@@ -212,6 +239,26 @@ uq_status uq_decode_attention_bf16(const void* q, const uq_cache* cache,
                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                                    float sm_scale, float* out, void* workspace,
                                    size_t workspace_bytes, cudaStream_t stream);
+uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                  int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                  int32_t batch, int32_t num_q_heads, float sm_scale, float* out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The TQ4 codebook ([TQ-guide] "랜덤 회전과 Beta 분포", "Lloyd-Max 스칼라 양자화
+ * (Q_mse)"): the Lloyd-Max quantiser with 2^bits levels of one coordinate of
+ * a uniformly random unit vector in R^head_dim, whose density is
+ * Gamma(d/2) / (sqrt(pi) Gamma((d-1)/2)) (1 - x^2)^((d-3)/2).  Computed on the
+ * host in double precision (the two optimality conditions alternated on the
+ * half-line until no centroid moves by 1e-14 standard deviations), symmetric.
+ * magnitudes : host float [2^(bits-1)], the non-negative centroids ascending,
+ *              each rounded to the nearest f16 (the values the cache decodes to).
+ * thresholds : host float [2^bits - 1], the fp32 roundings of the midpoints
+ *              between consecutive centroids, ascending (the middle one is 0).
+ * bits in 1..4, head_dim in 16..1024.  Host-only; enqueues nothing.  The TQ4
+ * cache uses bits = 4 with the cache's head_dim.
+ */
+uq_status uq_tq_codebook(int32_t head_dim, int32_t bits, float* magnitudes, float* thresholds);
 
 /* The same decode attention for callers that cannot allocate device memory
  * (no counterpart on the pages; a deployment convenience of this library).

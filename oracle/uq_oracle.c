@@ -366,8 +366,9 @@ void uqo_append_bf16(const void* k, const void* v, int in_fp32, int64_t T, const
 /* reconstruction magnitudes c_8..c_15 of the non-negative half and the fp32   */
 /* decision thresholds tau_8..tau_14 between them (the negative half mirrors). */
 /* Readings:                                                       */
-/*   T3  n = fl32(sqrt(S)), S the fp32 pairwise-tree sum of fl32(y_i^2) with   */
-/*       strides d/2, d/4, ..., 1; non-finite n: norm NaN, zero codes.         */
+/*   T3  n = fl32(sqrt(S)), S the fp32 sum of fl32(y_i^2) over a balanced     */
+/*       binary tree of adjacent elements (left half + right half,             */
+/*       recursively); non-finite n: norm NaN, zero codes.                     */
 /*   T4  with t_k = fl32(n * tau_k): y >= 0 -> code m = #{k : y >= t_k};       */
 /*       y < 0 -> code 8 | #{k : |y| > t_k}.  This is "index of the first     */
 /*       threshold above y/n" written without a division, on the sign-        */
@@ -390,13 +391,15 @@ double uqo_f16_round(float x) {
   return signbit(x) ? -r : r;
 }
 
-float uqo_tq_norm(const float* y, int d) {
-  float sq[1024];
-  for (int i = 0; i < d; ++i) sq[i] = y[i] * y[i];
-  for (int h = d / 2; h >= 1; h /= 2)
-    for (int i = 0; i < h; ++i) sq[i] = sq[i] + sq[i + h];
-  return sqrtf(sq[0]);
+/* Sum of fl32(y_i^2) over [a, b): fl32(left half + right half), recursively. */
+static float tq_sumsq(const float* y, int a, int b) {
+  if (b - a == 1) return y[a] * y[a];
+  int m = (a + b) / 2;
+  float left = tq_sumsq(y, a, m), right = tq_sumsq(y, m, b);
+  return left + right;
 }
+
+float uqo_tq_norm(const float* y, int d) { return sqrtf(tq_sumsq(y, 0, d)); }
 
 int uqo_tq_code(float y, const float* t) {
   int m = 0;

@@ -11,7 +11,8 @@ import workloads
 MAX_ABS = 2e-3   # attention tolerance vs the fp64 oracle on the same dequantised K/V and E4M3 query
 REL_L2 = 1e-3
 
-KIND = {uq.FP4_UE8M0: oracle.KIND_FP4, uq.FP8_E4M3: oracle.KIND_FP8, uq.BF16: oracle.KIND_BF16}
+KIND = {uq.FP4_UE8M0: oracle.KIND_FP4, uq.FP8_E4M3: oracle.KIND_FP8, uq.BF16: oracle.KIND_BF16,
+        uq.TQ4: oracle.KIND_TQ4}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

@@ -19,7 +19,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 UQ_OK = 0
-FP4_UE8M0, FP8_E4M3, BF16 = 0, 1, 2
+FP4_UE8M0, FP8_E4M3, BF16, TQ4 = 0, 1, 2, 3
 IN_BF16, IN_FP32 = 0, 1
 DEFAULT_SEED = 42
 STATUS_NAMES = {0: "UQ_OK", 1: "UQ_ERR_INVALID_ARG", 2: "UQ_ERR_UNSUPPORTED", 3: "UQ_ERR_ALIGNMENT",
@@ -50,6 +50,8 @@ _sig = {
     "uq_decode_attention": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_fp8": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_bf16": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_decode_attention_tq4": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_tq_codebook": (C.c_int, [_i32, _i32, _vp, _vp]),
     "uq_decode_attention_noalloc": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp]),
     "uq_decode_attention_append": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
                                              _vp, _sz, _vp]),
@@ -104,6 +106,12 @@ class KVCache:
             self.v_codes = alloc(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
             self.k_scales = alloc(shape + (head_dim // 32,), dtype=torch.uint8, device=device)
             self.v_scales = alloc(shape + (head_dim // 32,), dtype=torch.uint8, device=device)
+        elif dtype == TQ4:
+            self.k_codes = alloc(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
+            self.v_codes = alloc(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
+            nshape = shape + (4,)  # fp32 norm per row, held as 4 bytes
+            self.k_scales = alloc(nshape, dtype=torch.uint8, device=device)
+            self.v_scales = alloc(nshape, dtype=torch.uint8, device=device)
         else:
             el = torch.uint8 if dtype == FP8_E4M3 else torch.bfloat16
             if fill is None or dtype == FP8_E4M3:
@@ -214,6 +222,21 @@ def uq_decode_attention_bf16(q, cache, block_table, seq_lens, out=None, workspac
                              stream=None):
     return _decode(_lib.uq_decode_attention_bf16, "uq_decode_attention_bf16", q, cache, block_table, seq_lens,
                    out, workspace, sm_scale, stream)
+
+
+def uq_decode_attention_tq4(q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0, stream=None):
+    return _decode(_lib.uq_decode_attention_tq4, "uq_decode_attention_tq4", q, cache, block_table, seq_lens, out,
+                   workspace, sm_scale, stream)
+
+
+def uq_tq_codebook(head_dim: int, bits: int = 4):
+    """The TQ4 codebook the library uses: (f16 magnitudes of the non-negative
+    half, ascending; fp32 decision thresholds, ascending) as float32 numpy arrays."""
+    import numpy as np
+    mags = np.zeros(1 << (bits - 1), np.float32)
+    thr = np.zeros((1 << bits) - 1, np.float32)
+    _check(_lib.uq_tq_codebook(head_dim, bits, mags.ctypes.data, thr.ctypes.data), "uq_tq_codebook")
+    return mags, thr
 
 
 def uq_check_device_status(stream=None) -> int:

@@ -82,16 +82,17 @@ bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 // Shape and pointer checks common to append and decode.
 uq_status check_cache(const uq_cache* c) {
   if (!c) return UQ_ERR_INVALID_ARG;
-  if (c->dtype < UQ_FP4_UE8M0 || c->dtype > UQ_BF16) return UQ_ERR_INVALID_ARG;
+  if (c->dtype < UQ_FP4_UE8M0 || c->dtype > UQ_TQ4) return UQ_ERR_INVALID_ARG;
   if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 || c->head_dim <= 0)
     return UQ_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return UQ_ERR_UNSUPPORTED;
   if (!is_pow2(c->page_size) || c->page_size < 16 || c->page_size > 256) return UQ_ERR_UNSUPPORTED;
   if ((int64_t)c->num_pages * c->num_kv_heads * c->page_size >= (int64_t(1) << 40)) return UQ_ERR_UNSUPPORTED;
   if (!c->k_codes || !c->v_codes) return UQ_ERR_INVALID_ARG;
-  if (c->dtype == UQ_FP4_UE8M0 && (!c->k_scales || !c->v_scales)) return UQ_ERR_INVALID_ARG;
+  const bool packed = c->dtype == UQ_FP4_UE8M0 || c->dtype == UQ_TQ4;  // codes + per-row side array
+  if (packed && (!c->k_scales || !c->v_scales)) return UQ_ERR_INVALID_ARG;
   if (!aligned16(c->k_codes) || !aligned16(c->v_codes)) return UQ_ERR_ALIGNMENT;
-  if (c->dtype == UQ_FP4_UE8M0 && (!aligned16(c->k_scales) || !aligned16(c->v_scales))) return UQ_ERR_ALIGNMENT;
+  if (packed && (!aligned16(c->k_scales) || !aligned16(c->v_scales))) return UQ_ERR_ALIGNMENT;
   if (c->dtype == UQ_FP8_E4M3 && !(c->k_scale > 0.f && c->v_scale > 0.f)) return UQ_ERR_INVALID_ARG;
   return UQ_OK;
 }
@@ -136,6 +137,10 @@ size_t uq_cache_bytes(const uq_cache* c, int32_t which) {
       return (which == 0 || which == 2) ? rows * c->head_dim : 0;
     case UQ_BF16:
       return (which == 0 || which == 2) ? rows * c->head_dim * 2 : 0;
+    case UQ_TQ4:
+      if (which == 0 || which == 2) return rows * (c->head_dim / 2);
+      if (which == 1 || which == 3) return rows * sizeof(float);
+      return 0;
     default:
       return 0;
   }
@@ -155,7 +160,8 @@ uq_status uq_quantize_append(const void* k, const void* v, int32_t in_dtype, int
   if (!aligned16(k) || !aligned16(v)) return UQ_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0) return UQ_ERR_ALIGNMENT;
   const bool f32 = in_dtype == UQ_IN_FP32;
-  if (cache->dtype == UQ_FP4_UE8M0) return uqh::launch_append_fp4(k, v, f32, num_tokens, slot_mapping, *cache, stream);
+  if (cache->dtype == UQ_FP4_UE8M0 || cache->dtype == UQ_TQ4)
+    return uqh::launch_append_fp4(k, v, f32, num_tokens, slot_mapping, *cache, stream);
   return uqh::launch_append_anchor(k, v, f32, num_tokens, slot_mapping, *cache, stream);
 }
 
@@ -204,6 +210,14 @@ uq_status uq_decode_attention_bf16(const void* q, const uq_cache* cache, const i
                                    size_t workspace_bytes, cudaStream_t stream) {
   return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
                        workspace, workspace_bytes, stream, UQ_BF16);
+}
+
+uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                  int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                  int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                       workspace, workspace_bytes, stream, UQ_TQ4);
 }
 
 uq_status uq_check_device_status(cudaStream_t stream) {

@@ -6,6 +6,12 @@
 // group absmax times c = 0.156 (§3.3), and coded as E2M1 nibbles, 17 bytes
 // per 32 elements, written into its paged slot.
 //
+// TQ4 path (the TurboQuant Q_mse codebook variant, "TurboQuant 완전 정리",
+// juhoplayground.github.io, "Lloyd-Max 스칼라 양자화 (Q_mse)"): the same rotation,
+// then the row's L2 norm and one 4-bit index of the nearest Lloyd-Max
+// centroid per coordinate of the unit vector; same page layout, the norm in
+// place of the scale bytes.
+//
 // GB300 mapping: one thread owns one row (128 values live in registers, so the
 // whole butterfly needs no shuffles or shared-memory exchange).  Tiles of 64
 // token-head rows of K and of V are brought into shared memory by 2-D TMA
@@ -42,6 +48,7 @@ struct AppendParams {
   uint8_t* vs;
   unsigned int* status;
   uqh::SignMasks sign;
+  float tq_tpos[7];  // TQ4: positive decision thresholds tau_8..tau_14
 };
 
 // Rotation of a register-resident row whose signs were already applied.
@@ -79,12 +86,68 @@ __device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D
   }
 }
 
+// TQ4 quantiser on a rotated row (codes as quantize_regs; `norm_bits` the fp32
+// norm).  The norm is fl32(sqrt(S)) with S the fp32 sum of the squares over a
+// balanced binary tree of adjacent elements (left half + right half,
+// recursively), evaluated here as a binary counter so that only log2(D)
+// partial sums are live.  With t_k = fl32(n * tau_k), a coordinate y >= 0 gets
+// the magnitude rank #{k : y >= t_k} and y < 0 gets 8 | #{k : |y| > t_k}; on
+// the bit patterns of non-negative floats (ordered like the values) both
+// counts are #{k : key >= bits(t_k)} with key = bits(|y|) - (y < 0), found by
+// a three-step binary search over the sorted thresholds.
+template <int D>
+__device__ __forceinline__ void quantize_tq_regs(const float (&y)[D], uint32_t (&codes)[D / 8],
+                                                 uint32_t& norm_bits, const float (&tpos)[7]) {
+  float partial[8];
+  float S = 0.f;
+#pragma unroll
+  for (int i = 0; i < D; ++i) {
+    float v = __fmul_rn(y[i], y[i]);
+#pragma unroll
+    for (int lvl = 0; lvl < 8; ++lvl) {
+      if (((i + 1) >> lvl) & 1) {
+        partial[lvl] = v;
+        break;
+      }
+      v = __fadd_rn(partial[lvl], v);
+    }
+    if (i == D - 1) S = v;
+  }
+  const float n = __fsqrt_rn(S);
+  if (!(n <= 3.402823466e38f)) {  // NaN or Inf
+    norm_bits = 0x7FC00000u;
+#pragma unroll
+    for (int w = 0; w < D / 8; ++w) codes[w] = 0u;
+    return;
+  }
+  norm_bits = __float_as_uint(n);
+  uint32_t tb[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) tb[k] = __float_as_uint(__fmul_rn(n, tpos[k]));
+#pragma unroll
+  for (int w = 0; w < D / 8; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = y[8 * w + e];
+      const uint32_t neg = x < 0.f ? 1u : 0u;
+      const uint32_t key = (__float_as_uint(x) & 0x7FFFFFFFu) - neg;
+      uint32_t m = key >= tb[3] ? 4u : 0u;
+      m += key >= (m ? tb[5] : tb[1]) ? 2u : 0u;
+      const uint32_t t1 = (m & 4u) ? ((m & 2u) ? tb[6] : tb[4]) : ((m & 2u) ? tb[2] : tb[0]);
+      m += key >= t1 ? 1u : 0u;
+      word |= ((neg << 3) | m) << (4 * e);
+    }
+    codes[w] = word;
+  }
+}
+
 // Store one quantised row: codes[4g + w] is word w (bytes 4w..4w+3) of group
 // g in natural order.  K rows (KPERM) are stored group-interleaved by words --
 // word w of group g at word position (D/32)*w + g -- so that the decode can
 // fetch one word of every group with a single aligned load; V rows keep the
 // natural order.
-template <int D, bool KPERM>
+template <int D, bool KPERM, bool TQ = false>
 __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_base, int64_t row,
                                           const uint32_t (&codes)[D / 8], uint32_t scales) {
   constexpr int NG = D / 32;
@@ -96,13 +159,27 @@ __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_b
   uint4* cdst = reinterpret_cast<uint4*>(codes_base + row * (D / 2));
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) cdst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-  if (D == 128)
+  if (TQ || D == 128)  // TQ4: the fp32 norm; FP4: D/32 scale bytes
     *reinterpret_cast<uint32_t*>(scales_base + row * 4) = scales;
   else
     *reinterpret_cast<uint16_t*>(scales_base + row * 2) = static_cast<uint16_t>(scales);
 }
 
-template <int D, bool F32>
+// Quantiser stage of either format, then the store of the row.
+template <int D, bool TQ>
+__device__ __forceinline__ void quantize_store(float (&u)[D], const AppendParams& p, bool is_v, int64_t dst) {
+  uint32_t codes[D / 8], scales;
+  if (TQ)
+    quantize_tq_regs<D>(u, codes, scales, p.tq_tpos);
+  else
+    quantize_regs<D>(u, codes, scales);
+  if (is_v)
+    store_row<D, false, TQ>(p.vc, p.vs, dst, codes, scales);
+  else
+    store_row<D, true, TQ>(p.kc, p.ks, dst, codes, scales);
+}
+
+template <int D, bool F32, bool TQ>
 __global__ void __launch_bounds__(kAppendThreads)
     fp4_append_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                       const __grid_constant__ AppendParams p) {
@@ -176,8 +253,6 @@ __global__ void __launch_bounds__(kAppendThreads)
         }
       }
       rotate_regs<D>(u);
-      uint32_t codes[D / 8], scales;
-      quantize_regs<D>(u, codes, scales);
       const int64_t t = R / p.hkv;
       const int h = static_cast<int>(R - t * p.hkv);
       const int64_t slot = p.slots[t];
@@ -186,10 +261,7 @@ __global__ void __launch_bounds__(kAppendThreads)
       } else if (slot >= 0) {
         const int64_t page = slot >> p.ps_log2;
         const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
-        if (is_v)
-          store_row<D, false>(p.vc, p.vs, dst, codes, scales);
-        else
-          store_row<D, true>(p.kc, p.ks, dst, codes, scales);
+        quantize_store<D, TQ>(u, p, is_v, dst);
       }
     }
     __syncthreads();
@@ -207,7 +279,7 @@ __global__ void __launch_bounds__(kAppendThreads)
 // Small appends (a decode step's new tokens): one thread per K or V row read
 // straight from global memory, no tensor maps -- the per-call host work of the
 // tiled kernel would cost more than the copy.
-template <int D, bool F32>
+template <int D, bool F32, bool TQ>
 __global__ void __launch_bounds__(128) fp4_append_small_kernel(const void* k, const void* v,
                                                                const __grid_constant__ AppendParams p) {
   pdl_wait();
@@ -240,8 +312,6 @@ __global__ void __launch_bounds__(128) fp4_append_small_kernel(const void* k, co
     }
   }
   rotate_regs<D>(u);
-  uint32_t codes[D / 8], scales;
-  quantize_regs<D>(u, codes, scales);
   const int64_t t = R / p.hkv;
   const int h = static_cast<int>(R - t * p.hkv);
   const int64_t slot = p.slots[t];
@@ -250,10 +320,7 @@ __global__ void __launch_bounds__(128) fp4_append_small_kernel(const void* k, co
   } else if (slot >= 0) {
     const int64_t page = slot >> p.ps_log2;
     const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
-    if (is_v)
-      store_row<D, false>(p.vc, p.vs, dst, codes, scales);
-    else
-      store_row<D, true>(p.kc, p.ks, dst, codes, scales);
+    quantize_store<D, TQ>(u, p, is_v, dst);
   }
   pdl_trigger();
 }
@@ -397,12 +464,12 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int row_elems, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool TQ>
 uq_status run_fp4_append(const CUtensorMap& mk, const CUtensorMap& mv, const AppendParams& p, int64_t nrows,
                          cudaStream_t s) {
   constexpr int STAGEB = 2 * kRows * D * (F32 ? 4 : 2);
   constexpr size_t smem = 2 * STAGEB + 1024;
-  auto kern = fp4_append_kernel<D, F32>;
+  auto kern = fp4_append_kernel<D, F32, TQ>;
   static int configured_dev = -1;  // attribute is per device; re-set when the device changes
   const uqh::DevInfo& di = uqh::dev_info();
   if (configured_dev != di.device) {
@@ -441,23 +508,45 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
   p.status = status_word();
   make_sign_masks(c.rot_seed, c.head_dim, &p.sign);
   if (!p.status) return UQ_ERR_CUDA;
+  const bool tq = c.dtype == UQ_TQ4;
+  if (tq) {
+    TqTables tt;
+    const uq_status st = tq_tables(c.head_dim, &tt);
+    if (st != UQ_OK) return st;
+    for (int k = 0; k < 7; ++k) p.tq_tpos[k] = tt.tpos[k];
+  } else {
+    for (int k = 0; k < 7; ++k) p.tq_tpos[k] = 0.f;
+  }
+  // kernel instance by (head_dim, input type, format)
+  const int which = (c.head_dim == 128 ? 4 : 0) + (in_fp32 ? 2 : 0) + (tq ? 1 : 0);
   if (nrows <= kSmallAppendRows) {
     const unsigned grid = static_cast<unsigned>((2 * nrows + 127) / 128);
     cudaError_t e;
-    if (c.head_dim == 128)
-      e = in_fp32 ? launch_pdl(fp4_append_small_kernel<128, true>, grid, 128, 0, s, k, v, p)
-                  : launch_pdl(fp4_append_small_kernel<128, false>, grid, 128, 0, s, k, v, p);
-    else
-      e = in_fp32 ? launch_pdl(fp4_append_small_kernel<64, true>, grid, 128, 0, s, k, v, p)
-                  : launch_pdl(fp4_append_small_kernel<64, false>, grid, 128, 0, s, k, v, p);
+    switch (which) {
+      case 0: e = launch_pdl(fp4_append_small_kernel<64, false, false>, grid, 128, 0, s, k, v, p); break;
+      case 1: e = launch_pdl(fp4_append_small_kernel<64, false, true>, grid, 128, 0, s, k, v, p); break;
+      case 2: e = launch_pdl(fp4_append_small_kernel<64, true, false>, grid, 128, 0, s, k, v, p); break;
+      case 3: e = launch_pdl(fp4_append_small_kernel<64, true, true>, grid, 128, 0, s, k, v, p); break;
+      case 4: e = launch_pdl(fp4_append_small_kernel<128, false, false>, grid, 128, 0, s, k, v, p); break;
+      case 5: e = launch_pdl(fp4_append_small_kernel<128, false, true>, grid, 128, 0, s, k, v, p); break;
+      case 6: e = launch_pdl(fp4_append_small_kernel<128, true, false>, grid, 128, 0, s, k, v, p); break;
+      default: e = launch_pdl(fp4_append_small_kernel<128, true, true>, grid, 128, 0, s, k, v, p); break;
+    }
     return cuda_status(e);
   }
   CUtensorMap mk, mv;
   if (!encode_rows(&mk, k, nrows, c.head_dim, in_fp32) || !encode_rows(&mv, v, nrows, c.head_dim, in_fp32))
     return UQ_ERR_CUDA;
-  if (c.head_dim == 128)
-    return in_fp32 ? run_fp4_append<128, true>(mk, mv, p, nrows, s) : run_fp4_append<128, false>(mk, mv, p, nrows, s);
-  return in_fp32 ? run_fp4_append<64, true>(mk, mv, p, nrows, s) : run_fp4_append<64, false>(mk, mv, p, nrows, s);
+  switch (which) {
+    case 0: return run_fp4_append<64, false, false>(mk, mv, p, nrows, s);
+    case 1: return run_fp4_append<64, false, true>(mk, mv, p, nrows, s);
+    case 2: return run_fp4_append<64, true, false>(mk, mv, p, nrows, s);
+    case 3: return run_fp4_append<64, true, true>(mk, mv, p, nrows, s);
+    case 4: return run_fp4_append<128, false, false>(mk, mv, p, nrows, s);
+    case 5: return run_fp4_append<128, false, true>(mk, mv, p, nrows, s);
+    case 6: return run_fp4_append<128, true, false>(mk, mv, p, nrows, s);
+    default: return run_fp4_append<128, true, true>(mk, mv, p, nrows, s);
+  }
 }
 
 uq_status launch_append_anchor(const void* k, const void* v, bool in_fp32, int64_t ntok, const int64_t* slots,

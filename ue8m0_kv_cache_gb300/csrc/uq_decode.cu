@@ -58,7 +58,10 @@ constexpr int kChunk = 16;  // tokens per work unit (the MMA's m for QK)
 constexpr float kSlack = 8.f;
 constexpr float kPShift = 7.f;
 
-enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
+enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2, kTQ4 = 3 };
+// FP4 and TQ4 share the 4-bit packed codes, the per-row side array (scale
+// bytes or norm), the rotation and the two-unit main loop.
+constexpr bool packed4(int kind) { return kind == kFP4 || kind == kTQ4; }
 
 #ifndef UQ_FP4_MINB
 #define UQ_FP4_MINB 3  // resident blocks per SM the FP4 decode is compiled for
@@ -66,12 +69,13 @@ enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2 };
 
 template <int KIND, int D>
 struct DC {
-  static constexpr int KROW = KIND == kFP4 ? D / 2 : (KIND == kFP8 ? D : 2 * D);  // bytes/token row
-  static constexpr int SROW = KIND == kFP4 ? D / 32 : 0;                         // scale bytes/token
+  static constexpr int KROW = packed4(KIND) ? D / 2 : (KIND == kFP8 ? D : 2 * D);  // bytes/token row
+  // side bytes/token: FP4 scale bytes, TQ4 the fp32 norm
+  static constexpr int SROW = KIND == kFP4 ? D / 32 : (KIND == kTQ4 ? 4 : 0);
   static constexpr int KBYTES = kChunk * KROW;
   static constexpr int SBYTES = kChunk * SROW;
   static constexpr int STAGE = 2 * KBYTES + 2 * SBYTES;
-  static constexpr int NST = KIND == kFP4 ? 4 : 3;  // ring depth per warp
+  static constexpr int NST = packed4(KIND) ? 4 : 3;  // ring depth per warp
   static constexpr int NMMA = D / 16;               // k-steps of QK, m-blocks of PV
   static constexpr int NG = D / 32;                 // 32-channel groups
   static constexpr int CPT = D / 4;                 // QK channels per thread and token
@@ -98,6 +102,7 @@ struct DecParams {
   int64_t* ws_units;
   unsigned int* status;
   uqh::SignMasks sign;
+  uint32_t tq_lut[4];  // TQ4 codebook magnitudes as byte tables (see uqh::TqTables)
   // Fused append (FP4): new token of sequence b at physical slot new_slots[b]
   // (-1: none), rows k_new/v_new [B][Hkv][D] (bf16, or fp32 if new_f32).
   const void* k_new;
@@ -485,6 +490,203 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
   }
 }
 
+// Byte permute with the PTX default mode: a selector nibble with bit 3 set
+// replicates the sign bit of the selected byte over the result byte.
+__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// TQ4 codebook lookup: the 8 sign-magnitude nibbles of w to 4 f16x2 (nibbles
+// 2k, 2k+1 in o[k], low half first), the layout e2m1x8_to_f16x2 gives for FP4.
+// lut[0..1] hold the high bytes of the f16 magnitudes c_0..c_7, lut[2..3] the
+// low bytes: two byte permutes look up 4 magnitudes, two more interleave high
+// and low bytes into f16 pairs, and one sign-replicating permute per pair
+// moves the two sign bits (bit 3 of each nibble) to bits 15 and 31.
+__device__ __forceinline__ void tq_lut8_to_f16x2(uint32_t w, const uint32_t (&lut)[4], uint32_t (&o)[4]) {
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t hb = __byte_perm(lut[0], lut[1], sel), lb = __byte_perm(lut[2], lut[3], sel);
+  const uint32_t hb2 = __byte_perm(lut[0], lut[1], sel >> 16), lb2 = __byte_perm(lut[2], lut[3], sel >> 16);
+  o[0] = __byte_perm(lb, hb, 0x5140);
+  o[1] = __byte_perm(lb, hb, 0x7362);
+  o[2] = __byte_perm(lb2, hb2, 0x5140);
+  o[3] = __byte_perm(lb2, hb2, 0x7362);
+  const uint32_t w4 = w << 4;  // bit 3 of nibble 2k becomes the top bit of byte k
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // result byte 1 <- sign of byte k of w4 (nibble 2k), byte 3 <- sign of byte k of w (nibble 2k+1)
+    const uint32_t s = prmt_sx(w, w4, ((0x8u | k) << 12) | ((0x8u | (4 + k)) << 4));
+    o[k] ^= s & 0x80008000u;
+  }
+}
+
+// NU consecutive units of this warp, TQ4 cache: the FP4 loop with codebook
+// lookups in place of the hardware E2M1 conversion.  QK^T accumulates all
+// groups in one accumulator and applies the key norm once; the value norm of
+// each token is folded into P (times 2^(126 - RV), RV the running maximum of
+// the norms' exponent fields, so that P stays within f16) instead of into the
+// values.
+template <int D, int NU, bool TAIL>
+__device__ __forceinline__ void units_tq(const uint8_t* const (&st)[NU], int nvalid_last, int r, int c,
+                                         const uint32_t (&qb)[D / 16][2], float sl2e, const uint32_t (&lut)[4],
+                                         WarpState<D / 16>& S) {
+  using C = DC<kTQ4, D>;
+  constexpr int NG = C::NG;
+  constexpr int VB = C::VPT / 2;  // V code bytes per thread and token
+  const int t0 = 2 * c, t1 = t0 + 1, t8 = t0 + 8, t9 = t0 + 9;
+
+  // ---- QK^T: thread (r, c) holds word c of every 32-channel group of tokens r, r+8
+  float t[NU][4];
+  uint32_t kbad = 0;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const uint8_t* skc = st[u];
+    const uint8_t* skn = st[u] + 2 * C::KBYTES;
+    uint32_t kw0[NG], kw1[NG];
+    if (NG == 4) {
+      const uint4 x0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 16);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 16);
+      kw0[0] = x0.x; kw0[1] = x0.y; kw0[2 % NG] = x0.z; kw0[3 % NG] = x0.w;
+      kw1[0] = x1.x; kw1[1] = x1.y; kw1[2 % NG] = x1.z; kw1[3 % NG] = x1.w;
+    } else {
+      const uint2 x0 = *reinterpret_cast<const uint2*>(skc + r * C::KROW + c * 8);
+      const uint2 x1 = *reinterpret_cast<const uint2*>(skc + (r + 8) * C::KROW + c * 8);
+      kw0[0] = x0.x; kw0[1 % NG] = x0.y;
+      kw1[0] = x1.x; kw1[1 % NG] = x1.y;
+    }
+    const float n0 = *reinterpret_cast<const float*>(skn + r * 4);
+    const float n1 = *reinterpret_cast<const float*>(skn + (r + 8) * 4);
+    float acc[4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      uint32_t h0[4], h1[4];
+      tq_lut8_to_f16x2(kw0[g], lut, h0);
+      tq_lut8_to_f16x2(kw1[g], lut, h1);
+      if (g == 0) mma_f16_zc(acc, h0[0], h1[0], h0[1], h1[1], qb[0][0], qb[0][1]);
+      else mma_f16(acc, h0[0], h1[0], h0[1], h1[1], qb[2 * g][0], qb[2 * g][1]);
+      mma_f16(acc, h0[2], h1[2], h0[3], h1[3], qb[2 * g + 1][0], qb[2 * g + 1][1]);
+    }
+    const float f0 = n0 * sl2e, f1 = n1 * sl2e;
+    t[u][0] = acc[0] * f0; t[u][1] = acc[1] * f0; t[u][2] = acc[2] * f1; t[u][3] = acc[3] * f1;
+    if (TAIL && u == NU - 1) {
+      const bool v0 = r < nvalid_last, v1 = r + 8 < nvalid_last;
+      if (!v0) { t[u][0] = -INFINITY; t[u][1] = -INFINITY; }
+      if (!v1) { t[u][2] = -INFINITY; t[u][3] = -INFINITY; }
+      kbad |= ((v0 && !(n0 <= 3.402823466e38f)) || (v1 && !(n1 <= 3.402823466e38f))) ? 1u : 0u;
+    } else {
+      kbad |= (!(n0 <= 3.402823466e38f) || !(n1 <= 3.402823466e38f)) ? 1u : 0u;
+    }
+  }
+
+  // ---- V norms of tokens r, r+8 (the rows of this thread's P values)
+  float vn[NU][2];
+  uint32_t bmax = 0;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const uint8_t* svn = st[u] + 2 * C::KBYTES + C::SBYTES;
+    vn[u][0] = *reinterpret_cast<const float*>(svn + r * 4);
+    vn[u][1] = *reinterpret_cast<const float*>(svn + (r + 8) * 4);
+    if (TAIL && u == NU - 1) {
+      if (r >= nvalid_last) vn[u][0] = 0.f;
+      if (r + 8 >= nvalid_last) vn[u][1] = 0.f;
+    }
+    const uint32_t e0 = (__float_as_uint(vn[u][0]) >> 23) & 0xFFu, e1 = (__float_as_uint(vn[u][1]) >> 23) & 0xFFu;
+    bmax = max(bmax, max(e0, e1));
+  }
+  S.bad |= kbad | (bmax == 0xFFu ? 1u : 0u);
+  const uint32_t RVc = __reduce_max_sync(kFull, bmax);
+
+  // ---- softmax, with the same shared rare branch as the FP4 path
+  float mc0 = -INFINITY, mc1 = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    mc0 = fmaxf(mc0, fmaxf(t[u][0], t[u][2]));
+    mc1 = fmaxf(mc1, fmaxf(t[u][1], t[u][3]));
+  }
+  const bool grow_m = __any_sync(kFull, mc0 > S.M0 + kSlack || mc1 > S.M1 + kSlack);
+  if (grow_m || RVc > S.RV) {
+    float a0 = 1.f, a1 = 1.f, f = 1.f;
+    if (grow_m) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mc0 = fmaxf(mc0, __shfl_xor_sync(kFull, mc0, o));
+        mc1 = fmaxf(mc1, __shfl_xor_sync(kFull, mc1, o));
+      }
+      const float n0 = fmaxf(S.M0, mc0), n1 = fmaxf(S.M1, mc1);
+      a0 = ex2(S.M0 - n0);
+      a1 = ex2(S.M1 - n1);
+      S.M0 = n0;
+      S.M1 = n1;
+      S.L0 *= a0;
+      S.L1 *= a1;
+    }
+    if (RVc > S.RV) {
+      f = pow2i(static_cast<int>(S.RV) - static_cast<int>(RVc));
+      S.RV = RVc;
+      S.rref = pow2i(126 - static_cast<int>(RVc));
+    }
+    a0 *= f;
+    a1 *= f;
+#pragma unroll
+    for (int m = 0; m < C::NMMA; ++m) {
+      S.O[m][0] *= a0; S.O[m][1] *= a1; S.O[m][2] *= a0; S.O[m][3] *= a1;
+    }
+  }
+  uint32_t bp[NU][4];
+  {
+    const float s0 = kPShift - S.M0, s1 = kPShift - S.M1;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const float p0 = ex2(t[u][0] + s0), p1 = ex2(t[u][1] + s1), p2 = ex2(t[u][2] + s0), p3 = ex2(t[u][3] + s1);
+      S.L0 += p0 + p2;
+      S.L1 += p1 + p3;
+      // n * 2^(126 - RV) < 1 (exact: a power-of-two factor), then p * that
+      const float w0 = vn[u][0] * S.rref, w1 = vn[u][1] * S.rref;
+      const float q0 = p0 * w0, q1 = p1 * w0, q2 = p2 * w1, q3 = p3 * w1;
+      const float h0 = __uint_as_float(__float_as_uint(q0) & 0xFFFFE000u);
+      const float h1 = __uint_as_float(__float_as_uint(q1) & 0xFFFFE000u);
+      const float h2 = __uint_as_float(__float_as_uint(q2) & 0xFFFFE000u);
+      const float h3 = __uint_as_float(__float_as_uint(q3) & 0xFFFFE000u);
+      bp[u][0] = movmatrix_trans(pack_f16x2(h0, h1));
+      bp[u][1] = movmatrix_trans(pack_f16x2(h2, h3));
+      bp[u][2] = movmatrix_trans(pack_f16x2(q0 - h0, q1 - h1));
+      bp[u][3] = movmatrix_trans(pack_f16x2(q2 - h2, q3 - h3));
+    }
+  }
+
+  // ---- P.V: thread (r, c) takes channels r*VPT.. of tokens 2c, 2c+1, 2c+8, 2c+9
+#pragma unroll
+  for (int q4 = 0; q4 < VB / 4; ++q4) {
+    uint32_t A[NU][4][4];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const uint8_t* svc = st[u] + C::KBYTES;
+      const uint32_t w0 = reinterpret_cast<const uint32_t*>(svc + t0 * C::KROW + r * VB)[q4];
+      const uint32_t w1 = reinterpret_cast<const uint32_t*>(svc + t1 * C::KROW + r * VB)[q4];
+      const uint32_t w8 = reinterpret_cast<const uint32_t*>(svc + t8 * C::KROW + r * VB)[q4];
+      const uint32_t w9 = reinterpret_cast<const uint32_t*>(svc + t9 * C::KROW + r * VB)[q4];
+      // same channel of two tokens in one byte (low nibble = lower token), then the lookup
+      tq_lut8_to_f16x2((w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4), lut, A[u][0]);
+      tq_lut8_to_f16x2(((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u), lut, A[u][1]);
+      tq_lut8_to_f16x2((w8 & 0x0F0F0F0Fu) | ((w9 & 0x0F0F0F0Fu) << 4), lut, A[u][2]);
+      tq_lut8_to_f16x2(((w8 >> 4) & 0x0F0F0F0Fu) | (w9 & 0xF0F0F0F0u), lut, A[u][3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float acc[4];
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        if (u == 0) mma_f16_zc(acc, A[u][0][k], A[u][1][k], A[u][2][k], A[u][3][k], bp[u][0], bp[u][1]);
+        else mma_f16(acc, A[u][0][k], A[u][1][k], A[u][2][k], A[u][3][k], bp[u][0], bp[u][1]);
+        mma_f16(acc, A[u][0][k], A[u][1][k], A[u][2][k], A[u][3][k], bp[u][2], bp[u][3]);
+      }
+      add2(S.O[4 * q4 + k][0], S.O[4 * q4 + k][1], acc[0], acc[1]);
+      add2(S.O[4 * q4 + k][2], S.O[4 * q4 + k][3], acc[2], acc[3]);
+    }
+  }
+}
+
 // One 16-token unit, FP8 or BF16 cache (unrotated, per-tensor scales folded
 // into the logit scale and the final output).
 template <int KIND, int D, bool TAIL>
@@ -641,7 +843,7 @@ __device__ __forceinline__ void patch_stage(const uint8_t* scratch, uint8_t* st,
 }
 
 template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) decode_kernel(const __grid_constant__ DecParams p) {
   using C = DC<KIND, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -653,6 +855,9 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, c = lane & 3;
   const int ps_mask = (1 << p.ps_log2) - 1;
+  uint32_t lut[4];  // TQ4 codebook byte tables
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lut[i] = p.tq_lut[i];
   pdl_wait();  // the cache, query and block table are written by earlier kernels
 
   // Prefix sums of 16-token units per sequence.
@@ -675,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
   uint8_t* myring = ring + warp * C::NST * C::STAGE;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], KIND == kFP4 ? 1 + 32 : 1);  // see the copy issue
+    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], packed4(KIND) ? 1 + 32 : 1);  // see the copy issue
     fence_mbar_init();
   }
   if (tid == 0) abort_flag = 0;
@@ -728,6 +933,25 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
           qb[2 * g][1] = e4m3x2_to_f16x2(w.x >> 16);
           qb[2 * g + 1][0] = e4m3x2_to_f16x2(w.y);
           qb[2 * g + 1][1] = e4m3x2_to_f16x2(w.y >> 16);
+        }
+        __syncwarp();
+      } else if (KIND == kTQ4) {
+        // Rotate on the quad, round to f16 (nearest even), regroup through
+        // the warp's slice of the combine buffer: thread c needs channels
+        // 32g + 8c .. +7 of its head for every group g.
+        float x[D / 4];
+        rotate_quad<D, false>(qrow, hv, c, p.sign, x);
+        uint32_t* qs = reinterpret_cast<uint32_t*>(comb_o + warp * kHB * D);  // [8 heads][D] f16
+#pragma unroll
+        for (int e = 0; e < D / 4; e += 2) qs[(r * D + c * (D / 4) + e) / 2] = pack_f16x2(x[e], x[e + 1]);
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < C::NG; ++g) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qs + (r * D + 32 * g + 8 * c) / 2);
+          qb[2 * g][0] = w.x;
+          qb[2 * g][1] = w.y;
+          qb[2 * g + 1][0] = w.z;
+          qb[2 * g + 1][1] = w.w;
         }
         __syncwarp();
       } else {
@@ -785,8 +1009,8 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
                 ring_u32 + slot * uint32_t(C::STAGE) + cp_off),
             "l"(cp_base + row0 * C::KROW), "r"(uint32_t(C::KBYTES)), "r"(bar)
             : "memory");
-      if (KIND == kFP4) {
-        constexpr int SW = C::SBYTES / 4;  // scale words per array and unit
+      if (packed4(KIND)) {
+        constexpr int SW = C::SBYTES / 4;  // scale (or norm) words per array and unit
 #pragma unroll
         for (int w = lane; w < 2 * SW; w += 32) {
           const uint8_t* g = (w < SW ? p.ks : p.vs) + row0 * C::SROW + 4 * (w < SW ? w : w - SW);
@@ -809,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
     S.M0 = S.M1 = -INFINITY;
     S.L0 = S.L1 = 0.f;
     S.RV = 0;
-    S.rref = pow2i(127);
+    S.rref = pow2i(KIND == kTQ4 ? 126 : 127);
     S.bad = 0;
 #pragma unroll
     for (int m = 0; m < C::NMMA; ++m) S.O[m][0] = S.O[m][1] = S.O[m][2] = S.O[m][3] = 0.f;
@@ -818,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
     for (int i = 0; i < nw;) {
       // FP4 takes two units per step (independent work for the scheduler);
       // the anchors, and an odd last unit, take one.
-      const int nu = (KIND == kFP4 && i + 1 < nw) ? 2 : 1;  // warp-uniform
+      const int nu = (packed4(KIND) && i + 1 < nw) ? 2 : 1;  // warp-uniform
       bool ok = mbar_wait(&mybars[it % C::NST], (it / C::NST) & 1, kWaitBudget);
       if (nu == 2) ok = ok && mbar_wait(&mybars[(it + 1) % C::NST], ((it + 1) / C::NST) & 1, kWaitBudget);
       if (!__all_sync(kFull, ok)) {
@@ -848,6 +1072,16 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
           if (nvalid >= kChunk) units_fp4<D, 1, false>(sts, kChunk, r, c, qb, fac, S);
           else units_fp4<D, 1, true>(sts, nvalid, r, c, qb, fac, S);
         }
+      } else if (KIND == kTQ4) {
+        if (nu == 2) {
+          const uint8_t* const sts[2] = {st0, myring + ((it + 1) % C::NST) * C::STAGE};
+          if (nvalid >= kChunk) units_tq<D, 2, false>(sts, kChunk, r, c, qb, fac, lut, S);
+          else units_tq<D, 2, true>(sts, nvalid, r, c, qb, fac, lut, S);
+        } else {
+          const uint8_t* const sts[1] = {st0};
+          if (nvalid >= kChunk) units_tq<D, 1, false>(sts, kChunk, r, c, qb, fac, lut, S);
+          else units_tq<D, 1, true>(sts, nvalid, r, c, qb, fac, lut, S);
+        }
       } else {
         if (nvalid >= kChunk) unit_anchor<KIND, D, false>(st0, kChunk, r, c, qb, fac, S);
         else unit_anchor<KIND, D, true>(st0, nvalid, r, c, qb, fac, S);
@@ -875,14 +1109,17 @@ __global__ void __launch_bounds__(kThreads, KIND == kFP4 ? UQ_FP4_MINB : 4) deco
       S.L0 += __shfl_xor_sync(kFull, S.L0, o);
       S.L1 += __shfl_xor_sync(kFull, S.L1, o);
     }
-    if (KIND == kFP4 && __any_sync(kFull, S.bad != 0)) S.L0 = S.L1 = __int_as_float(0x7FC00000);
+    if (packed4(KIND) && __any_sync(kFull, S.bad != 0)) S.L0 = S.L1 = __int_as_float(0x7FC00000);
     if (r == 0) {
       comb_ml[(warp * kHB + 2 * c) * 2] = S.M0;
       comb_ml[(warp * kHB + 2 * c) * 2 + 1] = S.L0;
       comb_ml[(warp * kHB + 2 * c + 1) * 2] = S.M1;
       comb_ml[(warp * kHB + 2 * c + 1) * 2 + 1] = S.L1;
     }
-    const float osc = KIND == kFP4 ? pow2i(static_cast<int>(S.RV) - 127) : (KIND == kFP8 ? p.v_scale : 1.f);
+    // FP4: P.V ran on values * 2^(127 - RV); TQ4: on norms * 2^(126 - RV)
+    const float osc = KIND == kFP4   ? pow2i(static_cast<int>(S.RV) - 127)
+                      : KIND == kTQ4 ? pow2i(static_cast<int>(S.RV) - 126)
+                                     : (KIND == kFP8 ? p.v_scale : 1.f);
     {
       float* co = comb_o + warp * kHB * D;
 #pragma unroll
@@ -1032,7 +1269,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
     const float inv = 1.f / Ls;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= inv;
-    if (KIND == kFP4) {
+    if (packed4(KIND)) {
       // inverse rotation: s .* (H o) / sqrt(D); strides below EPL in-thread,
       // the rest across lanes.
 #pragma unroll
@@ -1151,7 +1388,14 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.ws_o = p.ws_ml + slots * kHB * 2;
   p.status = uqh::status_word();
   if (!p.status) return UQ_ERR_CUDA;
-  if (KIND == kFP4) uqh::make_sign_masks(c.rot_seed, D, &p.sign);
+  if (packed4(KIND)) uqh::make_sign_masks(c.rot_seed, D, &p.sign);
+  for (int i = 0; i < 4; ++i) p.tq_lut[i] = 0;
+  if (KIND == kTQ4) {
+    uqh::TqTables tt;
+    const uq_status st = uqh::tq_tables(D, &tt);
+    if (st != UQ_OK) return st;
+    for (int i = 0; i < 4; ++i) p.tq_lut[i] = tt.lut[i];
+  }
   p.k_new = a.k_new;
   p.v_new = a.v_new;
   p.new_slots = a.new_slots;
@@ -1206,6 +1450,8 @@ uq_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
       return d == 128 ? run_decode<kFP4, 128>(a, nhb, s) : run_decode<kFP4, 64>(a, nhb, s);
     case UQ_FP8_E4M3:
       return d == 128 ? run_decode<kFP8, 128>(a, nhb, s) : run_decode<kFP8, 64>(a, nhb, s);
+    case UQ_TQ4:
+      return d == 128 ? run_decode<kTQ4, 128>(a, nhb, s) : run_decode<kTQ4, 64>(a, nhb, s);
     default:
       return d == 128 ? run_decode<kBF16, 128>(a, nhb, s) : run_decode<kBF16, 64>(a, nhb, s);
   }

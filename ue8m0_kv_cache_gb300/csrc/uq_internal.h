@@ -58,9 +58,20 @@ inline int ilog2(int v) {
   return l;
 }
 
+// TQ4 codebook tables (uq_codebook.cu), cached per head_dim: the positive
+// decision thresholds tau_8..tau_14 of the 16-level codebook and the f16
+// magnitudes c_0..c_7 as byte tables (lut[0..1]: high bytes of c_0..c_3,
+// c_4..c_7; lut[2..3]: low bytes), the form the decode's byte permutes read.
+struct TqTables {
+  float tpos[7];
+  uint32_t lut[4];
+};
+uq_status tq_tables(int d, TqTables* out);
+uq_status tq_codebook_host(int d, int bits, float* mags, float* thresholds);
+
 // Append launchers (uq_append.cu).
 uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t ntok,
-                            const int64_t* slots, const uq_cache& c, cudaStream_t s);
+                            const int64_t* slots, const uq_cache& c, cudaStream_t s);  // FP4 and TQ4
 uq_status launch_append_anchor(const void* k, const void* v, bool in_fp32, int64_t ntok,
                                const int64_t* slots, const uq_cache& c, cudaStream_t s);
 uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y,
