@@ -236,6 +236,7 @@ def run_uq(args):
     if not args.no_anchors:
         caches["fp8"] = uq.KVCache(uq.FP8_E4M3, w.num_pages, HKV, PS, D, device=dev)
         caches["bf16"] = uq.KVCache(uq.BF16, w.num_pages, HKV, PS, D, device=dev)
+        caches["tq4"] = uq.KVCache(uq.TQ4, w.num_pages, HKV, PS, D, device=dev)
 
     # ---- setup: the cached 32768 tokens per sequence (untimed)
     for b in range(B):
@@ -257,21 +258,29 @@ def run_uq(args):
         uq.uq_quantize_append(kA, vA, sA, c)
     fp4 = caches["fp4"]
     l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    q_times = []
-    for i in range(3 + 5):
-        l2_flush.zero_()
-        e0, e1 = _event_pair()
-        e0.record(stream)
-        uq.uq_quantize_append(kA, vA, sA, fp4)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= 3:
-            q_times.append(e0.elapsed_time(e1) * 1e-3)
+
+    def time_append(cache):
+        times = []
+        for i in range(3 + 5):
+            l2_flush.zero_()
+            e0, e1 = _event_pair()
+            e0.record(stream)
+            uq.uq_quantize_append(kA, vA, sA, cache)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        return float(np.median(times))
+
     n_th = B * APPEND * HKV
     q_in, q_out = n_th * 2 * D * 2, n_th * FP4_BYTES_PER_TOKEN_HEAD + B * APPEND * 8
-    q_t = float(np.median(q_times))
+    q_t = time_append(fp4)
     quantize = {"GB_per_s": (q_in + q_out) / q_t / 1e9, "ms": q_t * 1e3, "tokens": B * APPEND,
                 "bytes_in": q_in, "bytes_out": q_out, "launches": 1}
+    tq4_quantize = None
+    if "tq4" in caches:  # the codebook variant writes the same 136 B per token-head
+        tq_t = time_append(caches["tq4"])
+        tq4_quantize = {"GB_per_s": (q_in + q_out) / tq_t / 1e9, "ms": tq_t * 1e3}
     del kA, vA, sA, l2_flush
     assert uq.uq_check_device_status() == 0
 
@@ -293,7 +302,7 @@ def run_uq(args):
     out = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
     wsp = uq.workspace(B, HQ, HKV, D, dev)
     decode_fn = {"fp4": uq.uq_decode_attention, "fp8": uq.uq_decode_attention_fp8,
-                 "bf16": uq.uq_decode_attention_bf16}
+                 "bf16": uq.uq_decode_attention_bf16, "tq4": uq.uq_decode_attention_tq4}
 
     def decode_loop(name, count, offset, timed_decode):
         c = caches[name]
@@ -354,12 +363,15 @@ def run_uq(args):
                 "frac_of_nominal_8TBps": achieved / 8000.0}
 
     anchors = {}
-    for name, per in (("fp8", FP8_BYTES_PER_TOKEN_HEAD), ("bf16", BF16_BYTES_PER_TOKEN_HEAD)):
+    for name, per in (("fp8", FP8_BYTES_PER_TOKEN_HEAD), ("bf16", BF16_BYTES_PER_TOKEN_HEAD),
+                      ("tq4", FP4_BYTES_PER_TOKEN_HEAD)):
         if name not in caches:
             continue
         tt, dt, _ = timed(name)
         anchors[name] = {"decode_tokens_per_s": B * steps / tt, "ms_per_step": tt / steps * 1e3,
                          "decode_ms": dt * 1e3, "kv_GB_per_s": B * HKV * ctx_mean * per / dt / 1e9}
+        if name == "tq4":
+            anchors[name]["quantize"] = tq4_quantize
     assert uq.uq_check_device_status() == 0
 
     # ---- end to end through the public API with host buffers
