@@ -245,6 +245,34 @@ uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const in
                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Chunked-prefill attention over an FP4 cache.  A prefill chunk first appends
+ * its n_b new tokens of sequence b with uq_quantize_append; then query i of
+ * the chunk (position p = seq_lens[b] - n_b + i) attends causally to keys
+ * 0..p of the sequence, with the decode's numerics ([UQ-review] §3.2: rotated
+ * E4M3 query, E2M1 x UE8M0 keys and values, fp32 output rotated back):
+ * out[t][h] = R^T softmax_j(sm_scale <q~_t, k^_j>) v^_j over j <= p.
+ * q           : device bf16 [num_q_tokens][num_q_heads][head_dim], 16-byte aligned;
+ *               the chunk of sequence b is rows cu_q[b] .. cu_q[b+1]-1.
+ * cu_q        : device int32 [batch + 1], non-decreasing, cu_q[0] = 0,
+ *               cu_q[batch] = num_q_tokens.
+ * seq_lens    : device int32 [batch]; keys of sequence b INCLUDING its chunk
+ *               (n_b <= seq_lens[b]; a violation is recorded as
+ *               UQ_ERR_DEVICE_BOUNDS and the chunk is clamped).
+ * block_table, max_pages_per_seq, sm_scale: as uq_decode_attention.
+ * out         : device fp32 [num_q_tokens][num_q_heads][head_dim].
+ * workspace   : device, 16-byte aligned, at least
+ *               uq_prefill_workspace_bytes(num_q_tokens, batch, num_q_heads,
+ *               num_kv_heads, head_dim, max_pages_per_seq * page_size) bytes.
+ * FP4 caches only (UQ_ERR_UNSUPPORTED otherwise); shapes as the decode.
+ */
+size_t uq_prefill_workspace_bytes(int32_t num_q_tokens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_keys);
+uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q_tokens, const uq_cache* cache,
+                               const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                               int32_t batch, int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The TQ4 codebook ([TQ-guide] "랜덤 회전과 Beta 분포", "Lloyd-Max 스칼라 양자화
  * (Q_mse)"): the Lloyd-Max quantiser with 2^bits levels of one coordinate of
  * a uniformly random unit vector in R^head_dim, whose density is

@@ -52,6 +52,8 @@ _sig = {
     "uq_decode_attention_bf16": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_tq4": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_tq_codebook": (C.c_int, [_i32, _i32, _vp, _vp]),
+    "uq_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "uq_prefill_attention": (C.c_int, [_vp, _vp, _i32, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "uq_decode_attention_noalloc": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp]),
     "uq_decode_attention_append": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
                                              _vp, _sz, _vp]),
@@ -237,6 +239,36 @@ def uq_tq_codebook(head_dim: int, bits: int = 4):
     thr = np.zeros((1 << bits) - 1, np.float32)
     _check(_lib.uq_tq_codebook(head_dim, bits, mags.ctypes.data, thr.ctypes.data), "uq_tq_codebook")
     return mags, thr
+
+
+def uq_prefill_workspace_bytes(num_q_tokens: int, batch: int, num_q_heads: int, num_kv_heads: int,
+                               head_dim: int, max_keys: int) -> int:
+    return int(_lib.uq_prefill_workspace_bytes(num_q_tokens, batch, num_q_heads, num_kv_heads, head_dim, max_keys))
+
+
+def uq_prefill_attention(q, cu_q, cache, block_table, seq_lens, out=None, workspace=None, sm_scale=0.0,
+                         stream=None):
+    """Chunked-prefill attention: q [T][Hq][D] bf16, the chunk of sequence b in rows cu_q[b]..cu_q[b+1]-1
+    (cu_q int32 [B+1]); seq_lens [B] count the chunk; returns fp32 [T][Hq][D]."""
+    _need(q, torch.bfloat16, "q")
+    _need(cu_q, torch.int32, "cu_q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    T, Hq, D = q.shape
+    B = seq_lens.numel()
+    if D != cache.head_dim or cu_q.numel() != B + 1 or block_table.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    if workspace is None:
+        n = uq_prefill_workspace_bytes(T, B, Hq, cache.num_kv_heads, D, block_table.shape[1] * cache.page_size)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.uq_prefill_attention(_ptr(q), _ptr(cu_q), T, C.byref(cache.struct), _ptr(block_table),
+                                     block_table.shape[1], _ptr(seq_lens), B, Hq, float(sm_scale), _ptr(out),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "uq_prefill_attention")
+    return out
 
 
 def uq_check_device_status(stream=None) -> int:

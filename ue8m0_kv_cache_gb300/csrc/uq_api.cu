@@ -220,6 +220,33 @@ uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const in
                        workspace, workspace_bytes, stream, UQ_TQ4);
 }
 
+size_t uq_prefill_workspace_bytes(int32_t num_q_tokens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_keys) {
+  if (num_q_tokens < 0 || batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      (head_dim != 64 && head_dim != 128) || max_keys <= 0)
+    return 0;
+  return uqh::prefill_workspace_bytes(num_q_tokens, batch, num_q_heads, num_kv_heads, head_dim, max_keys);
+}
+
+uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q_tokens, const uq_cache* cache,
+                               const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                               int32_t batch, int32_t num_q_heads, float sm_scale, float* out, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  uq_status st = check_cache(cache);
+  if (st != UQ_OK) return st;
+  if (cache->dtype != UQ_FP4_UE8M0) return UQ_ERR_UNSUPPORTED;
+  if (batch < 0 || num_q_tokens < 0 || num_q_heads <= 0 || max_pages_per_seq < 1) return UQ_ERR_INVALID_ARG;
+  if (num_q_heads % cache->num_kv_heads != 0) return UQ_ERR_INVALID_ARG;
+  if (batch == 0 || num_q_tokens == 0) return UQ_OK;
+  if (batch > 65536) return UQ_ERR_UNSUPPORTED;
+  if ((int64_t)max_pages_per_seq * cache->page_size >= (int64_t(1) << 31)) return UQ_ERR_UNSUPPORTED;
+  if (!q || !cu_q || !block_table || !seq_lens || !out || !workspace) return UQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return UQ_ERR_ALIGNMENT;
+  uqh::PrefillArgs a{q, cu_q, num_q_tokens, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads,
+                     sm_scale, out, workspace, workspace_bytes};
+  return uqh::launch_prefill(a, stream);
+}
+
 uq_status uq_check_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return UQ_ERR_CUDA;
   unsigned int v = 0, zero = 0;

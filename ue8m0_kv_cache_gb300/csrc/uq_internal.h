@@ -105,4 +105,23 @@ uq_status launch_decode(const DecodeArgs& a, cudaStream_t s);
 uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out,
                                 cudaStream_t s);
 
+// Chunked-prefill attention (uq_prefill.cu).
+struct PrefillArgs {
+  const void* q;            // bf16 [T][Hq][D]
+  const int32_t* cu_q;      // [B + 1]
+  int32_t num_q_tokens;     // T
+  const uq_cache* cache;
+  const int32_t* block_table;
+  int32_t max_pages;
+  const int32_t* seq_lens;  // [B]
+  int32_t batch;
+  int32_t num_q_heads;
+  float sm_scale;
+  float* out;               // fp32 [T][Hq][D]
+  void* ws;
+  size_t ws_bytes;
+};
+size_t prefill_workspace_bytes(int T, int B, int hq, int hkv, int d, int max_keys);
+uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
 }  // namespace uqh
