@@ -139,7 +139,7 @@ __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPThreads, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PC<D>;
   constexpr int NG = C::NG;
   constexpr int NKS = D / 16;  // QK k-steps
@@ -350,114 +350,120 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_kernel(const __grid_cons
         fence_proxy_async();
         issue(t + kPNST);
       }
-      // phase C: this warp's 16 rows against the tile's 64 keys
-      float S[8][4];
+      // phase C: this warp's 16 rows against the tile's 64 keys, in two
+      // sub-tiles of 32 keys (fewer live registers: S, P and the QK
+      // accumulators cover 32 keys at a time)
+#pragma unroll 1
+      for (int sub = 0; sub < 2; ++sub) {
+        const int kb0 = kbase + 32 * sub;
+        float S[4][4];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        float acc[8][4];
+        for (int g = 0; g < NG; ++g) {
+          float acc[4][4];
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int ks = 2 * g + kk;
+          for (int kk = 0; kk < 2; ++kk) {
+            const int ks = 2 * g + kk;
 #pragma unroll
-          for (int nbp = 0; nbp < 4; ++nbp) {
-            const int mi = lane >> 3, tok = 8 * (2 * nbp + (mi >> 1)) + (lane & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kf_u32 + tile_off<D>(tok, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-            if (kk == 0) {
-              mma_f16_zc(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-              mma_f16_zc(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            for (int nbp = 0; nbp < 2; ++nbp) {
+              const int mi = lane >> 3, tok = 32 * sub + 8 * (2 * nbp + (mi >> 1)) + (lane & 7);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(kf_u32 + tile_off<D>(tok, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+              if (kk == 0) {
+                mma_f16_zc(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_f16_zc(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+              } else {
+                mma_f16(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_f16(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+              }
+            }
+          }
+#pragma unroll
+          for (int nb = 0; nb < 4; ++nb) {
+            const float2 f = *reinterpret_cast<const float2*>(ksc + g * kKT + 32 * sub + 8 * nb + 2 * c);
+            if (g == 0) {
+              S[nb][0] = acc[nb][0] * f.x; S[nb][1] = acc[nb][1] * f.y;
+              S[nb][2] = acc[nb][2] * f.x; S[nb][3] = acc[nb][3] * f.y;
             } else {
-              mma_f16(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-              mma_f16(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+              S[nb][0] = fmaf(acc[nb][0], f.x, S[nb][0]); S[nb][1] = fmaf(acc[nb][1], f.y, S[nb][1]);
+              S[nb][2] = fmaf(acc[nb][2], f.x, S[nb][2]); S[nb][3] = fmaf(acc[nb][3], f.y, S[nb][3]);
             }
           }
         }
+        // causal and range mask, online softmax (exact running max per row)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-          const float2 f = *reinterpret_cast<const float2*>(ksc + g * kKT + 8 * nb + 2 * c);
-          if (g == 0) {
-            S[nb][0] = acc[nb][0] * f.x; S[nb][1] = acc[nb][1] * f.y;
-            S[nb][2] = acc[nb][2] * f.x; S[nb][3] = acc[nb][3] * f.y;
-          } else {
-            S[nb][0] = fmaf(acc[nb][0], f.x, S[nb][0]); S[nb][1] = fmaf(acc[nb][1], f.y, S[nb][1]);
-            S[nb][2] = fmaf(acc[nb][2], f.x, S[nb][2]); S[nb][3] = fmaf(acc[nb][3], f.y, S[nb][3]);
-          }
+        for (int nb = 0; nb < 4; ++nb) {
+          const int key = kb0 + 8 * nb + 2 * c;
+          S[nb][0] = (key <= pos0 && key < k_hi) ? S[nb][0] * p.sl2e : -INFINITY;
+          S[nb][1] = (key + 1 <= pos0 && key + 1 < k_hi) ? S[nb][1] * p.sl2e : -INFINITY;
+          S[nb][2] = (key <= pos1 && key < k_hi) ? S[nb][2] * p.sl2e : -INFINITY;
+          S[nb][3] = (key + 1 <= pos1 && key + 1 < k_hi) ? S[nb][3] * p.sl2e : -INFINITY;
+          mx0 = fmaxf(mx0, fmaxf(S[nb][0], S[nb][1]));
+          mx1 = fmaxf(mx1, fmaxf(S[nb][2], S[nb][3]));
         }
-      }
-      // causal and range mask, online softmax (exact running max per row)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        const int key = kbase + 8 * nb + 2 * c;
-        S[nb][0] = (key <= pos0 && key < k_hi) ? S[nb][0] * p.sl2e : -INFINITY;
-        S[nb][1] = (key + 1 <= pos0 && key + 1 < k_hi) ? S[nb][1] * p.sl2e : -INFINITY;
-        S[nb][2] = (key <= pos1 && key < k_hi) ? S[nb][2] * p.sl2e : -INFINITY;
-        S[nb][3] = (key + 1 <= pos1 && key + 1 < k_hi) ? S[nb][3] * p.sl2e : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(S[nb][0], S[nb][1]));
-        mx1 = fmaxf(mx1, fmaxf(S[nb][2], S[nb][3]));
-      }
+        for (int o = 1; o < 4; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float a0 = n0 == -INFINITY ? 1.f : ex2(m0 - n0), a1 = n1 == -INFINITY ? 1.f : ex2(m1 - n1);
+        const float base0 = n0 == -INFINITY ? 0.f : n0, base1 = n1 == -INFINITY ? 0.f : n1;
+        m0 = n0;
+        m1 = n1;
+        const float o0 = sub == 0 ? a0 * rvf : a0, o1 = sub == 0 ? a1 * rvf : a1;
 #pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-      }
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = n0 == -INFINITY ? 1.f : ex2(m0 - n0), a1 = n1 == -INFINITY ? 1.f : ex2(m1 - n1);
-      const float base0 = n0 == -INFINITY ? 0.f : n0, base1 = n1 == -INFINITY ? 0.f : n1;
-      m0 = n0;
-      m1 = n1;
-      const float o0 = a0 * rvf, o1 = a1 * rvf;
+        for (int nb = 0; nb < NNB; ++nb) {
+          O[nb][0] *= o0; O[nb][1] *= o0; O[nb][2] *= o1; O[nb][3] *= o1;
+        }
+        float s0 = 0.f, s1 = 0.f;
+        uint32_t ph[2][4], pl[2][4];  // P as A fragments of the sub-tile's 2 key k-steps, hi and lo parts
 #pragma unroll
-      for (int nb = 0; nb < NNB; ++nb) {
-        O[nb][0] *= o0; O[nb][1] *= o0; O[nb][2] *= o1; O[nb][3] *= o1;
-      }
-      float s0 = 0.f, s1 = 0.f;
-      uint32_t ph[4][4], pl[4][4];  // P as A fragments of the 4 key k-steps, hi and lo f16 parts
+        for (int nb = 0; nb < 4; ++nb) {
+          const float q0 = ex2(S[nb][0] - base0), q1 = ex2(S[nb][1] - base0);
+          const float q2 = ex2(S[nb][2] - base1), q3 = ex2(S[nb][3] - base1);
+          s0 += q0 + q1;
+          s1 += q2 + q3;
+          const float h0 = __uint_as_float(__float_as_uint(q0) & 0xFFFFE000u);
+          const float h1 = __uint_as_float(__float_as_uint(q1) & 0xFFFFE000u);
+          const float h2 = __uint_as_float(__float_as_uint(q2) & 0xFFFFE000u);
+          const float h3 = __uint_as_float(__float_as_uint(q3) & 0xFFFFE000u);
+          const int j = nb >> 1, hi = (nb & 1) * 2;  // n-block 2j -> a0, a1; 2j+1 -> a2, a3
+          ph[j][hi] = pack_f16x2(h0, h1);
+          ph[j][hi + 1] = pack_f16x2(h2, h3);
+          pl[j][hi] = pack_f16x2(q0 - h0, q1 - h1);
+          pl[j][hi + 1] = pack_f16x2(q2 - h2, q3 - h3);
+        }
+        l0 = l0 * a0 + s0;
+        l1 = l1 * a1 + s1;
+        // P.V in two halves of the channels, each sub-tile into a fresh accumulator
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        const float q0 = ex2(S[nb][0] - base0), q1 = ex2(S[nb][1] - base0);
-        const float q2 = ex2(S[nb][2] - base1), q3 = ex2(S[nb][3] - base1);
-        s0 += q0 + q1;
-        s1 += q2 + q3;
-        const float h0 = __uint_as_float(__float_as_uint(q0) & 0xFFFFE000u);
-        const float h1 = __uint_as_float(__float_as_uint(q1) & 0xFFFFE000u);
-        const float h2 = __uint_as_float(__float_as_uint(q2) & 0xFFFFE000u);
-        const float h3 = __uint_as_float(__float_as_uint(q3) & 0xFFFFE000u);
-        const int j = nb >> 1, hi = (nb & 1) * 2;  // n-block 2j -> a0, a1; 2j+1 -> a2, a3
-        ph[j][hi] = pack_f16x2(h0, h1);
-        ph[j][hi + 1] = pack_f16x2(h2, h3);
-        pl[j][hi] = pack_f16x2(q0 - h0, q1 - h1);
-        pl[j][hi + 1] = pack_f16x2(q2 - h2, q3 - h3);
-      }
-      l0 = l0 * a0 + s0;
-      l1 = l1 * a1 + s1;
-      // P.V in two halves of the channels, each tile into a fresh accumulator
+        for (int half = 0; half < 2; ++half) {
+          float acc[HNB][4];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float acc[HNB][4];
+          for (int j = 0; j < 2; ++j) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int nbp = 0; nbp < HNB / 2; ++nbp) {
-            const int nbA = half * HNB + 2 * nbp;
-            const int mi = lane >> 3, tok = 16 * j + 8 * (mi & 1) + (lane & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vf_u32 + tile_off<D>(tok, nbA + (mi >> 1)), b0, b1, b2, b3);
-            if (j == 0) {
-              mma_f16_zc(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
-              mma_f16_zc(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
-            } else {
-              mma_f16(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
-              mma_f16(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
+            for (int nbp = 0; nbp < HNB / 2; ++nbp) {
+              const int nbA = half * HNB + 2 * nbp;
+              const int mi = lane >> 3, tok = 32 * sub + 16 * j + 8 * (mi & 1) + (lane & 7);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(vf_u32 + tile_off<D>(tok, nbA + (mi >> 1)), b0, b1, b2, b3);
+              if (j == 0) {
+                mma_f16_zc(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
+                mma_f16_zc(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
+              } else {
+                mma_f16(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
+                mma_f16(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
+              }
+              mma_f16(acc[2 * nbp], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b0, b1);
+              mma_f16(acc[2 * nbp + 1], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b2, b3);
             }
-            mma_f16(acc[2 * nbp], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b0, b1);
-            mma_f16(acc[2 * nbp + 1], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b2, b3);
           }
-        }
 #pragma unroll
-        for (int i = 0; i < HNB; ++i) {
-          add2(O[half * HNB + i][0], O[half * HNB + i][1], acc[i][0], acc[i][1]);
-          add2(O[half * HNB + i][2], O[half * HNB + i][3], acc[i][2], acc[i][3]);
+          for (int i = 0; i < HNB; ++i) {
+            add2(O[half * HNB + i][0], O[half * HNB + i][1], acc[i][0], acc[i][1]);
+            add2(O[half * HNB + i][2], O[half * HNB + i][3], acc[i][2], acc[i][3]);
+          }
         }
       }
       __syncthreads();  // the f16 tiles may be overwritten
