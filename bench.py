@@ -31,6 +31,7 @@ CTX0, APPEND = 32768, 32768
 FP4_BYTES_PER_TOKEN_HEAD = 136   # K and V: 64 code bytes + 4 scale bytes each
 FP8_BYTES_PER_TOKEN_HEAD = 256
 BF16_BYTES_PER_TOKEN_HEAD = 512
+PF_CHUNK = 128                   # prefill chunk per sequence in the prefill measurement
 METRIC = "decode tokens/s at 64K ctx (KV-read GB/s and quantize GB/s reported)"
 WORKLOAD = "append64k: B8 Hkv8 Hq64 D128 ps16, 32768 cached + 32768 appended tokens/seq, then decode steps"
 
@@ -40,6 +41,15 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def _tensor_peak():
+    """Measured dense bf16 tensor rate (TFLOP/s), or the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def _peaks():
@@ -374,6 +384,39 @@ def run_uq(args):
             anchors[name]["quantize"] = tq4_quantize
     assert uq.uq_check_device_status() == 0
 
+    # ---- chunked-prefill attention over the same FP4 cache: the last PF_CHUNK
+    # tokens of every sequence attend causally to its 64K context
+    prefill = None
+    if not args.no_anchors:
+        T = B * PF_CHUNK
+        gq = torch.Generator(device=dev)
+        gq.manual_seed(4242 + rank)
+        qp = torch.randn((T, HQ, D), generator=gq, device=dev).to(torch.bfloat16)
+        cu = torch.arange(0, T + 1, PF_CHUNK, dtype=torch.int32, device=dev)
+        slp = torch.full((B,), L0, dtype=torch.int32, device=dev)
+        wsp_p = torch.empty(max(16, uq.uq_prefill_workspace_bytes(T, B, HQ, HKV, D, bt.shape[1] * PS)),
+                            dtype=torch.uint8, device=dev)
+        outp = torch.empty((T, HQ, D), dtype=torch.float32, device=dev)
+        times = []
+        for i in range(3 + 3):
+            e0, e1 = _event_pair()
+            e0.record(stream)
+            uq.uq_prefill_attention(qp, cu, fp4, bt, slp, out=outp, workspace=wsp_p)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        pt = float(np.median(times))
+        keys = B * HQ * sum(L0 - PF_CHUNK + i + 1 for i in range(PF_CHUNK))
+        flops = 4.0 * D * keys  # QK^T and P.V, one multiply-add each per (query row, key, channel)
+        tens_peak = _tensor_peak()
+        prefill = {"chunk_tokens_per_seq": PF_CHUNK, "context": L0, "ms": pt * 1e3, "TFLOP_per_s": flops / pt / 1e12,
+                   "query_tokens_per_s": T / pt, "tensor_peak_TFLOP_per_s": tens_peak,
+                   "frac_of_tensor_peak": flops / pt / 1e12 / tens_peak,
+                   "note": "mma.sync m16n8k16 f16 tensor path; P.V runs twice (hi + lo parts of P)"}
+        del qp, wsp_p, outp
+    assert uq.uq_check_device_status() == 0
+
     # ---- end to end through the public API with host buffers
     n_e2e = min(steps, 200)
     pin = lambda t: t.cpu().pin_memory()
@@ -416,7 +459,7 @@ def run_uq(args):
             "config": {"workload": WORKLOAD, "context_mean": ctx_mean, "batch_per_gpu": B,
                        "parallelism": "replicas (weak scaling, no collective)" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (FP4 KV read %.0f MB per step)" % (kv_bytes / 1e6)},
-            "kv_GB_per_s": achieved, "quantize": quantize, "anchors": anchors, "roofline": roofline,
+            "kv_GB_per_s": achieved, "quantize": quantize, "anchors": anchors, "prefill": prefill, "roofline": roofline,
             "clocks": clk, "e2e": e2e, "gpu_launches": 2 * steps, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
 
