@@ -43,6 +43,25 @@ def _dist():
     return ws, rank, local
 
 
+def _rank_seed(rank: int) -> int:
+    """Seed of rank `rank`'s own batch of sequences (weak scaling: every rank a different batch)."""
+    return 1005 + 7919 * rank
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_throughput(ws: int, seqs_per_rank: int, steps: int, total_s: float) -> float:
+    """Decode tokens/s of the whole job: every rank decodes its own sequences each step."""
+    return ws * seqs_per_rank * steps / total_s
+
+
 def _tensor_peak():
     """Measured dense bf16 tensor rate (TFLOP/s), or the fallback."""
     try:
@@ -240,7 +259,7 @@ def run_uq(args):
     steps, warmup = args.steps, args.warmup
     extra = steps + warmup + 8
     # Each rank holds its own batch of 8 sequences (weak scaling, no collective on the data path).
-    w = workloads.make("append64k", seq_lens=[CTX0 + APPEND] * B, extra_tokens=extra, seed=1005 + 7919 * rank)
+    w = workloads.make("append64k", seq_lens=[CTX0 + APPEND] * B, extra_tokens=extra, seed=_rank_seed(rank))
     stream = torch.cuda.current_stream()
     caches = {"fp4": uq.KVCache(uq.FP4_UE8M0, w.num_pages, HKV, PS, D, device=dev)}
     if not args.no_anchors:
@@ -356,15 +375,12 @@ def run_uq(args):
     clocks = Clocks(local if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0, _pci_bus_id(dev))
     total, dec_t, clk = timed("fp4", clocks)
     assert uq.uq_check_device_status() == 0
-    if ws > 1:
-        t = torch.tensor([total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
+    total = _max_over_ranks(total, ws, dev)
     ctx_mean = L0 + warmup + (steps + 1) / 2.0
     kv_bytes = B * HKV * ctx_mean * FP4_BYTES_PER_TOKEN_HEAD
     hbm, peak_kind = _peaks()
     ms_per_step = total / steps * 1e3
-    value = ws * B * steps / total
+    value = _job_throughput(ws, B, steps, total)
     achieved = kv_bytes / dec_t / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": _captured_traffic(B * HKV * ctx_mean), "peak_kind": peak_kind,
