@@ -88,8 +88,8 @@ __device__ __forceinline__ float pow2f(int e) {
   return 0.f;
 }
 
-// Row tiles of sequence b: ceil(n_b * G / 64).
-__device__ __forceinline__ int row_tiles(int n, int G) { return (n * G + kPRows - 1) / kPRows; }
+// Row tiles of sequence b: ceil(n_b * G / rows), rows the query rows of one work item.
+__device__ __forceinline__ int row_tiles(int n, int G, int rows) { return (n * G + rows - 1) / rows; }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -117,7 +117,8 @@ namespace {
 
 // Work items: for every sequence b, kv head, row tile and key split one item,
 // in that order; item_pre[b] counts the items of sequences before b.
-__global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, int splits, int32_t* item_pre) {
+__global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, int splits, int rows,
+                                    int32_t* item_pre) {
   const int lane = threadIdx.x;
   int run = 0;
   if (lane == 0) item_pre[0] = 0;
@@ -126,7 +127,7 @@ __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, 
     int x = 0;
     if (b < B) {
       const int n = max(0, cu_q[b + 1] - cu_q[b]);
-      x = Hkv * row_tiles(n, G) * splits;
+      x = Hkv * row_tiles(n, G, rows) * splits;
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
       if (q0 < 0 || q0 + n > p.T) n = 0;
     }
     const int ctx = L - n;  // keys before the chunk
-    const int tiles_b = row_tiles(n_plan, p.G);
+    const int tiles_b = row_tiles(n_plan, p.G, kPRows);
     const int64_t local = item - p.item_pre[b];
     const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * p.splits));
     const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * p.splits);
@@ -217,24 +218,30 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
     const int lp_last = (L - 1) >> p.ps_log2;  // last page of the sequence
 
     // ---- producer: lanes of warp 0 issue one tile's bulk copies, one copy each
-    auto issue = [&](int t) {
+    // warp 0, one lane per bulk copy of a tile: the page of the lane's copy
+    // (a global load, done one tile ahead), then the copy
+    auto page_of = [&](int t) {
+      const int rows_per = min(1 << p.ps_log2, kKT);
+      const int key = k_lo + t * kKT + (lane >> 2) * rows_per;
+      int lp = key >> p.ps_log2;
+      lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
+      int page = (lane < 4 * (kKT / rows_per)) ? bt_row[lp] : 0;
+      if (page < 0 || page >= p.num_pages) {
+        record_error(p.status, kErrBounds);
+        page = 0;
+      }
+      return page;
+    };
+    auto issue = [&](int t, int page) {
       const int st = (git + t) % kPNST;
       uint8_t* base = raw + st * C::RAW;
-      constexpr int R0 = 16;
-      const int rows_per = min(1 << p.ps_log2, kKT);  // rows of one page run
+      const int rows_per = min(1 << p.ps_log2, kKT);
       const int runs = kKT / rows_per;
       if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::RAW);
       __syncwarp();
       if (lane < 4 * runs) {
         const int run = lane >> 2, what = lane & 3;  // 0 K codes, 1 V codes, 2 K scales, 3 V scales
         const int key = k_lo + t * kKT + run * rows_per;
-        int lp = key >> p.ps_log2;
-        lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
-        int page = bt_row[lp];
-        if (page < 0 || page >= p.num_pages) {
-          record_error(p.status, kErrBounds);
-          page = 0;
-        }
         const int64_t row = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (key & ((1 << p.ps_log2) - 1));
         const int rb = what < 2 ? C::KROW : C::SROW;
         const uint8_t* src = (what == 0 ? p.kc : what == 1 ? p.vc : what == 2 ? p.ks : p.vs) + row * rb;
@@ -242,11 +249,10 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
                         run * rows_per * rb;
         bulk_g2s(base + dst, src, static_cast<uint32_t>(rows_per * rb), &bars[st]);
       }
-      (void)R0;
     };
     if (warp == 0) {
       fence_proxy_async();
-      for (int t = 0; t < (ntiles < kPNST ? ntiles : kPNST); ++t) issue(t);
+      for (int t = 0; t < (ntiles < kPNST ? ntiles : kPNST); ++t) issue(t, page_of(t));
     }
     if (tid == 0) *s_badpos = 0x7FFFFFFF;
 
@@ -283,6 +289,8 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
     bool aborted = false;
 
     for (int t = 0; t < ntiles; ++t) {
+      // page of the tile this iteration refills, loaded now so its latency hides behind the tile's work
+      const int nxt_page = (warp == 0 && t + kPNST < ntiles) ? page_of(t + kPNST) : 0;
       const int st = (git + t) % kPNST;
       const uint8_t* rk = raw + st * C::RAW;
       const uint8_t* rv = rk + kKT * C::KROW;
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             const int kb = rks[tid * C::SROW + g], vb = rvs[tid * C::SROW + g];
-            vmax = max(vmax, vb);
+            if (vb != 0xFF) vmax = max(vmax, vb);  // a non-finite group is handled by badpos
             bad |= (kb == 0xFF) | (vb == 0xFF);
           }
           atomicMax(&s_rvt[slot], vmax);
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kf_u32 + tile_off<D>(tok, 4 * g + w)),
                      "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
         uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (kbase + tok < k_hi) {
+        if (kbase + tok < k_hi && rvs[tok * C::SROW + pos / 4] != 0xFF) {
           const int vbyte = rvs[tok * C::SROW + pos / 4];
           const float f = pow2f(vbyte - RV);
           const uint32_t f2 = pack_f16x2(f, f);
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
       __syncthreads();
       if (warp == 0 && t + kPNST < ntiles) {  // the raw stage is free again
         fence_proxy_async();
-        issue(t + kPNST);
+        issue(t + kPNST, nxt_page);
       }
       // phase C: this warp's 16 rows against the tile's 64 keys, in two
       // sub-tiles of 32 keys (fewer live registers: S, P and the QK
@@ -496,13 +504,508 @@ __global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_cons
   pdl_trigger();
 }
 
+// ------------------------------------------------------------ tensor-memory (tcgen05) variant
+//
+// One CTA of 4 warps takes 128 query rows (one row per thread and per TMEM
+// lane) and a key range in tiles of 64 keys.  Per tile:
+//   1. the block converts the raw FP4 tile into f16 operands in the 128-byte
+//      swizzled K-major layout of the tensor cores: K' = code * 2^(byte - R_tok)
+//      (R_tok the largest group byte of the key, so every value is <= 6 and the
+//      per-key factor 2^(R_tok - 127) is applied to the logits), and V'^T =
+//      code * 2^(byte - RV) with channels as rows;
+//   2. one thread issues S = Q K'^T (M 128, N 64, 8 MMAs of K 16) into tensor
+//      memory;
+//   3. every thread reads its row of S, applies the key factors, the causal
+//      mask and the online softmax, and writes P = p (hi and lo f16 parts) back
+//      to tensor memory;
+//   4. one thread issues O_win += P V' (M 128, N 128, A = P from tensor memory).
+// O_win accumulates over a window of at most kWin tiles with one fixed
+// reference (running max and RV) and is then added to the row's fp32 O in
+// registers with IEEE rounding -- also whenever the reference must change --
+// so long contexts do not compound the accumulator's rounding.
+constexpr int kTRows = 128;     // query rows per CTA
+constexpr int kTKT = 64;        // keys per tile
+constexpr int kTNST = 3;        // raw stages
+constexpr int kTWin = 4;        // tiles per O window
+constexpr int kTCols = 256;     // tensor memory columns: S [0,64), P hi [64,96), P lo [96,128), O_win [128,256)
+constexpr float kTSlack = 8.f;  // running max raised only when a logit exceeds it by more than this (log2)
+
+template <int D>
+struct TC {
+  static constexpr int KROW = D / 2, SROW = D / 32, NG = D / 32;
+  static constexpr int RAW = 2 * kTKT * KROW + 2 * kTKT * SROW;
+  static constexpr int ATOMS = D / 64;               // 128-byte swizzle atoms along a D-channel row
+  static constexpr int QB = kTRows * 2 * D;          // Q, f16, [atom][row][128 B]
+  static constexpr int KB = kTKT * 2 * D;            // K', f16, [atom][key][128 B]
+  static constexpr int VB = D * kTKT * 2;            // V'^T, f16, [channel][128 B = 64 keys]
+  static constexpr int OFF_Q = 0;                    // operands first: 1024-byte aligned
+  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_V = OFF_K + KB;
+  static constexpr int OFF_RAW = OFF_V + VB;
+  static constexpr int OFF_KS = OFF_RAW + kTNST * RAW;  // fp32 [64] per-key logit factors
+  static constexpr int OFF_BAR = OFF_KS + kTKT * 4;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers and block state, + slack for the 1024-byte alignment
+};
+
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr) {
+  // shared-memory matrix descriptor: 128-byte swizzle (layout 2), 8-row groups 1024 B apart, version 1
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(16 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// kind::f16 instruction descriptors, D f32, A and B f16 K-major, M 128.
+constexpr uint32_t tc_idesc(int n) { return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24); }
+
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b),
+               "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d), "r"(a_tmem), "l"(b),
+               "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(addr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase by polling try_wait without a suspend
+// hint: the tensor-core completions waited for here take a few hundred cycles,
+// and a suspended thread would be woken later than that.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long long budget) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(a), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+
+// Byte offset of 16-byte chunk `ch` (8 f16) of row `row` in a K-major
+// operand of `rows` rows stored as 128-byte swizzled atoms: atom ch / 8 is a
+// [rows][128 B] block; inside it the chunk index is XORed with row & 7.
+__device__ __forceinline__ uint32_t sw128_off(int rows, int row, int ch) {
+  return static_cast<uint32_t>((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+  using C = TC<D>;
+  constexpr int NG = C::NG;
+  constexpr int KW = C::KROW / 4;  // code words per row
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t q_u32 = sb + C::OFF_Q, k_u32 = sb + C::OFF_K, v_u32 = sb + C::OFF_V;
+  uint8_t* raw = sm + C::OFF_RAW;
+  float* kfac = reinterpret_cast<float*>(sm + C::OFF_KS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);  // [0, kTNST) raw ring, [3] S done, [4] P.V done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 64);
+  int* s_vmax = reinterpret_cast<int*>(sm + C::OFF_BAR + 72);   // [2] tile max V byte
+  int* s_bad = s_vmax + 2;                                      // [2] tile's first key with a 0xFF group
+  int* s_kr = s_bad + 2;                                        // [64] largest K scale byte of each key
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTNST + 2; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    s_vmax[0] = s_vmax[1] = 0;
+    s_bad[0] = s_bad[1] = 0x7FFFFFFF;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "r"(kTCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
+  pdl_wait();
+  int64_t total = p.item_pre[p.B];
+  if (total > p.max_items) {
+    if (blockIdx.x == 0 && tid == 0) record_error(p.status, kErrBounds);
+    total = 0;
+  }
+  const int cap = p.max_pages << p.ps_log2;
+  uint32_t git = 0, s_phase = 0, pv_phase = 0;
+  bool pv_pending = false, failed = false;
+
+  for (int64_t item = blockIdx.x; item < total && !failed; item += gridDim.x) {
+    int lb = 1, hb = p.B;
+    while (lb < hb) {
+      const int mid = (lb + hb) >> 1;
+      if (p.item_pre[mid] > item) hb = mid; else lb = mid + 1;
+    }
+    const int b = lb - 1;
+    const int q0 = p.cu_q[b], n_plan = max(0, p.cu_q[b + 1] - q0);
+    int L = p.seq_lens[b];
+    int n = n_plan;
+    if (L < 0 || L > cap || n > L || q0 < 0 || q0 + n > p.T) {
+      if (tid == 0) record_error(p.status, kErrBounds);
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+      n = n > L ? L : n;
+      if (q0 < 0 || q0 + n > p.T) n = 0;
+    }
+    const int ctx = L - n;
+    const int tiles_b = row_tiles(n_plan, p.G, kTRows);
+    const int64_t local = item - p.item_pre[b];
+    const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * p.splits));
+    const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * p.splits);
+    const int rtile = rem / p.splits, split = rem - rtile * p.splits;
+    const int row0 = rtile * kTRows, nrows = n * p.G;
+    const int last_row = min(row0 + kTRows, nrows) - 1;
+    const int pos_max = ctx + last_row / p.G;
+    const int k_lo = split * p.kchunk;
+    const int k_hi = min(k_lo + p.kchunk, pos_max + 1);
+    const int my_row = row0 + tid;
+    const int pos = my_row < nrows ? ctx + my_row / p.G : -1;
+    float* ml_out = p.ws_ml + item * (kTRows * 2);
+    float* o_out = p.ws_o + item * (static_cast<int64_t>(kTRows) * D);
+    if (k_lo >= k_hi) {
+      ml_out[2 * tid] = -INFINITY;
+      ml_out[2 * tid + 1] = 0.f;
+      continue;
+    }
+    const int ntiles = (k_hi - k_lo + kTKT - 1) / kTKT;
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
+    const int lp_last = (L - 1) >> p.ps_log2;
+
+    // warp 0, one lane per bulk copy of a tile: the page of the lane's copy
+    // (a global load, done one tile ahead), then the copy
+    auto page_of = [&](int t) {
+      const int rows_per = min(1 << p.ps_log2, kTKT);
+      const int key = k_lo + t * kTKT + (lane >> 2) * rows_per;
+      int lp = key >> p.ps_log2;
+      lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
+      int page = (lane < 4 * (kTKT / rows_per)) ? bt_row[lp] : 0;
+      if (page < 0 || page >= p.num_pages) {
+        record_error(p.status, kErrBounds);
+        page = 0;
+      }
+      return page;
+    };
+    auto issue = [&](int t, int page) {
+      const int st = (git + t) % kTNST;
+      uint8_t* base = raw + st * C::RAW;
+      const int rows_per = min(1 << p.ps_log2, kTKT);
+      const int runs = kTKT / rows_per;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::RAW);
+      __syncwarp();
+      if (lane < 4 * runs) {
+        const int run = lane >> 2, what = lane & 3;  // 0 K codes, 1 V codes, 2 K scales, 3 V scales
+        const int key = k_lo + t * kTKT + run * rows_per;
+        const int64_t row = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (key & ((1 << p.ps_log2) - 1));
+        const int rb = what < 2 ? C::KROW : C::SROW;
+        const uint8_t* src = (what == 0 ? p.kc : what == 1 ? p.vc : what == 2 ? p.ks : p.vs) + row * rb;
+        const int dst = (what < 2 ? what * kTKT * C::KROW : 2 * kTKT * C::KROW + (what - 2) * kTKT * C::SROW) +
+                        run * rows_per * rb;
+        bulk_g2s(base + dst, src, static_cast<uint32_t>(rows_per * rb), &bars[st]);
+      }
+    };
+    if (warp == 0) {
+      fence_proxy_async();
+      for (int t = 0; t < (ntiles < kTNST ? ntiles : kTNST); ++t) issue(t, page_of(t));
+    }
+    // this thread's query row: rotated E4M3 -> f16, in the swizzled K-major A layout
+    {
+      const uint8_t* qsrc = p.qbytes + ((static_cast<int64_t>(q0) + (my_row < nrows ? my_row / p.G : 0)) * p.Hq +
+                                        kvh * p.G + (my_row < nrows ? my_row % p.G : 0)) * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {
+        uint2 w = make_uint2(0u, 0u);
+        if (my_row < nrows) w = *reinterpret_cast<const uint2*>(qsrc + 8 * ch);
+        const uint32_t h0 = e4m3x2_to_f16x2(w.x), h1 = e4m3x2_to_f16x2(w.x >> 16);
+        const uint32_t h2 = e4m3x2_to_f16x2(w.y), h3 = e4m3x2_to_f16x2(w.y >> 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_u32 + sw128_off(kTRows, tid, ch)), "r"(h0),
+                     "r"(h1), "r"(h2), "r"(h3) : "memory");
+      }
+    }
+
+    float m = -INFINITY, l = 0.f;
+    float O[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) O[k] = 0.f;
+    int RV = 0, badpos = 0x7FFFFFFF, win = 0;
+
+    for (int t = 0; t < ntiles; ++t) {
+      // page of the tile this iteration refills, loaded now so its latency hides behind the tile's work
+      const int nxt_page = (warp == 0 && t + kTNST < ntiles) ? page_of(t + kTNST) : 0;
+      const int st = (git + t) % kTNST;
+      const uint8_t* rk = raw + st * C::RAW;
+      const uint8_t* rv = rk + kTKT * C::KROW;
+      const uint8_t* rks = rv + kTKT * C::KROW;
+      const uint8_t* rvs = rks + kTKT * C::SROW;
+      const int kbase = k_lo + t * kTKT;
+      const int slot = t & 1;
+      // (a) the previous tile's P.V must be done before its operands are overwritten
+      bool ok = true;
+      if (pv_pending) {
+        ok = mbar_spin(&bars[kTNST + 1], pv_phase & 1, kWaitBudget);
+        ++pv_phase;
+        pv_pending = false;
+        tc_after();
+      }
+      ok = ok && mbar_spin(&bars[st], ((git + t) / kTNST) & 1, kWaitBudget);
+      // (b) per key: largest K scale byte, logit factor; the tile's largest V byte and first non-finite key
+      if (tid < kTKT) {
+        const int key = kbase + tid;
+        int kr = 0, vmax = 0, bad = 0;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const int kb = rks[tid * C::SROW + g], vb = rvs[tid * C::SROW + g];
+          kr = max(kr, kb);
+          if (vb != 0xFF) vmax = max(vmax, vb);  // a non-finite group is handled by badpos
+          bad |= (kb == 0xFF) | (vb == 0xFF);
+        }
+        s_kr[tid] = kr;
+        kfac[tid] = pow2f(kr - 127) * p.sl2e;
+        if (key < k_hi) {
+          atomicMax(&s_vmax[slot], vmax);
+          if (bad) atomicMin(&s_bad[slot], key);
+        }
+      }
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      const int RVn = max(RV, s_vmax[slot]);
+      badpos = min(badpos, s_bad[slot]);
+      if (tid == 0) {
+        s_vmax[slot ^ 1] = 0;
+        s_bad[slot ^ 1] = 0x7FFFFFFF;
+      }
+      // (c) K' = code * 2^(byte - R_key), V'^T = code * 2^(byte - RVn) (0 past the range)
+      for (int wi = tid; wi < kTKT * KW; wi += kPThreads) {
+        const int tok = wi / KW, pos = wi - tok * KW;
+        const int g = pos % NG, w = pos / NG;  // K rows: word w of group g at position NG*w + g
+        const float f = pow2f(static_cast<int>(rks[tok * C::SROW + g]) - s_kr[tok]);
+        const uint32_t f2 = pack_f16x2(f, f);
+        uint32_t h[4];
+        e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(rk)[wi], h);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = hmul2(h[k], f2);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(k_u32 + sw128_off(kTKT, tok, 4 * g + w)),
+                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+      }
+      for (int pw = tid; pw < (kTKT / 2) * KW; pw += kPThreads) {
+        const int i = pw / KW, pos = pw - i * KW, t0 = 2 * i, t1 = t0 + 1, gv = pos / 4;
+        const uint32_t w0 = reinterpret_cast<const uint32_t*>(rv)[t0 * KW + pos];
+        const uint32_t w1 = reinterpret_cast<const uint32_t*>(rv)[t1 * KW + pos];
+        const int vb0 = rvs[t0 * C::SROW + gv], vb1 = rvs[t1 * C::SROW + gv];
+        const float f0 = (kbase + t0 < k_hi && vb0 != 0xFF) ? pow2f(vb0 - RVn) : 0.f;
+        const float f1 = (kbase + t1 < k_hi && vb1 != 0xFF) ? pow2f(vb1 - RVn) : 0.f;
+        const uint32_t fm = pack_f16x2(f0, f1);
+        uint32_t e[4], o[4];
+        e2m1x8_to_f16x2((w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4), e);  // channels 8 pos + 2j
+        e2m1x8_to_f16x2(((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u), o);  // channels 8 pos + 2j + 1
+        const uint32_t colb = (t0 & 7) * 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ce = 8 * pos + 2 * j, co = ce + 1;
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(v_u32 + sw128_off(D, ce, t0 >> 3) + colb), "r"(hmul2(e[j], fm))
+                       : "memory");
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(v_u32 + sw128_off(D, co, t0 >> 3) + colb), "r"(hmul2(o[j], fm))
+                       : "memory");
+        }
+      }
+      fence_proxy_async();  // generic-proxy operand writes, read next by the tensor cores
+      tc_before();
+      __syncthreads();
+      // (d) S = Q K'^T into tensor memory columns [0, 64)
+      if (tid == 0) {
+        tc_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t a = tc_desc(q_u32 + (ks >> 2) * (kTRows * 128) + (ks & 3) * 32);
+          const uint64_t bd = tc_desc(k_u32 + (ks >> 2) * (kTKT * 128) + (ks & 3) * 32);
+          tc_mma_ss(tmem, a, bd, tc_idesc(kTKT), ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars[kTNST]);
+      }
+      if (warp == 0 && t + kTNST < ntiles) {  // the raw stage is free again
+        fence_proxy_async();
+        issue(t + kTNST, nxt_page);
+      }
+      ok = mbar_spin(&bars[kTNST], s_phase & 1, kWaitBudget);
+      ++s_phase;
+      tc_after();
+      // (e) this thread's row: logits, mask, online softmax, P to tensor memory
+      float x[kTKT];
+      {
+        uint32_t r32[32];
+        tmem_ld32(tmem + lanes + 0, r32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r32[k]);
+        tmem_ld32(tmem + lanes + 32, r32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kTKT; ++k) {
+        const int key = kbase + k;
+        x[k] = (key <= pos && key < k_hi) ? x[k] * kfac[k] : -INFINITY;
+        mx = fmaxf(mx, x[k]);
+      }
+      const bool need = mx > m + kTSlack || (m == -INFINITY && mx > -INFINITY);
+      const bool fold = __syncthreads_or(need || !ok) != 0 || RVn != RV || win == kTWin;
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      if (fold) {
+        if (win > 0) {  // the window's P.V finished in (a); add it to O with IEEE rounding
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r32[32];
+            tmem_ld32(tmem + lanes + 128 + c0, r32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) O[c0 + k] += __uint_as_float(r32[k]);
+          }
+        }
+        if (need) {
+          const float mn = fmaxf(m, mx);
+          const float a = m == -INFINITY ? 0.f : ex2(m - mn);
+#pragma unroll
+          for (int k = 0; k < D; ++k) O[k] *= a;
+          l *= a;
+          m = mn;
+        }
+        if (RVn != RV) {
+          const float f = pow2f(RV - RVn);
+#pragma unroll
+          for (int k = 0; k < D; ++k) O[k] *= f;
+          RV = RVn;
+        }
+        win = 0;
+      }
+      {
+        const float base = m == -INFINITY ? 0.f : m;
+        uint32_t ph[32], pl[32];
+#pragma unroll
+        for (int k = 0; k < kTKT; k += 2) {
+          const float p0 = ex2(x[k] - base), p1 = ex2(x[k + 1] - base);
+          l += p0 + p1;
+          const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+          const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+          ph[k / 2] = pack_f16x2(h0, h1);
+          pl[k / 2] = pack_f16x2(p0 - h0, p1 - h1);
+        }
+        tmem_st32(tmem + lanes + 64, ph);
+        tmem_st32(tmem + lanes + 96, pl);
+        tmem_wait_st();
+      }
+      tc_before();
+      __syncthreads();
+      // (f) O_win (+)= P V' into tensor memory columns [128, 128 + D)
+      if (tid == 0) {
+        tc_after();
+#pragma unroll
+        for (int j = 0; j < kTKT / 16; ++j) {
+          const uint64_t bd = tc_desc(v_u32 + j * 32);
+          tc_mma_ts(tmem + 128, tmem + 64 + 8 * j, bd, tc_idesc(D), (win > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 128, tmem + 96 + 8 * j, bd, tc_idesc(D), 1u);
+        }
+        tc_commit(&bars[kTNST + 1]);
+      }
+      pv_pending = true;
+      ++win;
+    }
+    git += ntiles;
+    if (failed) break;
+    // the item's last window, then the partial (m, l, O) of this row
+    bool ok = true;
+    if (pv_pending) {
+      ok = mbar_spin(&bars[kTNST + 1], pv_phase & 1, kWaitBudget);
+      ++pv_phase;
+      pv_pending = false;
+      tc_after();
+    }
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    if (win > 0) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r32[32];
+        tmem_ld32(tmem + lanes + 128 + c0, r32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) O[c0 + k] += __uint_as_float(r32[k]);
+      }
+    }
+    const float osc = pow2f(RV - 127);  // V' was code * 2^(byte - RV)
+    ml_out[2 * tid] = m;
+    ml_out[2 * tid + 1] = pos >= badpos ? __int_as_float(0x7FC00000) : l;
+#pragma unroll
+    for (int k = 0; k < D; k += 4)
+      *reinterpret_cast<float4*>(o_out + static_cast<int64_t>(tid) * D + k) =
+          make_float4(O[k] * osc, O[k + 1] * osc, O[k + 2] * osc, O[k + 3] * osc);
+    tc_before();
+    __syncthreads();  // every thread's tensor-memory reads done before the next item's MMAs
+    tc_after();
+  }
+  if (failed) {
+    if (tid == 0) {
+      record_error(p.status, kErrTimeout);
+      // let copies and MMAs in flight finish before the block's memory goes away
+      for (int s = 0; s < kTNST; ++s) mbar_wait(&bars[s], ((git + s) / kTNST) & 1, kWaitBudget);
+      if (pv_pending) mbar_wait(&bars[kTNST + 1], pv_phase & 1, kWaitBudget);
+    }
+  }
+  tc_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTCols));
+  }
+  pdl_trigger();
+}
+
 struct PrefillMergeParams {
   const float* ws_ml;
   const float* ws_o;
   const int32_t* item_pre;
   const int32_t* cu_q;
   const int32_t* seq_lens;
-  int B, T, Hq, G, splits, cap;
+  int B, T, Hq, G, splits, cap, rows;
   int64_t max_items;
   float* out;
   uqh::SignMasks sign;
@@ -536,12 +1039,12 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
   for (int e = 0; e < EPL; ++e) o[e] = 0.f;
   if (i >= 0 && i < n) {
     const int kvh = h / p.G, hl = h - kvh * p.G;
-    const int rowi = i * p.G + hl, rtile = rowi / kPRows, rr = rowi - rtile * kPRows;
-    const int64_t item0 = p.item_pre[b] + (static_cast<int64_t>(kvh) * row_tiles(n_plan, p.G) + rtile) * p.splits;
+    const int rowi = i * p.G + hl, rtile = rowi / p.rows, rr = rowi - rtile * p.rows;
+    const int64_t item0 = p.item_pre[b] + (static_cast<int64_t>(kvh) * row_tiles(n_plan, p.G, p.rows) + rtile) * p.splits;
     float Ms = -INFINITY;
     for (int s0 = 0; s0 < p.splits; s0 += 32) {
       const int s = s0 + lane;
-      if (s < p.splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * kPRows + rr) * 2]);
+      if (s < p.splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * p.rows + rr) * 2]);
     }
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
@@ -551,11 +1054,11 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
       float w = 0.f;
       bool live = false;
       if (s < p.splits) {
-        const float m = p.ws_ml[((item0 + s) * kPRows + rr) * 2];
+        const float m = p.ws_ml[((item0 + s) * p.rows + rr) * 2];
         live = m != -INFINITY;  // an empty split wrote no output row
         if (live) {
           w = ex2(m - Ms);
-          Ls += w * p.ws_ml[((item0 + s) * kPRows + rr) * 2 + 1];
+          Ls += w * p.ws_ml[((item0 + s) * p.rows + rr) * 2 + 1];
         }
       }
       const unsigned mask = __ballot_sync(kFull, live);
@@ -563,7 +1066,7 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
       for (int j = 0; j < cnt; ++j) {
         const float wj = __shfl_sync(kFull, w, j);
         if ((mask >> j) & 1u) {
-          const float* src = p.ws_o + ((item0 + s0 + j) * kPRows + rr) * D + lane * EPL;
+          const float* src = p.ws_o + ((item0 + s0 + j) * p.rows + rr) * D + lane * EPL;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) o[e] += wj * src[e];
         }
@@ -614,10 +1117,10 @@ struct PrefillPlan {
   size_t off_pre, off_q, off_ml, off_o, total;
 };
 
-PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int sms) {
+PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int sms, int rows) {
   PrefillPlan pl;
   const int G = hq / hkv;
-  const int64_t tiles = (static_cast<int64_t>(T) * G + kPRows - 1) / kPRows + B;  // bound on row tiles per kv head
+  const int64_t tiles = (static_cast<int64_t>(T) * G + rows - 1) / rows + B;  // bound on row tiles per kv head
   const int64_t base = static_cast<int64_t>(hkv) * tiles;
   const int64_t target = 2LL * 2 * sms;  // two waves of two blocks per SM
   const int max_splits = std::max(1, (max_keys + kKT - 1) / kKT);
@@ -627,28 +1130,39 @@ PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int
   pl.off_pre = 256;
   pl.off_q = pl.off_pre + align256(static_cast<size_t>(B + 1) * 4);
   pl.off_ml = pl.off_q + align256(static_cast<size_t>(T) * hq * d);
-  pl.off_o = pl.off_ml + align256(static_cast<size_t>(pl.max_items) * kPRows * 2 * 4);
-  pl.total = pl.off_o + static_cast<size_t>(pl.max_items) * kPRows * d * 4;
+  pl.off_o = pl.off_ml + align256(static_cast<size_t>(pl.max_items) * rows * 2 * 4);
+  pl.total = pl.off_o + static_cast<size_t>(pl.max_items) * rows * d * 4;
   return pl;
 }
 
+// The prefill kernel in use: the tensor-memory (tcgen05) kernel with 128 rows
+// per work item, or the warp-MMA kernel with 64.
+constexpr bool kPrefillTC = true;
+constexpr int kItemRows = kPrefillTC ? kTRows : kPRows;
+
 template <int D>
 uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
-  using C = PC<D>;
   const uq_cache& c = *a.cache;
   const uqh::DevInfo& di = uqh::dev_info();
   const int G = a.num_q_heads / c.num_kv_heads;
   const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D,
-                                      a.max_pages * c.page_size, di.sms);
+                                      a.max_pages * c.page_size, di.sms, kItemRows);
   if (a.ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
-  auto kern = prefill_kernel<D>;
+  auto kern = kPrefillTC ? prefill_tc_kernel<D> : prefill_kernel<D>;
+  const int smem = kPrefillTC ? TC<D>::SMEM : PC<D>::SMEM;
   static int cfg_dev = -1;
   static int per_sm = 0;
   if (cfg_dev != di.device) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return UQ_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPThreads, C::SMEM) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPThreads, smem) != cudaSuccess || per_sm < 1)
       return UQ_ERR_CUDA;
+    // The tensor-memory kernel runs two CTAs per SM: their shared memory (2 x 93 KB),
+    // registers (2 x 128 x 255) and tensor-memory columns (2 x 256 of 512) fit, and
+    // each CTA's serial phases (convert, QK^T, softmax, P.V) overlap the other's.
+    // (The occupancy query reports one for this kernel; measured, two are resident.)
+    if (kPrefillTC) per_sm = 512 / kTCols;
     cfg_dev = di.device;
   }
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -680,13 +1194,13 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   p.status = uqh::status_word();
   if (!p.status) return UQ_ERR_CUDA;
 
-  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.batch, G, c.num_kv_heads, pl.splits, p.item_pre);
+  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.batch, G, c.num_kv_heads, pl.splits, kItemRows, p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
   const uq_status st = uqh::launch_test_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
                                                   c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
   const int64_t grid = std::min<int64_t>(pl.max_items, static_cast<int64_t>(di.sms) * per_sm);
-  if (uqh::launch_pdl(kern, static_cast<unsigned>(std::max<int64_t>(grid, 1)), kPThreads, C::SMEM, s, p) !=
+  if (uqh::launch_pdl(kern, static_cast<unsigned>(std::max<int64_t>(grid, 1)), kPThreads, smem, s, p) !=
       cudaSuccess)
     return UQ_ERR_CUDA;
   PrefillMergeParams mp;
@@ -700,6 +1214,7 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   mp.Hq = a.num_q_heads;
   mp.G = G;
   mp.splits = pl.splits;
+  mp.rows = kItemRows;
   mp.max_items = pl.max_items;
   mp.cap = a.max_pages * c.page_size;
   mp.out = a.out;
@@ -714,7 +1229,7 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
 namespace uqh {
 
 size_t prefill_workspace_bytes(int T, int B, int hq, int hkv, int d, int max_keys) {
-  return plan_prefill(T, B, hq, hkv, d, max_keys, std::max(1, dev_info().sms)).total;
+  return plan_prefill(T, B, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows).total;
 }
 
 uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s) {
