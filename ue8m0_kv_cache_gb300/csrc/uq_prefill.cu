@@ -9,23 +9,27 @@
 // the output is rotated back.
 //
 // GB300 design (many query rows per key: a dense contraction, unlike decode)
-//   * A block takes 64 query rows of one (sequence, kv head) -- consecutive
-//     (token, head) pairs of the chunk, 16 per warp -- and one range of keys.
-//     Keys arrive in tiles of 64 tokens: the page rows of the tile's K codes,
-//     V codes and both scale rows come by 1-D bulk copies (TMA engine) into a
-//     ring of raw stages; the block converts each tile ONCE into f16 tiles in
-//     shared memory (K: the codes, exact; V: code * 2^(byte - RV), RV the
-//     block's running maximum V scale byte), so the conversion is shared by
-//     the 64 query rows instead of being repeated per 8 heads as in decode.
-//   * Each warp runs FlashAttention-style m16n8k16 MMAs: QK^T with B from
-//     ldmatrix on the swizzled K tile, one 32-channel group at a time into a
-//     fresh accumulator, times the group's 2^(byte-127) in fp32; online
-//     softmax on the register fragments; P (hi + lo f16 parts) as the A operand
-//     straight from the S fragments; P.V with B from ldmatrix.trans on the V
-//     tile, each tile summed in a fresh accumulator and added to the fp32
-//     output with IEEE rounding (as in decode).
-//   * Long key ranges are split over blocks; each (row tile, key split) writes
-//     a partial (m, l, O) and a merge kernel combines them by log-sum-exp and
+//   * A CTA of 4 warps takes 128 query rows of one (sequence, kv head) --
+//     consecutive (token, head) pairs of the chunk, one row per thread and per
+//     tensor-memory lane -- and one range of keys, in tiles of 64 keys.  The
+//     page rows of a tile's K codes, V codes and both scale rows come by 1-D
+//     bulk copies (TMA engine) into a ring of raw stages.
+//   * The CTA converts each raw tile ONCE into f16 operands in the tensor
+//     cores' 128-byte swizzled layout, shared by all 128 rows: K' = code *
+//     2^(byte - R_key) K-major (R_key the key's largest group byte, so every
+//     value is <= 6 in magnitude and the per-key factor 2^(R_key - 127) goes
+//     on the logit), V' = code * 2^(byte - RV) MN-major (channels contiguous,
+//     RV the CTA's running maximum V byte); exact in f16 except where a V
+//     group lies so far below RV that its values underflow.
+//   * One thread issues S = Q K'^T (tcgen05.mma kind::f16, M 128, N 64) into
+//     tensor memory; every thread reads its row of S, applies the key factors,
+//     the causal mask and the online softmax, and writes P back to tensor
+//     memory as hi and lo f16 parts; one thread issues O_win += P V' with A
+//     from tensor memory.  O_win sums a window of up to four tiles under one
+//     reference (running max, RV) and is then added to the row's fp32 O in
+//     registers with IEEE rounding, as the decode adds its per-unit partials.
+//   * Long key ranges are split over CTAs; each (row tile, key split) writes a
+//     partial (m, l, O) and a merge kernel combines them by log-sum-exp and
 //     applies the inverse rotation.
 #include <algorithm>
 #include <cmath>
@@ -37,28 +41,7 @@ namespace {
 
 using namespace uqd;
 
-constexpr int kPWarps = 4;
-constexpr int kPThreads = 32 * kPWarps;
-constexpr int kPRows = 16 * kPWarps;  // query rows per block
-constexpr int kKT = 64;               // keys per tile
-constexpr int kPNST = 3;              // raw stages in the ring
-
-template <int D>
-struct PC {
-  static constexpr int KROW = D / 2;             // code bytes per row
-  static constexpr int SROW = D / 32;            // scale bytes per row
-  static constexpr int NG = D / 32;              // groups
-  static constexpr int RAW = 2 * kKT * KROW + 2 * kKT * SROW;  // one raw tile
-  static constexpr int TILEB = kKT * D * 2;      // one f16 tile (K or V)
-  static constexpr int QB = 16 * D;              // E4M3 query bytes per warp
-  // raw ring | K f16 | V f16 | K scales (fp32 [NG][kKT]) | query staging | barriers + block state
-  static constexpr int OFF_K = kPNST * RAW;
-  static constexpr int OFF_V = OFF_K + TILEB;
-  static constexpr int OFF_S = OFF_V + TILEB;
-  static constexpr int OFF_Q = OFF_S + NG * kKT * 4;
-  static constexpr int OFF_B = OFF_Q + kPWarps * QB;
-  static constexpr int SMEM = OFF_B + 128;
-};
+constexpr int kPThreads = 128;  // 4 warps: one query row per thread
 
 struct PrefillParams {
   const uint8_t* qbytes;     // rotated E4M3 query, [T][Hq][D]
@@ -72,7 +55,7 @@ struct PrefillParams {
   const uint8_t* vs;
   int B, T, Hq, Hkv, G, ps_log2, num_pages;
   int splits;                // key splits per row tile
-  int kchunk;                // keys per split (multiple of kKT)
+  int kchunk;                // keys per split (multiple of the key tile)
   float sl2e;                // softmax scale * log2(e)
   float* ws_ml;              // partials: [items][64 rows][2]
   float* ws_o;               // partials: [items][64 rows][D]
@@ -90,26 +73,6 @@ __device__ __forceinline__ float pow2f(int e) {
 
 // Row tiles of sequence b: ceil(n_b * G / rows), rows the query rows of one work item.
 __device__ __forceinline__ int row_tiles(int n, int G, int rows) { return (n * G + rows - 1) / rows; }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// Byte offset of 16-byte chunk `ch` of row `row` in an f16 tile of D columns:
-// the chunk index is XORed with the row's low 3 bits, so the 8 rows an
-// ldmatrix reads at one logical chunk fall into 8 different bank groups.
-template <int D>
-__device__ __forceinline__ uint32_t tile_off(int row, int ch) {
-  return static_cast<uint32_t>(row * (D * 2) + ((ch ^ (row & 7)) << 4));
-}
 
 }  // namespace
 
@@ -139,390 +102,7 @@ __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, 
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PC<D>;
-  constexpr int NG = C::NG;
-  constexpr int NKS = D / 16;  // QK k-steps
-  constexpr int NNB = D / 8;   // P.V n-blocks (8 channels each)
-  constexpr int HNB = NNB / 2; // n-blocks per P.V half
-  constexpr int KW = C::KROW / 4;  // code words per row
-  extern __shared__ __align__(128) uint8_t sm[];
-  uint8_t* raw = sm;
-  float* ksc = reinterpret_cast<float*>(sm + C::OFF_S);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_B);
-  int* s_rvt = reinterpret_cast<int*>(sm + C::OFF_B + 8 * kPNST);  // [2] tile max V byte
-  int* s_badpos = s_rvt + 2;                                     // first key with a 0xFF byte
-  const uint32_t kf_u32 = smem_u32(sm + C::OFF_K), vf_u32 = smem_u32(sm + C::OFF_V);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, c = lane & 3;
-  if (tid == 0) {
-    for (int s = 0; s < kPNST; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-    s_rvt[0] = s_rvt[1] = 0;
-  }
-  __syncthreads();
-  pdl_wait();
-  int64_t total = p.item_pre[p.B];
-  if (total > p.max_items) {  // cu_q inconsistent with num_q_tokens: do nothing
-    if (blockIdx.x == 0 && tid == 0) record_error(p.status, kErrBounds);
-    total = 0;
-  }
-  const int cap = p.max_pages << p.ps_log2;
-  uint32_t git = 0;  // tiles through the ring so far (stage and parity)
-
-  for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
-    // ---- which sequence, kv head, row tile and key split
-    int lb = 1, hb = p.B;  // first b + 1 with item_pre[b + 1] > item
-    while (lb < hb) {
-      const int mid = (lb + hb) >> 1;
-      if (p.item_pre[mid] > item) hb = mid; else lb = mid + 1;
-    }
-    const int b = lb - 1;
-    const int q0 = p.cu_q[b], n_plan = max(0, p.cu_q[b + 1] - q0);  // the plan's row count
-    int L = p.seq_lens[b];
-    int n = n_plan;
-    if (L < 0 || L > cap || n > L || q0 < 0 || q0 + n > p.T) {
-      if (tid == 0) record_error(p.status, kErrBounds);
-      L = L < 0 ? 0 : (L > cap ? cap : L);
-      n = n > L ? L : n;
-      if (q0 < 0 || q0 + n > p.T) n = 0;
-    }
-    const int ctx = L - n;  // keys before the chunk
-    const int tiles_b = row_tiles(n_plan, p.G, kPRows);
-    const int64_t local = item - p.item_pre[b];
-    const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * p.splits));
-    const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * p.splits);
-    const int rtile = rem / p.splits, split = rem - rtile * p.splits;
-    const int row0 = rtile * kPRows;
-    const int nrows = n * p.G;
-    const int last_row = min(row0 + kPRows, nrows) - 1;
-    const int pos_max = ctx + last_row / p.G;  // the tile's last query position
-    const int k_lo = split * p.kchunk;
-    const int k_hi = min(k_lo + p.kchunk, pos_max + 1);
-    // this warp's rows r and r + 8
-    const int wr0 = row0 + warp * 16 + r, wr1 = wr0 + 8;
-    const int pos0 = wr0 < nrows ? ctx + wr0 / p.G : -1;
-    const int pos1 = wr1 < nrows ? ctx + wr1 / p.G : -1;
-    float* ml_out = p.ws_ml + item * (kPRows * 2);
-    float* o_out = p.ws_o + item * (static_cast<int64_t>(kPRows) * D);
-    if (k_lo >= k_hi) {  // the split lies past every row's position: an empty partial
-      if (tid < kPRows) {
-        ml_out[2 * tid] = -INFINITY;
-        ml_out[2 * tid + 1] = 0.f;
-      }
-      continue;
-    }
-    const int ntiles = (k_hi - k_lo + kKT - 1) / kKT;
-    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
-    const int lp_last = (L - 1) >> p.ps_log2;  // last page of the sequence
-
-    // ---- producer: lanes of warp 0 issue one tile's bulk copies, one copy each
-    // warp 0, one lane per bulk copy of a tile: the page of the lane's copy
-    // (a global load, done one tile ahead), then the copy
-    auto page_of = [&](int t) {
-      const int rows_per = min(1 << p.ps_log2, kKT);
-      const int key = k_lo + t * kKT + (lane >> 2) * rows_per;
-      int lp = key >> p.ps_log2;
-      lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
-      int page = (lane < 4 * (kKT / rows_per)) ? bt_row[lp] : 0;
-      if (page < 0 || page >= p.num_pages) {
-        record_error(p.status, kErrBounds);
-        page = 0;
-      }
-      return page;
-    };
-    auto issue = [&](int t, int page) {
-      const int st = (git + t) % kPNST;
-      uint8_t* base = raw + st * C::RAW;
-      const int rows_per = min(1 << p.ps_log2, kKT);
-      const int runs = kKT / rows_per;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::RAW);
-      __syncwarp();
-      if (lane < 4 * runs) {
-        const int run = lane >> 2, what = lane & 3;  // 0 K codes, 1 V codes, 2 K scales, 3 V scales
-        const int key = k_lo + t * kKT + run * rows_per;
-        const int64_t row = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (key & ((1 << p.ps_log2) - 1));
-        const int rb = what < 2 ? C::KROW : C::SROW;
-        const uint8_t* src = (what == 0 ? p.kc : what == 1 ? p.vc : what == 2 ? p.ks : p.vs) + row * rb;
-        const int dst = (what < 2 ? what * kKT * C::KROW : 2 * kKT * C::KROW + (what - 2) * kKT * C::SROW) +
-                        run * rows_per * rb;
-        bulk_g2s(base + dst, src, static_cast<uint32_t>(rows_per * rb), &bars[st]);
-      }
-    };
-    if (warp == 0) {
-      fence_proxy_async();
-      for (int t = 0; t < (ntiles < kPNST ? ntiles : kPNST); ++t) issue(t, page_of(t));
-    }
-    if (tid == 0) *s_badpos = 0x7FFFFFFF;
-
-    // ---- the warp's 16 query rows: rotated E4M3 bytes -> f16 A fragments
-    uint32_t qa[NKS][4];
-    {
-      uint8_t* qs = sm + C::OFF_Q + warp * C::QB;
-      constexpr int CH = D / 16;  // 16-byte chunks per row
-      for (int idx = lane; idx < 16 * CH; idx += 32) {
-        const int rr = idx / CH, ch = idx - rr * CH, row = row0 + warp * 16 + rr;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < nrows) {
-          const int64_t qrow = (static_cast<int64_t>(q0) + row / p.G) * p.Hq + kvh * p.G + row % p.G;
-          v = *reinterpret_cast<const uint4*>(p.qbytes + qrow * D + ch * 16);
-        }
-        *reinterpret_cast<uint4*>(qs + rr * D + ch * 16) = v;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int ks = 0; ks < NKS; ++ks) {
-        qa[ks][0] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(qs + r * D + 16 * ks + 2 * c));
-        qa[ks][1] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(qs + (r + 8) * D + 16 * ks + 2 * c));
-        qa[ks][2] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(qs + r * D + 16 * ks + 2 * c + 8));
-        qa[ks][3] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(qs + (r + 8) * D + 16 * ks + 2 * c + 8));
-      }
-    }
-    __syncthreads();  // s_badpos set; every warp past its previous item's last tile
-
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float O[NNB][4];
-#pragma unroll
-    for (int nb = 0; nb < NNB; ++nb) O[nb][0] = O[nb][1] = O[nb][2] = O[nb][3] = 0.f;
-    int RV = 0;  // running maximum V scale byte of this item (the same in every thread)
-    bool aborted = false;
-
-    for (int t = 0; t < ntiles; ++t) {
-      // page of the tile this iteration refills, loaded now so its latency hides behind the tile's work
-      const int nxt_page = (warp == 0 && t + kPNST < ntiles) ? page_of(t + kPNST) : 0;
-      const int st = (git + t) % kPNST;
-      const uint8_t* rk = raw + st * C::RAW;
-      const uint8_t* rv = rk + kKT * C::KROW;
-      const uint8_t* rks = rv + kKT * C::KROW;
-      const uint8_t* rvs = rks + kKT * C::SROW;
-      const int kbase = k_lo + t * kKT;
-      const bool ok = mbar_wait(&bars[st], ((git + t) / kPNST) & 1, kWaitBudget);
-      if (!__syncthreads_and(ok)) {  // a copy never landed: record, drain and give up on the launch
-        if (tid == 0) {
-          record_error(p.status, kErrTimeout);
-          for (int k = t; k < (ntiles < t + kPNST ? ntiles : t + kPNST); ++k)
-            mbar_wait(&bars[(git + k) % kPNST], ((git + k) / kPNST) & 1, kWaitBudget);
-        }
-        aborted = true;
-        break;
-      }
-      // phase A: the tile's largest V scale byte and its first non-finite group, over valid keys
-      const int slot = t & 1;
-      if (tid < kKT) {
-        const int key = kbase + tid;
-        if (key < k_hi) {
-          int vmax = 0, bad = 0;
-#pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const int kb = rks[tid * C::SROW + g], vb = rvs[tid * C::SROW + g];
-            if (vb != 0xFF) vmax = max(vmax, vb);  // a non-finite group is handled by badpos
-            bad |= (kb == 0xFF) | (vb == 0xFF);
-          }
-          atomicMax(&s_rvt[slot], vmax);
-          if (bad) atomicMin(s_badpos, key);
-        }
-      }
-      __syncthreads();
-      const int RVn = max(RV, s_rvt[slot]);
-      const float rvf = pow2f(RV - RVn);  // rescale of O when the reference grows
-      RV = RVn;
-      if (tid == 0) s_rvt[slot ^ 1] = 0;
-      // phase B: the tile in f16 -- K codes (exact) in natural channel order,
-      // V codes times 2^(byte - RV); keys past the range are zero in V
-      for (int wi = tid; wi < kKT * KW; wi += kPThreads) {
-        const int tok = wi / KW, pos = wi - tok * KW;
-        uint32_t h[4];
-        e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(rk)[wi], h);
-        const int g = pos % NG, w = pos / NG;  // K rows: word w of group g at position NG*w + g
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kf_u32 + tile_off<D>(tok, 4 * g + w)),
-                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (kbase + tok < k_hi && rvs[tok * C::SROW + pos / 4] != 0xFF) {
-          const int vbyte = rvs[tok * C::SROW + pos / 4];
-          const float f = pow2f(vbyte - RV);
-          const uint32_t f2 = pack_f16x2(f, f);
-          e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(rv)[wi], v);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) v[k] = hmul2(v[k], f2);
-        }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vf_u32 + tile_off<D>(tok, pos)),
-                     "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
-      }
-      for (int i = tid; i < NG * kKT; i += kPThreads) {
-        const int g = i / kKT, tok = i - g * kKT;
-        ksc[i] = __uint_as_float(static_cast<uint32_t>(rks[tok * C::SROW + g]) << 23);  // 2^(byte-127); 0 -> 0
-      }
-      __syncthreads();
-      if (warp == 0 && t + kPNST < ntiles) {  // the raw stage is free again
-        fence_proxy_async();
-        issue(t + kPNST, nxt_page);
-      }
-      // phase C: this warp's 16 rows against the tile's 64 keys, in two
-      // sub-tiles of 32 keys (fewer live registers: S, P and the QK
-      // accumulators cover 32 keys at a time)
-#pragma unroll 1
-      for (int sub = 0; sub < 2; ++sub) {
-        const int kb0 = kbase + 32 * sub;
-        float S[4][4];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          float acc[4][4];
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const int ks = 2 * g + kk;
-#pragma unroll
-            for (int nbp = 0; nbp < 2; ++nbp) {
-              const int mi = lane >> 3, tok = 32 * sub + 8 * (2 * nbp + (mi >> 1)) + (lane & 7);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(kf_u32 + tile_off<D>(tok, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-              if (kk == 0) {
-                mma_f16_zc(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_f16_zc(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-              } else {
-                mma_f16(acc[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_f16(acc[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-              }
-            }
-          }
-#pragma unroll
-          for (int nb = 0; nb < 4; ++nb) {
-            const float2 f = *reinterpret_cast<const float2*>(ksc + g * kKT + 32 * sub + 8 * nb + 2 * c);
-            if (g == 0) {
-              S[nb][0] = acc[nb][0] * f.x; S[nb][1] = acc[nb][1] * f.y;
-              S[nb][2] = acc[nb][2] * f.x; S[nb][3] = acc[nb][3] * f.y;
-            } else {
-              S[nb][0] = fmaf(acc[nb][0], f.x, S[nb][0]); S[nb][1] = fmaf(acc[nb][1], f.y, S[nb][1]);
-              S[nb][2] = fmaf(acc[nb][2], f.x, S[nb][2]); S[nb][3] = fmaf(acc[nb][3], f.y, S[nb][3]);
-            }
-          }
-        }
-        // causal and range mask, online softmax (exact running max per row)
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb) {
-          const int key = kb0 + 8 * nb + 2 * c;
-          S[nb][0] = (key <= pos0 && key < k_hi) ? S[nb][0] * p.sl2e : -INFINITY;
-          S[nb][1] = (key + 1 <= pos0 && key + 1 < k_hi) ? S[nb][1] * p.sl2e : -INFINITY;
-          S[nb][2] = (key <= pos1 && key < k_hi) ? S[nb][2] * p.sl2e : -INFINITY;
-          S[nb][3] = (key + 1 <= pos1 && key + 1 < k_hi) ? S[nb][3] * p.sl2e : -INFINITY;
-          mx0 = fmaxf(mx0, fmaxf(S[nb][0], S[nb][1]));
-          mx1 = fmaxf(mx1, fmaxf(S[nb][2], S[nb][3]));
-        }
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-        }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float a0 = n0 == -INFINITY ? 1.f : ex2(m0 - n0), a1 = n1 == -INFINITY ? 1.f : ex2(m1 - n1);
-        const float base0 = n0 == -INFINITY ? 0.f : n0, base1 = n1 == -INFINITY ? 0.f : n1;
-        m0 = n0;
-        m1 = n1;
-        const float o0 = sub == 0 ? a0 * rvf : a0, o1 = sub == 0 ? a1 * rvf : a1;
-#pragma unroll
-        for (int nb = 0; nb < NNB; ++nb) {
-          O[nb][0] *= o0; O[nb][1] *= o0; O[nb][2] *= o1; O[nb][3] *= o1;
-        }
-        float s0 = 0.f, s1 = 0.f;
-        uint32_t ph[2][4], pl[2][4];  // P as A fragments of the sub-tile's 2 key k-steps, hi and lo parts
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb) {
-          const float q0 = ex2(S[nb][0] - base0), q1 = ex2(S[nb][1] - base0);
-          const float q2 = ex2(S[nb][2] - base1), q3 = ex2(S[nb][3] - base1);
-          s0 += q0 + q1;
-          s1 += q2 + q3;
-          const float h0 = __uint_as_float(__float_as_uint(q0) & 0xFFFFE000u);
-          const float h1 = __uint_as_float(__float_as_uint(q1) & 0xFFFFE000u);
-          const float h2 = __uint_as_float(__float_as_uint(q2) & 0xFFFFE000u);
-          const float h3 = __uint_as_float(__float_as_uint(q3) & 0xFFFFE000u);
-          const int j = nb >> 1, hi = (nb & 1) * 2;  // n-block 2j -> a0, a1; 2j+1 -> a2, a3
-          ph[j][hi] = pack_f16x2(h0, h1);
-          ph[j][hi + 1] = pack_f16x2(h2, h3);
-          pl[j][hi] = pack_f16x2(q0 - h0, q1 - h1);
-          pl[j][hi + 1] = pack_f16x2(q2 - h2, q3 - h3);
-        }
-        l0 = l0 * a0 + s0;
-        l1 = l1 * a1 + s1;
-        // P.V in two halves of the channels, each sub-tile into a fresh accumulator
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float acc[HNB][4];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-#pragma unroll
-            for (int nbp = 0; nbp < HNB / 2; ++nbp) {
-              const int nbA = half * HNB + 2 * nbp;
-              const int mi = lane >> 3, tok = 32 * sub + 16 * j + 8 * (mi & 1) + (lane & 7);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(vf_u32 + tile_off<D>(tok, nbA + (mi >> 1)), b0, b1, b2, b3);
-              if (j == 0) {
-                mma_f16_zc(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
-                mma_f16_zc(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
-              } else {
-                mma_f16(acc[2 * nbp], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b0, b1);
-                mma_f16(acc[2 * nbp + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], b2, b3);
-              }
-              mma_f16(acc[2 * nbp], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b0, b1);
-              mma_f16(acc[2 * nbp + 1], pl[j][0], pl[j][1], pl[j][2], pl[j][3], b2, b3);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < HNB; ++i) {
-            add2(O[half * HNB + i][0], O[half * HNB + i][1], acc[i][0], acc[i][1]);
-            add2(O[half * HNB + i][2], O[half * HNB + i][3], acc[i][2], acc[i][3]);
-          }
-        }
-      }
-      __syncthreads();  // the f16 tiles may be overwritten
-    }
-    if (aborted) break;
-    git += ntiles;
-    // ---- partial of this (row tile, key split): m, l (quad-reduced) and unnormalised O
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-      l0 += __shfl_xor_sync(kFull, l0, o);
-      l1 += __shfl_xor_sync(kFull, l1, o);
-    }
-    const int badpos = *s_badpos;  // rows that see a non-finite group are NaN
-    if (pos0 >= badpos) l0 = __int_as_float(0x7FC00000);
-    if (pos1 >= badpos) l1 = __int_as_float(0x7FC00000);
-    const float osc = pow2f(RV - 127);  // V was taken as code * 2^(byte - RV)
-    const int lr0 = warp * 16 + r, lr1 = lr0 + 8;
-    if (c == 0) {
-      ml_out[2 * lr0] = m0;
-      ml_out[2 * lr0 + 1] = l0;
-      ml_out[2 * lr1] = m1;
-      ml_out[2 * lr1 + 1] = l1;
-    }
-#pragma unroll
-    for (int nb = 0; nb < NNB; ++nb) {
-      *reinterpret_cast<float2*>(o_out + lr0 * D + 8 * nb + 2 * c) = make_float2(O[nb][0] * osc, O[nb][1] * osc);
-      *reinterpret_cast<float2*>(o_out + lr1 * D + 8 * nb + 2 * c) = make_float2(O[nb][2] * osc, O[nb][3] * osc);
-    }
-  }
-  pdl_trigger();
-}
-
-// ------------------------------------------------------------ tensor-memory (tcgen05) variant
-//
-// One CTA of 4 warps takes 128 query rows (one row per thread and per TMEM
-// lane) and a key range in tiles of 64 keys.  Per tile:
-//   1. the block converts the raw FP4 tile into f16 operands in the 128-byte
-//      swizzled K-major layout of the tensor cores: K' = code * 2^(byte - R_tok)
-//      (R_tok the largest group byte of the key, so every value is <= 6 and the
-//      per-key factor 2^(R_tok - 127) is applied to the logits), and V'^T =
-//      code * 2^(byte - RV) with channels as rows;
-//   2. one thread issues S = Q K'^T (M 128, N 64, 8 MMAs of K 16) into tensor
-//      memory;
-//   3. every thread reads its row of S, applies the key factors, the causal
-//      mask and the online softmax, and writes P = p (hi and lo f16 parts) back
-//      to tensor memory;
-//   4. one thread issues O_win += P V' (M 128, N 128, A = P from tensor memory).
-// O_win accumulates over a window of at most kWin tiles with one fixed
-// reference (running max and RV) and is then added to the row's fp32 O in
-// registers with IEEE rounding -- also whenever the reference must change --
-// so long contexts do not compound the accumulator's rounding.
+// ------------------------------------------------------------ tensor-memory (tcgen05) kernel
 constexpr int kTRows = 128;     // query rows per CTA
 constexpr int kTKT = 64;        // keys per tile
 constexpr int kTNST = 3;        // raw stages
@@ -534,10 +114,9 @@ template <int D>
 struct TC {
   static constexpr int KROW = D / 2, SROW = D / 32, NG = D / 32;
   static constexpr int RAW = 2 * kTKT * KROW + 2 * kTKT * SROW;
-  static constexpr int ATOMS = D / 64;               // 128-byte swizzle atoms along a D-channel row
   static constexpr int QB = kTRows * 2 * D;          // Q, f16, [atom][row][128 B]
   static constexpr int KB = kTKT * 2 * D;            // K', f16, [atom][key][128 B]
-  static constexpr int VB = D * kTKT * 2;            // V'^T, f16, [channel][128 B = 64 keys]
+  static constexpr int VB = kTKT * 2 * D;            // V', f16, MN-major: [atom][key][128 B = 64 channels]
   static constexpr int OFF_Q = 0;                    // operands first: 1024-byte aligned
   static constexpr int OFF_K = OFF_Q + QB;
   static constexpr int OFF_V = OFF_K + KB;
@@ -552,8 +131,18 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t addr) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(16 >> 4) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
-// kind::f16 instruction descriptors, D f32, A and B f16 K-major, M 128.
-constexpr uint32_t tc_idesc(int n) { return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24); }
+// MN-major operand with the 128-byte swizzle: 64 contiguous f16 of the M/N
+// dimension per 128-byte row, 8 K rows per 1024-byte atom; the next 8 K rows
+// 1024 bytes on (stride offset), the next 64 M/N elements `lead` bytes on.
+__device__ __forceinline__ uint64_t tc_desc_mn(uint32_t addr, uint32_t lead) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lead >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// kind::f16 instruction descriptors: D f32, A and B f16, A K-major, B K-major
+// or (b_mn) MN-major, M 128.
+constexpr uint32_t tc_idesc(int n, bool b_mn = false) {
+  return (1u << 4) | (b_mn ? 1u << 16 : 0u) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24);
+}
 
 __device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -807,39 +396,31 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         s_vmax[slot ^ 1] = 0;
         s_bad[slot ^ 1] = 0x7FFFFFFF;
       }
-      // (c) K' = code * 2^(byte - R_key), V'^T = code * 2^(byte - RVn) (0 past the range)
+      // (c) K' = code * 2^(byte - R_key) and V' = code * 2^(byte - RVn) (0 past the range), 8 channels
+      // of one key per thread and step; 8 neighbouring threads fill one swizzled 128-byte row
       for (int wi = tid; wi < kTKT * KW; wi += kPThreads) {
-        const int tok = wi / KW, pos = wi - tok * KW;
-        const int g = pos % NG, w = pos / NG;  // K rows: word w of group g at position NG*w + g
-        const float f = pow2f(static_cast<int>(rks[tok * C::SROW + g]) - s_kr[tok]);
-        const uint32_t f2 = pack_f16x2(f, f);
-        uint32_t h[4];
-        e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(rk)[wi], h);
+        const int tok = wi / KW, ch = wi - tok * KW;  // 16-byte chunk ch = channels 8 ch .. 8 ch + 7
+        const int g = ch >> 2;
+        const uint32_t off = sw128_off(kTKT, tok, ch);
+        // K rows are group-interleaved (word w of group g at position NG * w + g), V rows natural
+        const uint32_t kw = reinterpret_cast<const uint32_t*>(rk)[tok * KW + NG * (ch & 3) + g];
+        const uint32_t vw = reinterpret_cast<const uint32_t*>(rv)[wi];
+        const int vb = rvs[tok * C::SROW + g];
+        const float fk = pow2f(static_cast<int>(rks[tok * C::SROW + g]) - s_kr[tok]);
+        const float fv = (kbase + tok < k_hi && vb != 0xFF) ? pow2f(vb - RVn) : 0.f;
+        const uint32_t fk2 = pack_f16x2(fk, fk), fv2 = pack_f16x2(fv, fv);
+        uint32_t hk[4], hv[4];
+        e2m1x8_to_f16x2(kw, hk);
+        e2m1x8_to_f16x2(vw, hv);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) h[k] = hmul2(h[k], f2);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(k_u32 + sw128_off(kTKT, tok, 4 * g + w)),
-                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-      }
-      for (int pw = tid; pw < (kTKT / 2) * KW; pw += kPThreads) {
-        const int i = pw / KW, pos = pw - i * KW, t0 = 2 * i, t1 = t0 + 1, gv = pos / 4;
-        const uint32_t w0 = reinterpret_cast<const uint32_t*>(rv)[t0 * KW + pos];
-        const uint32_t w1 = reinterpret_cast<const uint32_t*>(rv)[t1 * KW + pos];
-        const int vb0 = rvs[t0 * C::SROW + gv], vb1 = rvs[t1 * C::SROW + gv];
-        const float f0 = (kbase + t0 < k_hi && vb0 != 0xFF) ? pow2f(vb0 - RVn) : 0.f;
-        const float f1 = (kbase + t1 < k_hi && vb1 != 0xFF) ? pow2f(vb1 - RVn) : 0.f;
-        const uint32_t fm = pack_f16x2(f0, f1);
-        uint32_t e[4], o[4];
-        e2m1x8_to_f16x2((w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4), e);  // channels 8 pos + 2j
-        e2m1x8_to_f16x2(((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u), o);  // channels 8 pos + 2j + 1
-        const uint32_t colb = (t0 & 7) * 2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ce = 8 * pos + 2 * j, co = ce + 1;
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(v_u32 + sw128_off(D, ce, t0 >> 3) + colb), "r"(hmul2(e[j], fm))
-                       : "memory");
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(v_u32 + sw128_off(D, co, t0 >> 3) + colb), "r"(hmul2(o[j], fm))
-                       : "memory");
+        for (int k = 0; k < 4; ++k) {
+          hk[k] = hmul2(hk[k], fk2);
+          hv[k] = hmul2(hv[k], fv2);
         }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(k_u32 + off), "r"(hk[0]), "r"(hk[1]),
+                     "r"(hk[2]), "r"(hk[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(v_u32 + off), "r"(hv[0]), "r"(hv[1]),
+                     "r"(hv[2]), "r"(hv[3]) : "memory");
       }
       fence_proxy_async();  // generic-proxy operand writes, read next by the tensor cores
       tc_before();
@@ -937,10 +518,10 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       if (tid == 0) {
         tc_after();
 #pragma unroll
-        for (int j = 0; j < kTKT / 16; ++j) {
-          const uint64_t bd = tc_desc(v_u32 + j * 32);
-          tc_mma_ts(tmem + 128, tmem + 64 + 8 * j, bd, tc_idesc(D), (win > 0 || j > 0) ? 1u : 0u);
-          tc_mma_ts(tmem + 128, tmem + 96 + 8 * j, bd, tc_idesc(D), 1u);
+        for (int j = 0; j < kTKT / 16; ++j) {  // keys 16 j .. 16 j + 15: two 8-key rows of swizzle atoms
+          const uint64_t bd = tc_desc_mn(v_u32 + j * 2048, kTKT * 128);
+          tc_mma_ts(tmem + 128, tmem + 64 + 8 * j, bd, tc_idesc(D, true), (win > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 128, tmem + 96 + 8 * j, bd, tc_idesc(D, true), 1u);
         }
         tc_commit(&bars[kTNST + 1]);
       }
@@ -1123,9 +704,9 @@ PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int
   const int64_t tiles = (static_cast<int64_t>(T) * G + rows - 1) / rows + B;  // bound on row tiles per kv head
   const int64_t base = static_cast<int64_t>(hkv) * tiles;
   const int64_t target = 2LL * 2 * sms;  // two waves of two blocks per SM
-  const int max_splits = std::max(1, (max_keys + kKT - 1) / kKT);
+  const int max_splits = std::max(1, (max_keys + kTKT - 1) / kTKT);
   pl.splits = static_cast<int>(std::min<int64_t>(max_splits, std::max<int64_t>(1, (target + base - 1) / base)));
-  pl.kchunk = ((max_keys + pl.splits - 1) / pl.splits + kKT - 1) / kKT * kKT;
+  pl.kchunk = ((max_keys + pl.splits - 1) / pl.splits + kTKT - 1) / kTKT * kTKT;
   pl.max_items = base * pl.splits;
   pl.off_pre = 256;
   pl.off_q = pl.off_pre + align256(static_cast<size_t>(B + 1) * 4);
@@ -1135,10 +716,7 @@ PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int
   return pl;
 }
 
-// The prefill kernel in use: the tensor-memory (tcgen05) kernel with 128 rows
-// per work item, or the warp-MMA kernel with 64.
-constexpr bool kPrefillTC = true;
-constexpr int kItemRows = kPrefillTC ? kTRows : kPRows;
+constexpr int kItemRows = kTRows;  // query rows per work item
 
 template <int D>
 uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
@@ -1148,21 +726,19 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D,
                                       a.max_pages * c.page_size, di.sms, kItemRows);
   if (a.ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
-  auto kern = kPrefillTC ? prefill_tc_kernel<D> : prefill_kernel<D>;
-  const int smem = kPrefillTC ? TC<D>::SMEM : PC<D>::SMEM;
+  auto kern = prefill_tc_kernel<D>;
+  const int smem = TC<D>::SMEM;
   static int cfg_dev = -1;
   static int per_sm = 0;
   if (cfg_dev != di.device) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return UQ_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPThreads, smem) != cudaSuccess || per_sm < 1)
-      return UQ_ERR_CUDA;
-    // The tensor-memory kernel runs two CTAs per SM: their shared memory (2 x 93 KB),
-    // registers (2 x 128 x 255) and tensor-memory columns (2 x 256 of 512) fit, and
-    // each CTA's serial phases (convert, QK^T, softmax, P.V) overlap the other's.
-    // (The occupancy query reports one for this kernel; measured, two are resident.)
-    if (kPrefillTC) per_sm = 512 / kTCols;
+    // Two CTAs per SM: their shared memory (2 x 93 KB), registers (2 x 128 x 255)
+    // and tensor-memory columns (2 x 256 of 512) fit, and each CTA's serial phases
+    // (convert, QK^T, softmax, P.V) overlap the other's.  The occupancy query
+    // reports one for this kernel; measured, two are resident.
+    per_sm = 512 / kTCols;
     cfg_dev = di.device;
   }
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
