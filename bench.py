@@ -429,7 +429,8 @@ def run_uq(args):
         prefill = {"chunk_tokens_per_seq": PF_CHUNK, "context": L0, "ms": pt * 1e3, "TFLOP_per_s": flops / pt / 1e12,
                    "query_tokens_per_s": T / pt, "tensor_peak_TFLOP_per_s": tens_peak,
                    "frac_of_tensor_peak": flops / pt / 1e12 / tens_peak,
-                   "note": "mma.sync m16n8k16 f16 tensor path; P.V runs twice (hi + lo parts of P)"}
+                   "note": "tcgen05 kind::f16, M 128 x N 64 tiles, S/P/O in tensor memory; "
+                           "P.V runs twice (hi + lo parts of P)"}
         del qp, wsp_p, outp
     assert uq.uq_check_device_status() == 0
 
