@@ -508,7 +508,11 @@ def run_decode_only(args):
     torch.cuda.set_device(dev)
     import ue8m0_kv_cache_gb300 as uq
     import workloads
-    w = workloads.make(args.workload)
+    over = {}
+    if args.batch > 0:
+        base = workloads.make(args.workload)
+        over = dict(B=args.batch, seq_lens=[base.seq_lens[b % base.B] for b in range(args.batch)])
+    w = workloads.make(args.workload, **over)
     cache = uq.KVCache(uq.FP4_UE8M0, w.num_pages, w.Hkv, w.ps, w.D, device=dev)
     for b in range(w.B):
         start = w.shared_prefix if (b > 0 and w.shared_prefix) else 0
@@ -518,6 +522,10 @@ def run_decode_only(args):
             uq.uq_quantize_append(k, v, torch.from_numpy(w.slots(b, t0, n)).to(dev), cache)
     bt = torch.from_numpy(w.block_table).to(dev)
     sl = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+    if args.kernel == "prefill":
+        return _prefill_only(args, uq, w, cache, bt, sl, dev)
+    if args.kernel == "cascade":
+        return _cascade_only(args, uq, w, cache, bt, sl, dev)
     q = w.q(0, device=dev)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
     wsp = uq.workspace(w.B, w.Hq, w.Hkv, w.D, dev)
@@ -547,6 +555,86 @@ def run_decode_only(args):
     print(json.dumps(line), flush=True)
 
 
+def _prefill_only(args, uq, w, cache, bt, sl, dev):
+    """Chunked-prefill attention on a filled cache: the last --chunk tokens of
+    every sequence attend causally to the whole sequence."""
+    n = min(args.chunk, min(w.seq_lens))
+    T = w.B * n
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    q = torch.randn((T, w.Hq, w.D), generator=g, device=dev).to(torch.bfloat16)
+    cu = torch.arange(0, T + 1, n, dtype=torch.int32, device=dev)
+    wsp = torch.empty(max(16, uq.uq_prefill_workspace_bytes(T, w.B, w.Hq, w.Hkv, w.D, bt.shape[1] * w.ps)),
+                      dtype=torch.uint8, device=dev)
+    out = torch.empty((T, w.Hq, w.D), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        uq.uq_prefill_attention(q, cu, cache, bt, sl, out=out, workspace=wsp)
+    torch.cuda.synchronize()
+    t0, t1 = _event_pair()
+    stream = torch.cuda.current_stream()
+    t0.record(stream)
+    for _ in range(args.steps):
+        uq.uq_prefill_attention(q, cu, cache, bt, sl, out=out, workspace=wsp)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert uq.uq_check_device_status() == 0
+    dt = t0.elapsed_time(t1) * 1e-3 / args.steps
+    keys = w.Hq * sum(L - n + i + 1 for L in w.seq_lens for i in range(n))
+    flops = 4.0 * w.D * keys
+    peak = _tensor_peak()
+    line = {"metric": "chunked-prefill attention TFLOP/s", "value": flops / dt / 1e12, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "dtype": "e2m1/ue8m0 cache, f16 tcgen05 operands", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "chunk": n,
+                       "tokens": sum(w.seq_lens)},
+            "tensor_peak_TFLOP_per_s": peak, "frac_of_tensor_peak": flops / dt / 1e12 / peak,
+            "gpu_launches": 4 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
+def _cascade_only(args, uq, w, cache, bt, sl, dev):
+    """Cascade decode: all sequences form one group over the workload's shared
+    prefix; the plain decode of the same step is timed beside it."""
+    q = w.q(0, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    cu = torch.tensor([0, w.B], dtype=torch.int32, device=dev)
+    pre = torch.tensor([w.shared_prefix], dtype=torch.int32, device=dev)
+    wsc = torch.empty(uq.uq_cascade_workspace_bytes(w.B, 1, w.Hq, w.Hkv, w.D, w.shared_prefix), dtype=torch.uint8,
+                      device=dev)
+    wsp = uq.workspace(w.B, w.Hq, w.Hkv, w.D, dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(f):
+        for _ in range(args.warmup):
+            f()
+        torch.cuda.synchronize()
+        t0, t1 = _event_pair()
+        t0.record(stream)
+        for _ in range(args.steps):
+            f()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        assert uq.uq_check_device_status() == 0
+        return t0.elapsed_time(t1) * 1e-3 / args.steps
+
+    dc = timed(lambda: uq.uq_cascade_decode_attention(q, cache, bt, sl, cu, pre, w.shared_prefix,
+                                                      min_rows=args.min_rows, out=out, workspace=wsc))
+    dp = timed(lambda: uq.uq_decode_attention(q, cache, bt, sl, out=out, workspace=wsp))
+    logical = sum(w.seq_lens) * w.Hkv * FP4_BYTES_PER_TOKEN_HEAD
+    unique = (sum(w.seq_lens) - (w.B - 1) * w.shared_prefix) * w.Hkv * FP4_BYTES_PER_TOKEN_HEAD
+    hbm, kind = _peaks()
+    line = {"metric": "cascade decode tokens/s (one attention layer)", "value": w.B / dc, "unit": "decode tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dc * 1e3,
+            "higher_is_better": True, "dtype": "e2m1/ue8m0 cache", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "tokens": sum(w.seq_lens),
+                       "shared_prefix": w.shared_prefix, "min_rows": args.min_rows},
+            "plain_decode_ms": dp * 1e3, "speedup_vs_plain_decode": dp / dc,
+            "kv_GB_per_s_unique": unique / dc / 1e9, "kv_GB_per_s_logical": logical / dc / 1e9,
+            "frac_of_peak_unique": unique / dc / 1e9 / hbm, "peak": hbm, "peak_kind": kind,
+            "gpu_launches": 5 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,11 +645,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="append64k",
                     choices=["append64k", "tiny", "gqa8k", "mixed", "prefix128k"])
+    ap.add_argument("--kernel", default="decode", choices=["decode", "prefill", "cascade"],
+                    help="with a workload other than append64k: what each step runs")
+    ap.add_argument("--chunk", type=int, default=16, help="--kernel prefill: query tokens per sequence")
+    ap.add_argument("--min-rows", type=int, default=0, help="--kernel cascade: min_rows of the cascade call")
+    ap.add_argument("--batch", type=int, default=0, help="with a workload other than append64k: override B")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload != "append64k":
+    elif args.workload != "append64k" or args.kernel != "decode":
         run_decode_only(args)
     else:
         run_uq(args)

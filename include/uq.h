@@ -273,6 +273,44 @@ uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q
                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Cascade (shared-prefix) decode over an FP4 cache.  Agent sessions reuse one
+ * long prefix across many sequences and turns ([UQ-review] §1); sequences that
+ * reference the same prefix pages can read and convert them once for all.
+ * The result equals uq_decode_attention on the same arguments (up to the
+ * order of fp32 additions) whenever the promise below holds.
+ * cu_seqs     : device int32 [num_groups + 1], non-decreasing, cu_seqs[0] = 0,
+ *               cu_seqs[num_groups] <= batch: group g is sequences
+ *               cu_seqs[g] .. cu_seqs[g+1]-1; later sequences belong to no group.
+ * prefix_lens : device int32 [num_groups].  PROMISE: keys 0 .. prefix_lens[g]-1
+ *               of every sequence of group g sit on the same pages (the block
+ *               table rows agree there).  The pages are read from the row of the
+ *               group's first sequence.  prefix_lens[g] <= seq_lens[b] for each b
+ *               of the group (a violation is recorded as UQ_ERR_DEVICE_BOUNDS).
+ * max_prefix_len : host bound on prefix_lens (sizes the work split; larger
+ *               prefixes are cut to it, the rest going to the per-sequence part).
+ * min_rows    : a group is attended once only if it has at least min_rows
+ *               query rows (sequences x num_q_heads / num_kv_heads); smaller
+ *               groups run as a plain decode.  The shared-prefix kernel
+ *               (tensor-core tiles of 128 query rows) is faster than the decode
+ *               from about 64 rows.
+ * Work split: group g's first S_g = floor(min(prefix_lens[g], max_prefix_len,
+ * max_pages_per_seq * page_size) / 16) * 16 keys go to the shared-prefix kernel
+ * (all the group's queries at once); keys S_g .. seq_lens[b]-1 of each sequence
+ * to the decode; a log-sum-exp merge combines both, then rotates back.
+ * Other arguments as uq_decode_attention; workspace at least
+ * uq_cascade_workspace_bytes(batch, num_groups, num_q_heads, num_kv_heads,
+ * head_dim, max_prefix_len).  FP4 caches, head_dim 64 or 128.
+ */
+size_t uq_cascade_workspace_bytes(int32_t batch, int32_t num_groups, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_prefix_len);
+uq_status uq_cascade_decode_attention(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                      int32_t num_q_heads, const int32_t* cu_seqs, const int32_t* prefix_lens,
+                                      int32_t num_groups, int32_t max_prefix_len, int32_t min_rows,
+                                      float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
+/*
  * The TQ4 codebook ([TQ-guide] "랜덤 회전과 Beta 분포", "Lloyd-Max 스칼라 양자화
  * (Q_mse)"): the Lloyd-Max quantiser with 2^bits levels of one coordinate of
  * a uniformly random unit vector in R^head_dim, whose density is

@@ -105,3 +105,33 @@ def test_workspace_size_is_positive_and_monotone():
     b = uq.uq_decode_workspace_bytes(64, 64, 8, 128)
     assert 0 < a < b
     assert uq.uq_decode_workspace_bytes(8, 12, 8, 128) == 0
+
+
+def _cascade(struct, q=0x200000, bt=0x300000, sl=0x300000, B=2, hq=8, cu=0x600000, pre=0x600100, ng=1,
+             max_prefix=4096, min_rows=0, out=0x400000, ws=0x500000, wsb=1 << 30):
+    return uq._lib.uq_cascade_decode_attention(q, C.byref(struct), bt, 4, sl, B, hq, cu, pre, ng, max_prefix,
+                                               min_rows, 0.0, out, ws, wsb, None)
+
+
+def test_cascade_argument_validation_without_a_device():
+    E = {v: k for k, v in uq.STATUS_NAMES.items()}
+    assert _cascade(_struct(uq.FP8_E4M3)) == E["UQ_ERR_UNSUPPORTED"]
+    assert _cascade(_struct(d=256)) == E["UQ_ERR_UNSUPPORTED"]
+    assert _cascade(_struct(), ng=-1) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), min_rows=-3) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), max_prefix=-1) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), cu=None) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), pre=None) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), B=0) == 0  # no-op
+    assert _cascade(_struct(), q=None) == E["UQ_ERR_INVALID_ARG"]
+    assert _cascade(_struct(), out=0x400008) == E["UQ_ERR_ALIGNMENT"]
+    assert _cascade(_struct(), wsb=64) == E["UQ_ERR_WORKSPACE"]
+
+
+def test_cascade_workspace_covers_the_decode_workspace():
+    dec = uq.uq_decode_workspace_bytes(4, 64, 8, 128)
+    a = uq.uq_cascade_workspace_bytes(4, 1, 64, 8, 128, 98304)
+    b = uq.uq_cascade_workspace_bytes(4, 0, 64, 8, 128, 98304)
+    assert a > dec and b >= dec
+    assert uq.uq_cascade_workspace_bytes(4, 1, 64, 8, 256, 98304) == 0
+    assert uq.uq_cascade_workspace_bytes(4, -1, 64, 8, 128, 98304) == 0

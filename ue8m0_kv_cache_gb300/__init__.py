@@ -54,6 +54,9 @@ _sig = {
     "uq_tq_codebook": (C.c_int, [_i32, _i32, _vp, _vp]),
     "uq_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "uq_prefill_attention": (C.c_int, [_vp, _vp, _i32, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_cascade_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "uq_cascade_decode_attention": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _f32,
+                                              _vp, _vp, _sz, _vp]),
     "uq_decode_attention_noalloc": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp]),
     "uq_decode_attention_append": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
                                              _vp, _sz, _vp]),
@@ -268,6 +271,39 @@ def uq_prefill_attention(q, cu_q, cache, block_table, seq_lens, out=None, worksp
                                      block_table.shape[1], _ptr(seq_lens), B, Hq, float(sm_scale), _ptr(out),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)), "uq_prefill_attention")
+    return out
+
+
+def uq_cascade_workspace_bytes(batch: int, num_groups: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               max_prefix_len: int) -> int:
+    return int(_lib.uq_cascade_workspace_bytes(batch, num_groups, num_q_heads, num_kv_heads, head_dim,
+                                               max_prefix_len))
+
+
+def uq_cascade_decode_attention(q, cache, block_table, seq_lens, cu_seqs, prefix_lens, max_prefix_len, min_rows=64,
+                                out=None, workspace=None, sm_scale=0.0, stream=None):
+    """Cascade decode: q [B][Hq][D] bf16; group g = sequences cu_seqs[g]..cu_seqs[g+1]-1 (int32 [G+1]) whose first
+    prefix_lens[g] keys (int32 [G]) are the same pages; returns fp32 [B][Hq][D], equal to uq_decode_attention."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(cu_seqs, torch.int32, "cu_seqs")
+    _need(prefix_lens, torch.int32, "prefix_lens")
+    B, Hq, D = q.shape
+    ng = prefix_lens.numel()
+    if D != cache.head_dim or seq_lens.numel() != B or block_table.shape[0] != B or cu_seqs.numel() != ng + 1:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    if workspace is None:
+        n = uq_cascade_workspace_bytes(B, ng, Hq, cache.num_kv_heads, D, max_prefix_len)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.uq_cascade_decode_attention(_ptr(q), C.byref(cache.struct), _ptr(block_table), block_table.shape[1],
+                                            _ptr(seq_lens), B, Hq, _ptr(cu_seqs), _ptr(prefix_lens), ng,
+                                            int(max_prefix_len), int(min_rows), float(sm_scale), _ptr(out),
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            _stream(stream)), "uq_cascade_decode_attention")
     return out
 
 

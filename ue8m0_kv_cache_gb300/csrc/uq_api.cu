@@ -1,6 +1,7 @@
 // uq_api.cu -- the extern "C" entry points of libuq.so (declared in
 // include/uq.h): argument validation, dispatch to the kernels, the device
 // status word, and the host-side sign generator of the rotation.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -245,6 +246,60 @@ uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q
   uqh::PrefillArgs a{q, cu_q, num_q_tokens, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads,
                      sm_scale, out, workspace, workspace_bytes};
   return uqh::launch_prefill(a, stream);
+}
+
+size_t uq_cascade_workspace_bytes(int32_t batch, int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_prefix_len) {
+  const size_t dec = uq_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
+  if (dec == 0 || num_groups < 0 || max_prefix_len < 0 || (head_dim != 64 && head_dim != 128)) return 0;
+  const size_t pre = num_groups > 0 ? uqh::cascade_prefix_workspace_bytes(batch, num_groups, num_q_heads,
+                                                                         num_kv_heads, head_dim, max_prefix_len)
+                                    : 0;
+  return ((dec + 255) & ~size_t(255)) + pre;
+}
+
+uq_status uq_cascade_decode_attention(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                                      int32_t num_q_heads, const int32_t* cu_seqs, const int32_t* prefix_lens,
+                                      int32_t num_groups, int32_t max_prefix_len, int32_t min_rows, float sm_scale,
+                                      float* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  uq_status st = check_cache(cache);
+  if (st != UQ_OK) return st;
+  if (cache->dtype != UQ_FP4_UE8M0) return UQ_ERR_UNSUPPORTED;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return UQ_ERR_UNSUPPORTED;
+  if (num_groups < 0 || max_prefix_len < 0 || min_rows < 0) return UQ_ERR_INVALID_ARG;
+  if (num_groups > 0 && (!cu_seqs || !prefix_lens)) return UQ_ERR_INVALID_ARG;
+  if (batch <= 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
+    return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                         workspace, workspace_bytes, stream, UQ_FP4_UE8M0);
+  const size_t dec = uq_decode_workspace_bytes(batch, num_q_heads, cache->num_kv_heads, cache->head_dim);
+  const size_t dec_al = (dec + 255) & ~size_t(255);
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int64_t cap = std::min<int64_t>(static_cast<int64_t>(max_pages_per_seq) * cache->page_size, max_prefix_len);
+  // No group can reach min_rows, or nothing to share: a plain decode.
+  if (num_groups == 0 || cap < 16 || static_cast<int64_t>(batch) * G < min_rows)
+    return decode_common(q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                         workspace, workspace_bytes, stream, UQ_FP4_UE8M0);
+  if (!q || !block_table || !seq_lens || !out || !workspace) return UQ_ERR_INVALID_ARG;
+  if (max_pages_per_seq < 1 || batch > 4096) return UQ_ERR_INVALID_ARG;
+  if ((int64_t)max_pages_per_seq * cache->page_size >= (int64_t(1) << 31)) return UQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return UQ_ERR_ALIGNMENT;
+  if (workspace_bytes < dec_al) return UQ_ERR_WORKSPACE;
+  uqh::CascadeGroups cg;
+  cg.cu = cu_seqs;
+  cg.prefix = prefix_lens;
+  cg.groups = num_groups;
+  cg.min_rows = min_rows;
+  cg.cap = static_cast<int32_t>(cap);
+  uqh::PrefixPartials px;
+  st = uqh::launch_cascade_prefix(q, cache, block_table, max_pages_per_seq, batch, num_q_heads, cg, sm_scale,
+                                  static_cast<uint8_t*>(workspace) + dec_al, workspace_bytes - dec_al, &px, stream);
+  if (st != UQ_OK) return st;
+  uqh::DecodeArgs a{q, cache, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                    workspace, dec};
+  a.casc = cg;
+  a.px = px;
+  return uqh::launch_decode(a, stream);
 }
 
 uq_status uq_check_device_status(cudaStream_t stream) {

@@ -114,6 +114,10 @@ struct DecParams {
   uint8_t* wks;
   uint8_t* wvc;
   uint8_t* wvs;
+  // Cascade (casc_cu == nullptr: none): the decode skips each group's shared keys.
+  const int32_t* casc_cu;
+  const int32_t* casc_prefix;
+  int casc_groups, casc_min_rows, casc_cap;
 };
 
 // Contiguous range [lo, hi) of the U units that block c of C handles.
@@ -141,6 +145,16 @@ __device__ __forceinline__ float scale_of(uint32_t w) {
 // Non-zero if any byte of w is 0xFF (a non-finite group).
 __device__ __forceinline__ uint32_t has_ff(uint32_t w) {
   return ((w & 0x7F7F7F7Fu) + 0x01010101u) & w & 0x80808080u;
+}
+
+// Keys of sequence b attended by the shared-prefix kernel of a cascade decode
+// (a multiple of 16; 0 without cascade).
+template <typename P>
+__device__ __forceinline__ int casc_skip(const P& p, int b) {
+  if (p.casc_cu == nullptr) return 0;
+  const int g = casc_group(p.casc_cu, p.casc_groups, b);
+  if (g < 0) return 0;
+  return casc_shared_keys(p.casc_cu[g + 1] - p.casc_cu[g], p.G, p.casc_prefix[g], p.casc_min_rows, p.casc_cap);
 }
 
 __device__ __forceinline__ int clamp_len(const DecParams& p, int b) {
@@ -866,7 +880,12 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
     if (lane == 0) pre[0] = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int b = b0 + lane;
-      int x = b < p.B ? (clamp_len(p, b) + kChunk - 1) / kChunk : 0;
+      int x = 0;
+      if (b < p.B) {
+        const int L = clamp_len(p, b), skip = casc_skip(p, b);
+        if (skip > L) record_error(p.status, kErrBounds);  // a shared prefix longer than the sequence
+        x = max(0, (L + kChunk - 1) / kChunk - skip / kChunk);
+      }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFull, x, o);
@@ -909,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
     const int kvh = pl / p.nhb, hblk = pl - kvh * p.nhb;
     const int pair = b * pps + pl;
     const int L = clamp_len(p, b);
+    const int ub = casc_skip(p, b) / kChunk;  // first unit of the sequence that this decode takes
 
     // Query fragments (once per segment, outside the unit loop).
     uint32_t qb[C::NMMA][2];
@@ -978,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
     auto page_of_lane = [&](int i) {
       int page = 0;
       if (i < nw) {
-        page = bt_row[((j0 + warp + i * kWarps) * kChunk) >> p.ps_log2];
+        page = bt_row[((ub + j0 + warp + i * kWarps) * kChunk) >> p.ps_log2];
         if (page < 0 || page >= p.num_pages) {
           record_error(p.status, kErrBounds);
           page = 0;
@@ -997,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
     const uint32_t cp_off = lane == 1 ? C::KBYTES : 0;
     const uint32_t ring_u32 = smem_u32(myring), bars_u32 = smem_u32(mybars);
     auto issue = [&](int i, int slot, int page) {
-      const int tok0 = (j0 + warp + i * kWarps) * kChunk;
+      const int tok0 = (ub + j0 + warp + i * kWarps) * kChunk;
       const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
       const uint32_t bar = bars_u32 + 8u * slot;
       if (lane == 0)
@@ -1061,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
         __syncwarp();
       }
       const uint8_t* st0 = myring + (it % C::NST) * C::STAGE;
-      const int nvalid = L - (j0 + warp + (i + nu - 1) * kWarps) * kChunk;  // of the last unit taken
+      const int nvalid = L - (ub + j0 + warp + (i + nu - 1) * kWarps) * kChunk;  // of the last unit taken
       if (KIND == kFP4) {
         if (nu == 2) {
           const uint8_t* const sts[2] = {st0, myring + ((it + 1) % C::NST) * C::STAGE};
@@ -1188,6 +1208,16 @@ struct MergeParams {
   float* out;
   unsigned int* status;
   uqh::SignMasks sign;
+  // Cascade (casc_cu == nullptr: none): the shared-prefix partials of each
+  // group's sequences, [items][px_rows] (m, l) and O, merged in as well.
+  const int32_t* casc_cu;
+  const int32_t* casc_prefix;
+  int casc_groups, casc_min_rows, casc_cap;
+  const float* px_ml;
+  const float* px_o;
+  const int32_t* px_item_pre;
+  int px_splits, px_rows;
+  int64_t px_max_items;
 };
 
 template <int KIND, int D>
@@ -1203,14 +1233,30 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
   float o[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-  if (L > 0) {
+  // cascade: the keys the shared-prefix kernel took, and where its partials of this row are
+  const int skip = casc_skip(p, b);
+  const bool dec = L > skip;  // the decode took keys skip .. L - 1
+  int64_t pitem = -1;
+  int prr = 0;
+  if (skip > 0 && p.px_item_pre[p.casc_groups] <= p.px_max_items) {
+    const int g = casc_group(p.casc_cu, p.casc_groups, b);
+    const int n = p.casc_cu[g + 1] - p.casc_cu[g], i = b - p.casc_cu[g];
+    const int kvh = h / p.G, rowi = i * p.G + (h - kvh * p.G), rt = rowi / p.px_rows;
+    prr = rowi - rt * p.px_rows;
+    pitem = p.px_item_pre[g] + (static_cast<int64_t>(kvh) * ((n * p.G + p.px_rows - 1) / p.px_rows) + rt) * p.px_splits;
+  }
+  if (dec || pitem >= 0) {
     const int kvh = h / p.G, hl = h - kvh * p.G, hb = hl / kHB, hh = hl - hb * kHB;
     const int pair = (b * p.Hkv + kvh) * p.nhb + hb;
-    int first = p.ws_info[2 * pair], last = p.ws_info[2 * pair + 1];
-    if (first < 0 || last < first || last >= p.num_ctas) {  // never written: a decode block gave up
-      record_error(p.status, kErrTimeout);
-      first = 1;
-      last = 0;
+    int first = 1, last = 0;
+    if (dec) {
+      first = p.ws_info[2 * pair];
+      last = p.ws_info[2 * pair + 1];
+      if (first < 0 || last < first || last >= p.num_ctas) {  // never written: a decode block gave up
+        record_error(p.status, kErrTimeout);
+        first = 1;
+        last = 0;
+      }
     }
     const int64_t U = *p.ws_units;
     // The partials of this row are slots first..last (those with an empty
@@ -1223,6 +1269,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
       if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
       if (lo < hi) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
     }
+    // The decode's partials carry p * 2^kPShift against their maximum, the shared-prefix
+    // kernel's plain p: its maxima enter the merge raised by kPShift.
+    if (pitem >= 0)
+      for (int s = lane; s < p.px_splits; s += 32)
+        Ms = fmaxf(Ms, p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift);
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
     float Ls = 0.f;
@@ -1261,6 +1312,32 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
           const VecF<EPL> v = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + pair) * kHB + hh) * D + lane * EPL);
 #pragma unroll
           for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
+        }
+      }
+    }
+    if (pitem >= 0) {  // the shared-prefix splits; an empty split (m = -inf) wrote no O row
+      for (int s0 = 0; s0 < p.px_splits; s0 += 32) {
+        const int s = s0 + lane;
+        float w = 0.f;
+        bool live = false;
+        if (s < p.px_splits) {
+          const float m = p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift;
+          live = m != -INFINITY;
+          if (live) {
+            w = ex2(m - Ms);
+            Ls += w * p.px_ml[((pitem + s) * p.px_rows + prr) * 2 + 1];
+          }
+        }
+        const unsigned mask = __ballot_sync(kFull, live);
+        const int cnt = min(32, p.px_splits - s0);
+        for (int j = 0; j < cnt; ++j) {
+          const float wj = __shfl_sync(kFull, w, j);
+          if ((mask >> j) & 1u) {
+            const VecF<EPL> v =
+                *reinterpret_cast<const VecF<EPL>*>(p.px_o + ((pitem + s0 + j) * p.px_rows + prr) * D + lane * EPL);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
+          }
         }
       }
     }
@@ -1405,6 +1482,11 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.wks = static_cast<uint8_t*>(c.k_scales);
   p.wvc = static_cast<uint8_t*>(c.v_codes);
   p.wvs = static_cast<uint8_t*>(c.v_scales);
+  p.casc_cu = a.casc.cu;
+  p.casc_prefix = a.casc.prefix;
+  p.casc_groups = a.casc.groups;
+  p.casc_min_rows = a.casc.min_rows;
+  p.casc_cap = a.casc.cap;
   if (uqh::launch_pdl(kern, (unsigned)grid, kThreads, smem, s, p) != cudaSuccess) return UQ_ERR_CUDA;
 
   MergeParams mp;
@@ -1423,6 +1505,17 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   mp.out = a.out;
   mp.status = p.status;
   mp.sign = p.sign;
+  mp.casc_cu = a.casc.cu;
+  mp.casc_prefix = a.casc.prefix;
+  mp.casc_groups = a.casc.groups;
+  mp.casc_min_rows = a.casc.min_rows;
+  mp.casc_cap = a.casc.cap;
+  mp.px_ml = a.px.ml;
+  mp.px_o = a.px.o;
+  mp.px_item_pre = a.px.item_pre;
+  mp.px_splits = a.px.splits;
+  mp.px_rows = a.px.rows;
+  mp.px_max_items = a.px.max_items;
   const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads;
   return uqh::cuda_status(uqh::launch_pdl(merge_kernel<KIND, D>, (unsigned)((rows + 3) / 4), 128, 0, s, mp));
 }

@@ -279,4 +279,26 @@ constexpr unsigned kErrTimeout = 6u;  // UQ_ERR_DEVICE_TIMEOUT
 constexpr unsigned kErrBounds = 7u;   // UQ_ERR_DEVICE_BOUNDS
 constexpr long long kWaitBudget = 4000000000ll;  // ~2 s at 2 GHz
 
+// Cascade decode.  Group g holds the consecutive sequences cu[g] .. cu[g+1]-1,
+// whose first prefix[g] keys are the same cache pages.  A group with at least
+// min_rows query rows (sequences x query heads per kv head) has its first
+// S_g = floor(min(prefix, cap) / 16) * 16 keys attended by the shared-prefix
+// kernel, for all its sequences at once; the decode takes keys S_g .. L_b - 1
+// of every sequence (from 16-token unit S_g / 16).  Other groups: S_g = 0.
+__device__ __forceinline__ int casc_shared_keys(int nseq, int G, int prefix, int min_rows, int cap) {
+  if (nseq <= 0 || prefix <= 0 || static_cast<long long>(nseq) * G < min_rows) return 0;
+  return (prefix < cap ? prefix : cap) & ~15;
+}
+
+// The group g with cu[g] <= b < cu[g + 1], or -1 (cu non-decreasing over ng + 1 entries).
+__device__ __forceinline__ int casc_group(const int32_t* cu, int ng, int b) {
+  if (cu == nullptr || ng <= 0 || b < cu[0] || b >= cu[ng]) return -1;
+  int lo = 0, hi = ng;  // cu[lo] <= b < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= b) lo = mid; else hi = mid;
+  }
+  return b < cu[lo + 1] ? lo : -1;
+}
+
 }  // namespace uqd

@@ -80,6 +80,25 @@ uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes,
                                cudaStream_t s);
 uq_status launch_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 
+// Cascade decode: groups of consecutive sequences that share a key prefix
+// (see casc_shared_keys in uq_device.cuh for the split between the kernels).
+struct CascadeGroups {
+  const int32_t* cu = nullptr;      // [groups + 1] first sequence of each group
+  const int32_t* prefix = nullptr;  // [groups] shared keys of each group
+  int32_t groups = 0;
+  int32_t min_rows = 0;             // query rows a group needs to use the shared-prefix kernel
+  int32_t cap = 0;                  // bound on the shared keys: min(max_pages * page_size, max_prefix_len)
+};
+// Partials (m, l, O) of the shared-prefix kernel, read by the decode merge.
+struct PrefixPartials {
+  const float* ml = nullptr;          // [items][rows][2]
+  const float* o = nullptr;           // [items][rows][D]
+  const int32_t* item_pre = nullptr;  // [groups + 1] work items before each group
+  int32_t splits = 0;
+  int32_t rows = 0;                   // query rows per work item
+  int64_t max_items = 0;
+};
+
 // Decode launchers (uq_decode.cu).
 struct DecodeArgs {
   const void* q;
@@ -98,6 +117,10 @@ struct DecodeArgs {
   const void* v_new = nullptr;
   const int64_t* new_slots = nullptr;
   int new_f32 = 0;
+  // cascade (FP4; casc.cu == nullptr: none): keys below each group's shared
+  // prefix are skipped here and their partials px merged in
+  CascadeGroups casc;
+  PrefixPartials px;
 };
 size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas);
 int decode_max_ctas();
@@ -123,5 +146,11 @@ struct PrefillArgs {
 };
 size_t prefill_workspace_bytes(int T, int B, int hq, int hkv, int d, int max_keys);
 uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// Shared-prefix part of a cascade decode: the query of every sequence
+// (bf16 [batch][Hq][D]) against its group's first S_g keys, as partials.
+size_t cascade_prefix_workspace_bytes(int batch, int groups, int hq, int hkv, int d, int max_keys);
+uq_status launch_cascade_prefix(const void* q, const uq_cache* cache, const int32_t* block_table,
+                                int32_t max_pages, int32_t batch, int32_t num_q_heads, const CascadeGroups& cg,
+                                float sm_scale, void* ws, size_t ws_bytes, PrefixPartials* out, cudaStream_t s);
 
 }  // namespace uqh

@@ -45,8 +45,8 @@ constexpr int kPThreads = 128;  // 4 warps: one query row per thread
 
 struct PrefillParams {
   const uint8_t* qbytes;     // rotated E4M3 query, [T][Hq][D]
-  const int32_t* cu_q;       // [B + 1] first query token of each sequence
-  const int32_t* seq_lens;   // [B] keys of each sequence after the chunk
+  const int32_t* cu_q;       // [B + 1] first query token of each sequence (cascade: of each group)
+  const int32_t* seq_lens;   // [B] keys of each sequence after the chunk (cascade: shared prefix of each group)
   const int32_t* block_table;
   int max_pages;
   const uint8_t* kc;
@@ -57,11 +57,16 @@ struct PrefillParams {
   int splits;                // key splits per row tile
   int kchunk;                // keys per split (multiple of the key tile)
   float sl2e;                // softmax scale * log2(e)
-  float* ws_ml;              // partials: [items][64 rows][2]
-  float* ws_o;               // partials: [items][64 rows][D]
+  float* ws_ml;              // partials: [items][128 rows][2]
+  float* ws_o;               // partials: [items][128 rows][D]
   int32_t* item_pre;         // [B + 1] prefix sums of work items per sequence
   int64_t max_items;
   unsigned int* status;
+  // Cascade mode: "sequence" b is group b, its queries are the decode queries of
+  // sequences cu_q[b] .. cu_q[b+1]-1 (T = batch), its keys the group's shared
+  // prefix from the block-table row of its first sequence, attended without a
+  // causal mask.
+  int cascade, min_rows, casc_cap;
 };
 
 // 2^e as fp32 for e in [-149, 127], 0 below.
@@ -80,8 +85,9 @@ namespace {
 
 // Work items: for every sequence b, kv head, row tile and key split one item,
 // in that order; item_pre[b] counts the items of sequences before b.
+// Cascade mode (prefix != nullptr): a group whose shared keys are 0 has no items.
 __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, int splits, int rows,
-                                    int32_t* item_pre) {
+                                    const int32_t* prefix, int min_rows, int cap, int32_t* item_pre) {
   const int lane = threadIdx.x;
   int run = 0;
   if (lane == 0) item_pre[0] = 0;
@@ -90,7 +96,8 @@ __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, 
     int x = 0;
     if (b < B) {
       const int n = max(0, cu_q[b + 1] - cu_q[b]);
-      x = Hkv * row_tiles(n, G, rows) * splits;
+      const bool live = prefix == nullptr || casc_shared_keys(n, G, prefix[b], min_rows, cap) > 0;
+      x = live ? Hkv * row_tiles(n, G, rows) * splits : 0;
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -262,13 +269,19 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     const int q0 = p.cu_q[b], n_plan = max(0, p.cu_q[b + 1] - q0);
     int L = p.seq_lens[b];
     int n = n_plan;
-    if (L < 0 || L > cap || n > L || q0 < 0 || q0 + n > p.T) {
+    if (p.cascade) {
+      L = casc_shared_keys(n_plan, p.G, L, p.min_rows, p.casc_cap);
+      if (q0 < 0 || q0 + n > p.T) {
+        if (tid == 0) record_error(p.status, kErrBounds);
+        L = 0;  // no keys: the item writes empty partials below
+      }
+    } else if (L < 0 || L > cap || n > L || q0 < 0 || q0 + n > p.T) {
       if (tid == 0) record_error(p.status, kErrBounds);
       L = L < 0 ? 0 : (L > cap ? cap : L);
       n = n > L ? L : n;
       if (q0 < 0 || q0 + n > p.T) n = 0;
     }
-    const int ctx = L - n;
+    const int ctx = p.cascade ? 0 : L - n;
     const int tiles_b = row_tiles(n_plan, p.G, kTRows);
     const int64_t local = item - p.item_pre[b];
     const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * p.splits));
@@ -276,11 +289,11 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     const int rtile = rem / p.splits, split = rem - rtile * p.splits;
     const int row0 = rtile * kTRows, nrows = n * p.G;
     const int last_row = min(row0 + kTRows, nrows) - 1;
-    const int pos_max = ctx + last_row / p.G;
+    const int pos_max = p.cascade ? L - 1 : ctx + last_row / p.G;
     const int k_lo = split * p.kchunk;
     const int k_hi = min(k_lo + p.kchunk, pos_max + 1);
     const int my_row = row0 + tid;
-    const int pos = my_row < nrows ? ctx + my_row / p.G : -1;
+    const int pos = my_row < nrows ? (p.cascade ? L - 1 : ctx + my_row / p.G) : -1;
     float* ml_out = p.ws_ml + item * (kTRows * 2);
     float* o_out = p.ws_o + item * (static_cast<int64_t>(kTRows) * D);
     if (k_lo >= k_hi) {
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       continue;
     }
     const int ntiles = (k_hi - k_lo + kTKT - 1) / kTKT;
-    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_pages;
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(p.cascade ? q0 : b) * p.max_pages;
     const int lp_last = (L - 1) >> p.ps_log2;
 
     // warp 0, one lane per bulk copy of a tile: the page of the lane's copy
@@ -718,67 +731,90 @@ PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int
 
 constexpr int kItemRows = kTRows;  // query rows per work item
 
+// Kernel attributes, once per device; the CTAs per SM.
 template <int D>
-uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
-  const uq_cache& c = *a.cache;
-  const uqh::DevInfo& di = uqh::dev_info();
-  const int G = a.num_q_heads / c.num_kv_heads;
-  const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D,
-                                      a.max_pages * c.page_size, di.sms, kItemRows);
-  if (a.ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
-  auto kern = prefill_tc_kernel<D>;
-  const int smem = TC<D>::SMEM;
+int prefill_ctas_per_sm() {
   static int cfg_dev = -1;
-  static int per_sm = 0;
+  const uqh::DevInfo& di = uqh::dev_info();
   if (cfg_dev != di.device) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return UQ_ERR_CUDA;
-    // Two CTAs per SM: their shared memory (2 x 93 KB), registers (2 x 128 x 255)
-    // and tensor-memory columns (2 x 256 of 512) fit, and each CTA's serial phases
-    // (convert, QK^T, softmax, P.V) overlap the other's.  The occupancy query
-    // reports one for this kernel; measured, two are resident.
-    per_sm = 512 / kTCols;
+    if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC<D>::SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+            cudaSuccess)
+      return 0;
     cfg_dev = di.device;
   }
-  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  // Two CTAs per SM: their shared memory (2 x 93 KB), registers (2 x 128 x 255)
+  // and tensor-memory columns (2 x 256 of 512) fit, and each CTA's serial phases
+  // (convert, QK^T, softmax, P.V) overlap the other's.  The occupancy query
+  // reports one for this kernel; measured, two are resident.
+  return 512 / kTCols;
+}
+
+// Parameters common to prefill and the cascade prefix; the caller sets the rest.
+template <int D>
+PrefillParams base_params(const uq_cache& c, const int32_t* block_table, int max_pages, int B, int T, int hq,
+                          float sm_scale, const PrefillPlan& pl, uint8_t* ws) {
   PrefillParams p;
   p.qbytes = ws + pl.off_q;
-  p.cu_q = a.cu_q;
-  p.seq_lens = a.seq_lens;
-  p.block_table = a.block_table;
-  p.max_pages = a.max_pages;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
   p.kc = static_cast<const uint8_t*>(c.k_codes);
   p.ks = static_cast<const uint8_t*>(c.k_scales);
   p.vc = static_cast<const uint8_t*>(c.v_codes);
   p.vs = static_cast<const uint8_t*>(c.v_scales);
-  p.B = a.batch;
-  p.T = a.num_q_tokens;
-  p.Hq = a.num_q_heads;
+  p.B = B;
+  p.T = T;
+  p.Hq = hq;
   p.Hkv = c.num_kv_heads;
-  p.G = G;
+  p.G = hq / c.num_kv_heads;
   p.ps_log2 = uqh::ilog2(c.page_size);
   p.num_pages = c.num_pages;
   p.splits = pl.splits;
   p.kchunk = pl.kchunk;
-  const float sm = a.sm_scale > 0.f ? a.sm_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  const float sm = sm_scale > 0.f ? sm_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   p.sl2e = sm * 1.4426950408889634f;
   p.ws_ml = reinterpret_cast<float*>(ws + pl.off_ml);
   p.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.item_pre = reinterpret_cast<int32_t*>(ws + pl.off_pre);
   p.max_items = pl.max_items;
   p.status = uqh::status_word();
-  if (!p.status) return UQ_ERR_CUDA;
+  p.cascade = 0;
+  p.min_rows = 0;
+  p.casc_cap = 0;
+  return p;
+}
 
-  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.batch, G, c.num_kv_heads, pl.splits, kItemRows, p.item_pre);
+template <int D>
+uq_status launch_items(const PrefillParams& p, const PrefillPlan& pl, cudaStream_t s) {
+  const int per_sm = prefill_ctas_per_sm<D>();
+  if (per_sm < 1) return UQ_ERR_CUDA;
+  const int64_t grid = std::min<int64_t>(pl.max_items, static_cast<int64_t>(uqh::dev_info().sms) * per_sm);
+  return uqh::cuda_status(uqh::launch_pdl(prefill_tc_kernel<D>, static_cast<unsigned>(std::max<int64_t>(grid, 1)),
+                                          kPThreads, TC<D>::SMEM, s, p));
+}
+
+template <int D>
+uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
+  const uq_cache& c = *a.cache;
+  const int G = a.num_q_heads / c.num_kv_heads;
+  const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D,
+                                      a.max_pages * c.page_size, uqh::dev_info().sms, kItemRows);
+  if (a.ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  PrefillParams p = base_params<D>(c, a.block_table, a.max_pages, a.batch, a.num_q_tokens, a.num_q_heads,
+                                   a.sm_scale, pl, ws);
+  if (!p.status) return UQ_ERR_CUDA;
+  p.cu_q = a.cu_q;
+  p.seq_lens = a.seq_lens;
+  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.batch, G, c.num_kv_heads, pl.splits, kItemRows, nullptr, 0, 0,
+                                       p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
-  const uq_status st = uqh::launch_test_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
-                                                  c.rot_seed, ws + pl.off_q, s);
+  uq_status st = uqh::launch_test_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
+                                            c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
-  const int64_t grid = std::min<int64_t>(pl.max_items, static_cast<int64_t>(di.sms) * per_sm);
-  if (uqh::launch_pdl(kern, static_cast<unsigned>(std::max<int64_t>(grid, 1)), kPThreads, smem, s, p) !=
-      cudaSuccess)
-    return UQ_ERR_CUDA;
+  st = launch_items<D>(p, pl, s);
+  if (st != UQ_OK) return st;
   PrefillMergeParams mp;
   mp.ws_ml = p.ws_ml;
   mp.ws_o = p.ws_o;
@@ -800,6 +836,38 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
       uqh::launch_pdl(prefill_merge_kernel<D>, static_cast<unsigned>((rows + 3) / 4), 128, 0, s, mp));
 }
 
+template <int D>
+uq_status run_cascade_prefix(const void* q, const uq_cache& c, const int32_t* block_table, int max_pages, int batch,
+                             int hq, const uqh::CascadeGroups& cg, float sm_scale, void* ws_v, size_t ws_bytes,
+                             uqh::PrefixPartials* out, cudaStream_t s) {
+  const int G = hq / c.num_kv_heads;
+  const PrefillPlan pl = plan_prefill(batch, cg.groups, hq, c.num_kv_heads, D, cg.cap, uqh::dev_info().sms,
+                                      kItemRows);
+  if (ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(ws_v);
+  PrefillParams p = base_params<D>(c, block_table, max_pages, cg.groups, batch, hq, sm_scale, pl, ws);
+  if (!p.status) return UQ_ERR_CUDA;
+  p.cu_q = cg.cu;
+  p.seq_lens = cg.prefix;
+  p.cascade = 1;
+  p.min_rows = cg.min_rows;
+  p.casc_cap = cg.cap;
+  prefill_plan_kernel<<<1, 32, 0, s>>>(cg.cu, cg.groups, G, c.num_kv_heads, pl.splits, kItemRows, cg.prefix,
+                                       cg.min_rows, cg.cap, p.item_pre);
+  if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
+  uq_status st = uqh::launch_test_query_fp8(q, static_cast<int64_t>(batch) * hq, D, c.rot_seed, ws + pl.off_q, s);
+  if (st != UQ_OK) return st;
+  st = launch_items<D>(p, pl, s);
+  if (st != UQ_OK) return st;
+  out->ml = p.ws_ml;
+  out->o = p.ws_o;
+  out->item_pre = p.item_pre;
+  out->splits = pl.splits;
+  out->rows = kItemRows;
+  out->max_items = pl.max_items;
+  return UQ_OK;
+}
+
 }  // namespace
 
 namespace uqh {
@@ -810,6 +878,20 @@ size_t prefill_workspace_bytes(int T, int B, int hq, int hkv, int d, int max_key
 
 uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   return a.cache->head_dim == 128 ? run_prefill<128>(a, s) : run_prefill<64>(a, s);
+}
+
+size_t cascade_prefix_workspace_bytes(int batch, int groups, int hq, int hkv, int d, int max_keys) {
+  return plan_prefill(batch, groups, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows).total;
+}
+
+uq_status launch_cascade_prefix(const void* q, const uq_cache* cache, const int32_t* block_table, int32_t max_pages,
+                                int32_t batch, int32_t num_q_heads, const CascadeGroups& cg, float sm_scale, void* ws,
+                                size_t ws_bytes, PrefixPartials* out, cudaStream_t s) {
+  return cache->head_dim == 128
+             ? run_cascade_prefix<128>(q, *cache, block_table, max_pages, batch, num_q_heads, cg, sm_scale, ws,
+                                       ws_bytes, out, s)
+             : run_cascade_prefix<64>(q, *cache, block_table, max_pages, batch, num_q_heads, cg, sm_scale, ws,
+                                      ws_bytes, out, s);
 }
 
 }  // namespace uqh
