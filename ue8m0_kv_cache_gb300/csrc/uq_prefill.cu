@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     const int k_hi = min(k_lo + p.kchunk, pos_max + 1);
     const int my_row = row0 + tid;
     const int pos = my_row < nrows ? (p.cascade ? L - 1 : ctx + my_row / p.G) : -1;
+    const int pos_lo = p.cascade ? L - 1 : ctx + row0 / p.G;  // the smallest position of the item's rows
     float* ml_out = p.ws_ml + item * (kTRows * 2);
     float* o_out = p.ws_o + item * (static_cast<int64_t>(kTRows) * D);
     if (k_lo >= k_hi) {
@@ -470,11 +471,19 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
       }
       float mx = -INFINITY;
+      if (kbase + kTKT <= k_hi && kbase + kTKT - 1 <= pos_lo && pos >= 0) {  // every key visible to the row
 #pragma unroll
-      for (int k = 0; k < kTKT; ++k) {
-        const int key = kbase + k;
-        x[k] = (key <= pos && key < k_hi) ? x[k] * kfac[k] : -INFINITY;
-        mx = fmaxf(mx, x[k]);
+        for (int k = 0; k < kTKT; ++k) {
+          x[k] *= kfac[k];
+          mx = fmaxf(mx, x[k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kTKT; ++k) {
+          const int key = kbase + k;
+          x[k] = (key <= pos && key < k_hi) ? x[k] * kfac[k] : -INFINITY;
+          mx = fmaxf(mx, x[k]);
+        }
       }
       const bool need = mx > m + kTSlack || (m == -INFINITY && mx > -INFINITY);
       const bool fold = __syncthreads_or(need || !ok) != 0 || RVn != RV || win == kTWin;
