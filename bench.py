@@ -635,6 +635,74 @@ def _cascade_only(args, uq, w, cache, bt, sl, dev):
     print(json.dumps(line), flush=True)
 
 
+def run_layers(args):
+    """A decode step through every attention layer of an L-layer stack (B 8, Hkv 8, Hq 64, D 128, context
+    --ctx): each layer appends the step's token and decodes.  The policy stack keeps the first and last two
+    layers in BF16 and the rest in FP4; all-FP4 and all-FP8 stacks are timed beside it; steps replay one
+    captured CUDA graph per stack (eager timed too for the policy stack)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import ue8m0_kv_cache_gb300 as uq
+    import workloads
+    from ue8m0_kv_cache_gb300.policy import LayeredKVCache, LayerPolicy, layered_workspace
+    L = args.layers
+    w = workloads.make("gqa8k", B=B, Hkv=HKV, Hq=HQ, D=D, ps=PS, seq_lens=[args.ctx] * B, seed=1006,
+                       extra_tokens=args.steps + args.warmup + 16)
+    stacks = {"policy_bf16_boundary2": LayerPolicy(L, boundary=2),
+              "all_fp4": LayerPolicy(L, boundary=0),
+              "all_fp8": LayerPolicy(L, boundary=0, inner=uq.FP8_E4M3)}
+    caches = {k: LayeredKVCache(p, w.num_pages, HKV, PS, D, device=dev) for k, p in stacks.items()}
+    for b in range(B):  # every layer holds the same values (timing does not depend on them)
+        for t0 in range(0, args.ctx, 8192):
+            n = min(8192, args.ctx - t0)
+            k, v = w.kv(b, t0, n, device=dev)
+            sl_b = torch.from_numpy(w.slots(b, t0, n)).to(dev)
+            for lc in caches.values():
+                for l in range(L):
+                    lc.append(l, k, v, sl_b)
+    torch.cuda.synchronize()
+    bt = torch.from_numpy(w.block_table).to(dev)
+    seq = torch.full((B,), args.ctx + 1, dtype=torch.int32, device=dev)
+    slots = torch.from_numpy(np.array([w.slots(b, args.ctx, 1)[0] for b in range(B)])).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    q = [torch.randn((B, HQ, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    kn = [torch.randn((B, HKV, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    vn = [torch.randn((B, HKV, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    out = [torch.empty((B, HQ, D), dtype=torch.float32, device=dev) for _ in range(L)]
+    wsp = layered_workspace(B, HQ, HKV, D, dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(f):
+        for _ in range(args.warmup):
+            f()
+        torch.cuda.synchronize()
+        t0, t1 = _event_pair()
+        t0.record(stream)
+        for _ in range(args.steps):
+            f()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        assert uq.uq_check_device_status() == 0
+        return t0.elapsed_time(t1) * 1e-3 / args.steps
+
+    res = {}
+    pol = caches["policy_bf16_boundary2"]
+    res["policy_eager_ms"] = 1e3 * timed(lambda: pol.decode_step(q, kn, vn, slots, bt, seq, out, wsp))
+    for name, lc in caches.items():
+        lc.capture_step(q, kn, vn, slots, bt, seq, out, wsp)
+        res[name + "_graph_ms"] = 1e3 * timed(lc.replay)
+        res[name + "_cache_GB"] = lc.nbytes() / 1e9
+    dt = res["policy_bf16_boundary2_graph_ms"] * 1e-3
+    line = {"metric": "decode tokens/s through all attention layers", "value": B / dt, "unit": "decode tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "dtype": "bf16 boundary layers, e2m1/ue8m0 inner layers", "data": "synthetic",
+            "config": {"workload": "layers%d_ctx%d" % (L, args.ctx), "B": B, "Hkv": HKV, "Hq": HQ, "D": D,
+                       "layers": L, "context": args.ctx},
+            "stacks": res, "gpu_launches": args.steps * (2 * L + stacks["policy_bf16_boundary2"].count(uq.BF16))}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -645,15 +713,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="append64k",
                     choices=["append64k", "tiny", "gqa8k", "mixed", "prefix128k"])
-    ap.add_argument("--kernel", default="decode", choices=["decode", "prefill", "cascade"],
+    ap.add_argument("--kernel", default="decode", choices=["decode", "prefill", "cascade", "layers"],
                     help="with a workload other than append64k: what each step runs")
     ap.add_argument("--chunk", type=int, default=16, help="--kernel prefill: query tokens per sequence")
     ap.add_argument("--min-rows", type=int, default=0, help="--kernel cascade: min_rows of the cascade call")
     ap.add_argument("--batch", type=int, default=0, help="with a workload other than append64k: override B")
+    ap.add_argument("--layers", type=int, default=32, help="--kernel layers: attention layers in the stack")
+    ap.add_argument("--ctx", type=int, default=32768, help="--kernel layers: context per sequence")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel == "layers":
+        run_layers(args)
     elif args.workload != "append64k" or args.kernel != "decode":
         run_decode_only(args)
     else:

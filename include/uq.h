@@ -121,6 +121,10 @@ typedef struct uq_cache {
   float k_scale;        /* FP8 only (1.0 if unused) */
   float v_scale;        /* FP8 only (1.0 if unused) */
   uint64_t rot_seed;    /* FP4 and TQ4 */
+  float fp4_c;          /* FP4: the constant c of the scale rule, t = fl32(c * absmax); 0 selects
+                           the pages' 0.156f ([UQ-review] §3.3).  A per-layer constant is the
+                           pages' open option ([UQ-review] §7.3); uq_calibrate_c measures one.
+                           Negative, NaN or infinite: UQ_ERR_INVALID_ARG. */
 } uq_cache;
 
 /* Byte size of array `which` of the cache (0 = k_codes, 1 = k_scales,
@@ -271,6 +275,24 @@ uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q
                                const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
                                int32_t batch, int32_t num_q_heads, float sm_scale, float* out, void* workspace,
                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * c calibration ([UQ-residency]: the shrink constant is the c minimising
+ * E[(z - c m q(z / (c m)))^2] over rotated groups, z an element, m the group's
+ * absolute maximum, q the E2M1 grid; [UQ-review] §7.3: per-layer constants).
+ * Rotates n_vec rows x ([n_vec][head_dim], bf16 or fp32, device, 16-byte
+ * aligned) with the cache rotation of rot_seed and, for each of the n_c
+ * constants c_list[i] (host, 1 <= n_c <= 64, each finite > 0), writes to
+ * sse[i] (device fp64 [n_c], 8-byte aligned; overwritten) the sum over all
+ * elements of (z - rec)^2, where rec is the round trip of z through:
+ *   mode  0: the deployed rule of uq_quantize_append with c = c_list[i]
+ *            (UE8M0 byte of fl32(c m), E2M1 codes of z 2^-E);
+ *   mode -1: a continuous scale s = c m (codes of fl32(z / s), rec = s value).
+ * Groups with m = 0 add nothing; a non-finite group makes sse[i] NaN.  Set a
+ * layer's uq_cache.fp4_c to the minimiser over its captured keys.
+ */
+uq_status uq_calibrate_c(const void* x, int32_t in_dtype, int64_t n_vec, int32_t head_dim, uint64_t rot_seed,
+                         const float* c_list, int32_t n_c, int32_t mode, double* sse, cudaStream_t stream);
 
 /*
  * Cascade (shared-prefix) decode over an FP4 cache.  Agent sessions reuse one

@@ -52,6 +52,8 @@ _lib.uqo_e4m3_code.argtypes = [C.c_float]
 _lib.uqo_query_fp8.argtypes = [_u16p, C.c_int, C.c_uint64, _u8p]
 _lib.uqo_append_fp4.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
                                 C.c_int, C.c_uint64, _u8p, _u8p, _u8p, _u8p]
+_lib.uqo_append_fp4_c.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
+                                  C.c_int, C.c_uint64, C.c_float, _u8p, _u8p, _u8p, _u8p]
 _lib.uqo_append_fp8.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
                                 C.c_int, C.c_float, C.c_float, _u8p, _u8p]
 _lib.uqo_append_bf16.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
@@ -201,9 +203,11 @@ class Cache:
     """Host copy of a paged cache in the library's layout [P][Hkv][ps][row]."""
 
     def __init__(self, kind, num_pages, num_kv_heads, page_size, head_dim, k_scale=1.0, v_scale=1.0,
-                 seed=DEFAULT_SEED):
+                 seed=DEFAULT_SEED, c=None):
+        """c: the FP4 scale-rule constant (None: the pages' 0.156)."""
         self.kind, self.P, self.Hkv, self.ps, self.d = kind, num_pages, num_kv_heads, page_size, head_dim
         self.k_scale, self.v_scale, self.seed = float(k_scale), float(v_scale), seed
+        self.c = C_CONSTANT if c is None else float(c)
         rows = num_pages * num_kv_heads * page_size
         if kind == KIND_FP4:
             self.kc = np.zeros((rows, head_dim // 2), np.uint8)
@@ -233,7 +237,7 @@ class Cache:
         slots = _c(slot_mapping, np.int64)
         args = (ka.ctypes.data, va.ctypes.data, f32, T, slots, self.Hkv, self.ps, self.d)
         if self.kind == KIND_FP4:
-            _lib.uqo_append_fp4(*args, self.seed, self.kc, self.ks, self.vc, self.vs)
+            _lib.uqo_append_fp4_c(*args, self.seed, np.float32(self.c), self.kc, self.ks, self.vc, self.vs)
         elif self.kind == KIND_TQ4:
             _lib.uqo_append_tq4(*args, self.seed, _c(self.tau[8:], np.float32), self.kc, self.ks, self.vc, self.vs)
         elif self.kind == KIND_FP8:

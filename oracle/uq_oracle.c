@@ -225,16 +225,24 @@ static void load_row(const void* src, int in_fp32, int64_t row, int d, float* ou
 }
 
 /* Rotate + quantise n vectors (bf16 or fp32 rows). */
-void uqo_quantize_vectors(const void* x, int in_fp32, int64_t n, int d, uint64_t seed,
-                          uint8_t* codes, uint8_t* scales) {
+/* With a constant c of one's own in R2 (the pages keep one global c and name  */
+/* per-layer constants as an open option, [UQ-review] 7.3; the c sweep of     */
+/* [UQ-residency] is the objective that picks one).                            */
+void uqo_quantize_vectors_c(const void* x, int in_fp32, int64_t n, int d, uint64_t seed, float c,
+                            uint8_t* codes, uint8_t* scales) {
   int8_t s[1024];
   float xr[1024], y[1024];
   uqo_signs(seed, d, s);
   for (int64_t v = 0; v < n; ++v) {
     load_row(x, in_fp32, v, d, xr);
     uqo_rotate_fp32(xr, d, s, y);
-    uqo_quantize_rotated(y, 1, d, uqo_c_constant(), 0, codes + v * (d / 2), scales + v * (d / 32));
+    uqo_quantize_rotated(y, 1, d, c, 0, codes + v * (d / 2), scales + v * (d / 32));
   }
+}
+
+void uqo_quantize_vectors(const void* x, int in_fp32, int64_t n, int d, uint64_t seed,
+                          uint8_t* codes, uint8_t* scales) {
+  uqo_quantize_vectors_c(x, in_fp32, n, d, seed, uqo_c_constant(), codes, scales);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -306,9 +314,9 @@ static int64_t cache_row(int64_t slot, int h, int Hkv, int ps) {
 
 /* Quantize-append of T tokens of K and V ([T][Hkv][d], bf16 or fp32) into an */
 /* FP4 cache; slots < 0 are skipped.                                          */
-void uqo_append_fp4(const void* k, const void* v, int in_fp32, int64_t T, const int64_t* slots,
-                         int Hkv, int ps, int d, uint64_t seed, uint8_t* kc, uint8_t* ks,
-                         uint8_t* vc, uint8_t* vs) {
+void uqo_append_fp4_c(const void* k, const void* v, int in_fp32, int64_t T, const int64_t* slots,
+                      int Hkv, int ps, int d, uint64_t seed, float c, uint8_t* kc, uint8_t* ks,
+                      uint8_t* vc, uint8_t* vs) {
   size_t esz = in_fp32 ? 4 : 2;
   for (int64_t t = 0; t < T; ++t) {
     if (slots[t] < 0) continue;
@@ -317,11 +325,17 @@ void uqo_append_fp4(const void* k, const void* v, int in_fp32, int64_t T, const 
       const char* kr = (const char*)k + (size_t)src * d * esz;
       const char* vr = (const char*)v + (size_t)src * d * esz;
       uint8_t kn[512];
-      uqo_quantize_vectors(kr, in_fp32, 1, d, seed, kn, ks + dst * (d / 32));
+      uqo_quantize_vectors_c(kr, in_fp32, 1, d, seed, c, kn, ks + dst * (d / 32));
       for (int j = 0; j < d / 2; ++j) kc[dst * (d / 2) + uqo_kbyte_pos(j, d)] = kn[j];
-      uqo_quantize_vectors(vr, in_fp32, 1, d, seed, vc + dst * (d / 2), vs + dst * (d / 32));
+      uqo_quantize_vectors_c(vr, in_fp32, 1, d, seed, c, vc + dst * (d / 2), vs + dst * (d / 32));
     }
   }
+}
+
+void uqo_append_fp4(const void* k, const void* v, int in_fp32, int64_t T, const int64_t* slots,
+                    int Hkv, int ps, int d, uint64_t seed, uint8_t* kc, uint8_t* ks,
+                    uint8_t* vc, uint8_t* vs) {
+  uqo_append_fp4_c(k, v, in_fp32, T, slots, Hkv, ps, d, seed, uqo_c_constant(), kc, ks, vc, vs);
 }
 
 /* FP8 anchor append: e4m3_RNE_sat(x / scale), unrotated. */

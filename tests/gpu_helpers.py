@@ -23,9 +23,9 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def new_cache(w: workloads.Workload, dtype=uq.FP4_UE8M0, fill=0xFF, k_scale=1.0, v_scale=1.0):
+def new_cache(w: workloads.Workload, dtype=uq.FP4_UE8M0, fill=0xFF, k_scale=1.0, v_scale=1.0, fp4_c=0.0):
     return uq.KVCache(dtype, w.num_pages, w.Hkv, w.ps, w.D, k_scale=k_scale, v_scale=v_scale,
-                      fill=fill if dtype != uq.BF16 else 0x7FC0)
+                      fill=fill if dtype != uq.BF16 else 0x7FC0, fp4_c=fp4_c)
 
 
 def fill_cache(w, caches, block=8192, upto=None):
@@ -43,7 +43,7 @@ def fill_cache(w, caches, block=8192, upto=None):
     torch.cuda.synchronize()
 
 
-def oracle_for(w, seqs, dtype=uq.FP4_UE8M0, k_scale=1.0, v_scale=1.0, seed=uq.DEFAULT_SEED):
+def oracle_for(w, seqs, dtype=uq.FP4_UE8M0, k_scale=1.0, v_scale=1.0, seed=uq.DEFAULT_SEED, c=None):
     """Oracle cache holding only sequences `seqs` (identity page layout), built
     from the same seeded K/V; returns (cache, block_table, seq_lens)."""
     lens = [w.seq_lens[b] for b in seqs]
@@ -54,7 +54,7 @@ def oracle_for(w, seqs, dtype=uq.FP4_UE8M0, k_scale=1.0, v_scale=1.0, seed=uq.DE
     for i, p in enumerate(pages):
         bt[i, :p] = np.arange(nxt, nxt + p)
         nxt += p
-    oc = oracle.Cache(KIND[dtype], max(nxt, 1), w.Hkv, w.ps, w.D, k_scale=k_scale, v_scale=v_scale, seed=seed)
+    oc = oracle.Cache(KIND[dtype], max(nxt, 1), w.Hkv, w.ps, w.D, k_scale=k_scale, v_scale=v_scale, seed=seed, c=c)
     dev = torch.device("cuda")
     for i, b in enumerate(seqs):
         for t0 in range(0, lens[i], 16384):

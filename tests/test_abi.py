@@ -135,3 +135,23 @@ def test_cascade_workspace_covers_the_decode_workspace():
     assert a > dec and b >= dec
     assert uq.uq_cascade_workspace_bytes(4, 1, 64, 8, 256, 98304) == 0
     assert uq.uq_cascade_workspace_bytes(4, -1, 64, 8, 128, 98304) == 0
+
+
+def test_calibration_and_constant_argument_validation_without_a_device():
+    E = {v: k for k, v in uq.STATUS_NAMES.items()}
+    cs = (C.c_float * 2)(0.156, 0.2)
+    bad = (C.c_float * 2)(0.156, -1.0)
+    f = uq._lib.uq_calibrate_c
+    assert f(0x200000, 0, 16, 96, 42, C.cast(cs, C.c_void_p), 2, 0, 0x300000, None) == E["UQ_ERR_UNSUPPORTED"]
+    assert f(0x200000, 5, 16, 128, 42, C.cast(cs, C.c_void_p), 2, 0, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert f(0x200000, 0, 16, 128, 42, C.cast(cs, C.c_void_p), 0, 0, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert f(0x200000, 0, 16, 128, 42, C.cast(cs, C.c_void_p), 65, 0, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert f(0x200000, 0, 16, 128, 42, C.cast(cs, C.c_void_p), 2, 1, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert f(0x200000, 0, 16, 128, 42, C.cast(bad, C.c_void_p), 2, 0, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert f(0x200004, 0, 16, 128, 42, C.cast(cs, C.c_void_p), 2, 0, 0x300000, None) == E["UQ_ERR_ALIGNMENT"]
+    assert f(0x200000, 0, 16, 128, 42, C.cast(cs, C.c_void_p), 2, 0, 0x300004, None) == E["UQ_ERR_ALIGNMENT"]
+    s = _struct()
+    s.fp4_c = -0.5
+    assert _append(s) == E["UQ_ERR_INVALID_ARG"]
+    s.fp4_c = float("nan")
+    assert _decode(s) == E["UQ_ERR_INVALID_ARG"]

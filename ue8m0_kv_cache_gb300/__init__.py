@@ -38,7 +38,7 @@ class UqCacheStruct(C.Structure):
                 ("page_size", C.c_int32), ("head_dim", C.c_int32),
                 ("k_codes", C.c_void_p), ("k_scales", C.c_void_p), ("v_codes", C.c_void_p),
                 ("v_scales", C.c_void_p), ("k_scale", C.c_float), ("v_scale", C.c_float),
-                ("rot_seed", C.c_uint64)]
+                ("rot_seed", C.c_uint64), ("fp4_c", C.c_float)]
 
 
 _vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
@@ -54,6 +54,7 @@ _sig = {
     "uq_tq_codebook": (C.c_int, [_i32, _i32, _vp, _vp]),
     "uq_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "uq_prefill_attention": (C.c_int, [_vp, _vp, _i32, _CP, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "uq_calibrate_c": (C.c_int, [_vp, _i32, _i64, _i32, C.c_uint64, _vp, _i32, _i32, _vp, _vp]),
     "uq_cascade_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "uq_cascade_decode_attention": (C.c_int, [_vp, _CP, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _f32,
                                               _vp, _vp, _sz, _vp]),
@@ -101,7 +102,8 @@ class KVCache:
 
     def __init__(self, dtype: int, num_pages: int, num_kv_heads: int, page_size: int, head_dim: int,
                  device="cuda", rot_seed: int = DEFAULT_SEED, k_scale: float = 1.0, v_scale: float = 1.0,
-                 fill: Optional[int] = None):
+                 fill: Optional[int] = None, fp4_c: float = 0.0):
+        """fp4_c: the constant c of the FP4 scale rule (0: the default 0.156)."""
         self.dtype, self.num_pages, self.num_kv_heads = dtype, num_pages, num_kv_heads
         self.page_size, self.head_dim = page_size, head_dim
         shape = (num_pages, num_kv_heads, page_size)
@@ -128,7 +130,7 @@ class KVCache:
             self.k_scales = self.v_scales = None
         self.struct = UqCacheStruct(dtype, num_pages, num_kv_heads, page_size, head_dim,
                                     _ptr(self.k_codes), _ptr(self.k_scales), _ptr(self.v_codes),
-                                    _ptr(self.v_scales), k_scale, v_scale, rot_seed)
+                                    _ptr(self.v_scales), k_scale, v_scale, rot_seed, fp4_c)
 
     @property
     def rot_seed(self) -> int:
@@ -305,6 +307,21 @@ def uq_cascade_decode_attention(q, cache, block_table, seq_lens, cu_seqs, prefix
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _stream(stream)), "uq_cascade_decode_attention")
     return out
+
+
+def uq_calibrate_c(x: torch.Tensor, c_list, mode: int = 0, rot_seed: int = DEFAULT_SEED, stream=None):
+    """Mean squared error of the FP4 round trip of the rotated rows of x ([N][D] bf16 or fp32) for each
+    constant c of c_list (mode 0: the deployed power-of-two scale; -1: continuous scale c * absmax)."""
+    if x.dtype not in (torch.bfloat16, torch.float32) or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA bf16 or fp32 tensor")
+    d = x.shape[-1]
+    n = x.numel() // d
+    cs = (C.c_float * len(c_list))(*[float(c) for c in c_list])
+    sse = torch.empty(len(c_list), dtype=torch.float64, device=x.device)
+    _check(_lib.uq_calibrate_c(_ptr(x), IN_FP32 if x.dtype == torch.float32 else IN_BF16, n, d, rot_seed,
+                               C.cast(cs, C.c_void_p), len(c_list), mode, _ptr(sse), _stream(stream)),
+           "uq_calibrate_c")
+    return (sse / max(1, n * d)).cpu().numpy()
 
 
 def uq_check_device_status(stream=None) -> int:

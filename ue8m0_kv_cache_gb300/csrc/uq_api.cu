@@ -95,6 +95,7 @@ uq_status check_cache(const uq_cache* c) {
   if (!aligned16(c->k_codes) || !aligned16(c->v_codes)) return UQ_ERR_ALIGNMENT;
   if (packed && (!aligned16(c->k_scales) || !aligned16(c->v_scales))) return UQ_ERR_ALIGNMENT;
   if (c->dtype == UQ_FP8_E4M3 && !(c->k_scale > 0.f && c->v_scale > 0.f)) return UQ_ERR_INVALID_ARG;
+  if (!(c->fp4_c >= 0.f && c->fp4_c <= 3.4e38f)) return UQ_ERR_INVALID_ARG;
   return UQ_OK;
 }
 
@@ -300,6 +301,19 @@ uq_status uq_cascade_decode_attention(const void* q, const uq_cache* cache, cons
   a.casc = cg;
   a.px = px;
   return uqh::launch_decode(a, stream);
+}
+
+uq_status uq_calibrate_c(const void* x, int32_t in_dtype, int64_t n_vec, int32_t head_dim, uint64_t rot_seed,
+                         const float* c_list, int32_t n_c, int32_t mode, double* sse, cudaStream_t stream) {
+  if (in_dtype != UQ_IN_BF16 && in_dtype != UQ_IN_FP32) return UQ_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return UQ_ERR_UNSUPPORTED;
+  if (n_vec < 0 || n_c < 1 || n_c > 64 || (mode != 0 && mode != -1) || !c_list || !sse) return UQ_ERR_INVALID_ARG;
+  if (n_vec > 0 && !x) return UQ_ERR_INVALID_ARG;
+  for (int i = 0; i < n_c; ++i)
+    if (!(c_list[i] > 0.f && c_list[i] <= 3.4e38f)) return UQ_ERR_INVALID_ARG;
+  if (n_vec > 0 && !aligned16(x)) return UQ_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(sse) & 7u) != 0) return UQ_ERR_ALIGNMENT;
+  return uqh::launch_calibrate(x, in_dtype == UQ_IN_FP32, n_vec, head_dim, rot_seed, c_list, n_c, mode, sse, stream);
 }
 
 uq_status uq_check_device_status(cudaStream_t stream) {

@@ -49,6 +49,7 @@ struct AppendParams {
   unsigned int* status;
   uqh::SignMasks sign;
   float tq_tpos[7];  // TQ4: positive decision thresholds tau_8..tau_14
+  float c;           // FP4: the constant of the scale rule
 };
 
 // Rotation of a register-resident row whose signs were already applied.
@@ -64,14 +65,14 @@ __device__ __forceinline__ void rotate_regs(float (&u)[D]) {
 // row's D/2 code bytes, `scales` the D/32 scale bytes (little-endian).
 template <int D>
 __device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D / 8],
-                                              uint32_t& scales) {
+                                              uint32_t& scales, float c = kFp4C) {
   scales = 0;
 #pragma unroll
   for (int g = 0; g < D / 32; ++g) {
     float mx = max_abs_nan(y[32 * g], y[32 * g + 1]);
 #pragma unroll
     for (int i = 2; i < 32; ++i) mx = max_abs_nan(mx, y[32 * g + i]);
-    const uint32_t byte = scale_byte(fabsf(mx));
+    const uint32_t byte = scale_byte(fabsf(mx), c);
     const float inv = inv_scale(byte == 0xFFu ? 127u : byte);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) mul2(y[32 * g + i], y[32 * g + i + 1], inv);
@@ -172,7 +173,7 @@ __device__ __forceinline__ void quantize_store(float (&u)[D], const AppendParams
   if (TQ)
     quantize_tq_regs<D>(u, codes, scales, p.tq_tpos);
   else
-    quantize_regs<D>(u, codes, scales);
+    quantize_regs<D>(u, codes, scales, p.c);
   if (is_v)
     store_row<D, false, TQ>(p.vc, p.vs, dst, codes, scales);
   else
@@ -426,6 +427,87 @@ __global__ void test_quantize_kernel(const float* y, int64_t n, uint8_t* codes, 
   store_row<D, false>(codes, scales, r, c, s);
 }
 
+// c calibration: the squared reconstruction error of the FP4 round trip of
+// rotated rows, for each constant c of a list ([UQ-residency]: c* = argmin_c
+// E[(z - c m q(z / (c m)))^2]; [UQ-review] §7.3: per-layer constants).  One
+// thread per row: the row is rotated as in the append, then for each c every
+// 32-channel group is coded with mode 0, the deployed rule (the append's scale
+// byte, r = y * 2^-E and the hardware E2M1 conversion), or mode -1, a
+// continuous scale s = c * m (r = fl32(y / s)); the error y - s * value is
+// summed in fp64 and added to sse[c] once per warp.
+struct CalibParams {
+  const void* x;
+  int64_t n;
+  int in_fp32, n_c, mode;
+  float c[64];
+  double* sse;
+  uqh::SignMasks sign;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) calibrate_kernel(const __grid_constant__ CalibParams p) {
+  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const bool live = r < p.n;
+  float y[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) {
+    uint32_t b = 0;
+    if (live)
+      b = p.in_fp32 ? __float_as_uint(static_cast<const float*>(p.x)[r * D + i])
+                    : static_cast<uint32_t>(static_cast<const uint16_t*>(p.x)[r * D + i]) << 16;
+    y[i] = __uint_as_float(b ^ p.sign.m[i]);
+  }
+  rotate_regs<D>(y);
+  for (int ci = 0; ci < p.n_c; ++ci) {
+    const float c = p.c[ci];
+    double acc = 0.0;
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+      float mx = max_abs_nan(y[32 * g], y[32 * g + 1]);
+#pragma unroll
+      for (int i = 2; i < 32; ++i) mx = max_abs_nan(mx, y[32 * g + i]);
+      const float m = fabsf(mx);
+      if (m == 0.f) continue;
+      uint32_t byte = 0;
+      double s;
+      float inv;
+      if (p.mode == 0) {
+        byte = scale_byte(m, c);
+        s = ldexp(1.0, static_cast<int>(byte) - 127);
+        inv = inv_scale(byte == 0xFFu ? 127u : byte);
+      } else {
+        s = static_cast<double>(c) * static_cast<double>(m);
+        inv = 0.f;
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float v = y[32 * g + 8 * w + k];
+          e[k] = p.mode == 0 ? v * inv : static_cast<float>(static_cast<double>(v) / s);
+        }
+        const uint32_t word = cvt_e2m1x2(e[0], e[1]) | (cvt_e2m1x2(e[2], e[3]) << 8) |
+                              (cvt_e2m1x2(e[4], e[5]) << 16) | (cvt_e2m1x2(e[6], e[7]) << 24);
+        uint32_t h[4];
+        e2m1x8_to_f16x2(word, h);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+          const double d0 = static_cast<double>(y[32 * g + 8 * w + 2 * k]) - static_cast<double>(f.x) * s;
+          const double d1 = static_cast<double>(y[32 * g + 8 * w + 2 * k + 1]) - static_cast<double>(f.y) * s;
+          acc += d0 * d0 + d1 * d1;
+        }
+      }
+      if (byte == 0xFFu) acc = __longlong_as_double(0x7FF8000000000000ll);  // a non-finite group
+    }
+    if (!live) acc = 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&p.sse[ci], acc);
+  }
+}
+
 __global__ void test_cvt_e4m3_kernel(const float* x, int64_t n2, uint16_t* out) {
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i < n2) out[i] = static_cast<uint16_t>(cvt_e4m3x2(x[2 * i], x[2 * i + 1]));
@@ -517,6 +599,7 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
   } else {
     for (int k = 0; k < 7; ++k) p.tq_tpos[k] = 0.f;
   }
+  p.c = fp4_c(c);
   // kernel instance by (head_dim, input type, format)
   const int which = (c.head_dim == 128 ? 4 : 0) + (in_fp32 ? 2 : 0) + (tq ? 1 : 0);
   if (nrows <= kSmallAppendRows) {
@@ -592,6 +675,27 @@ uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes,
     test_quantize_kernel<128><<<grid, 128, 0, s>>>(y, n, codes, scales);
   else
     test_quantize_kernel<64><<<grid, 128, 0, s>>>(y, n, codes, scales);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_calibrate(const void* x, bool in_fp32, int64_t n, int d, uint64_t seed, const float* c_list,
+                           int n_c, int mode, double* sse, cudaStream_t s) {
+  CalibParams p;
+  p.x = x;
+  p.n = n;
+  p.in_fp32 = in_fp32 ? 1 : 0;
+  p.n_c = n_c;
+  p.mode = mode;
+  for (int i = 0; i < 64; ++i) p.c[i] = i < n_c ? c_list[i] : 0.f;
+  p.sse = sse;
+  make_sign_masks(seed, d, &p.sign);
+  if (cudaMemsetAsync(sse, 0, sizeof(double) * n_c, s) != cudaSuccess) return UQ_ERR_CUDA;
+  if (n == 0) return UQ_OK;
+  const unsigned grid = static_cast<unsigned>((n + 127) / 128);
+  if (d == 128)
+    calibrate_kernel<128><<<grid, 128, 0, s>>>(p);
+  else
+    calibrate_kernel<64><<<grid, 128, 0, s>>>(p);
   return cuda_status(cudaGetLastError());
 }
 

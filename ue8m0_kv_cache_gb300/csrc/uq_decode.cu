@@ -114,6 +114,7 @@ struct DecParams {
   uint8_t* wks;
   uint8_t* wvc;
   uint8_t* wvs;
+  float fp4_c;  // the scale-rule constant of the cache
   // Cascade (casc_cu == nullptr: none): the decode skips each group's shared keys.
   const int32_t* casc_cu;
   const int32_t* casc_prefix;
@@ -222,13 +223,14 @@ __device__ __forceinline__ void rotated_query_bytes(const uint16_t* qrow, bool v
 // the group's UE8M0 byte and the E2M1 codes of this thread's channels, with
 // the same arithmetic as the append path.  All lanes must call it.
 template <int D>
-__device__ __forceinline__ void quantize_quad(float (&x)[D / 4], uint32_t (&codes)[D / 32], uint32_t& byte) {
+__device__ __forceinline__ void quantize_quad(float (&x)[D / 4], uint32_t (&codes)[D / 32], uint32_t& byte,
+                                              float c) {
   constexpr int CPT = D / 4;
   float mx = max_abs_nan(x[0], x[1]);
 #pragma unroll
   for (int i = 2; i < CPT; ++i) mx = max_abs_nan(mx, x[i]);
   if (CPT < 32) mx = max_abs_nan(mx, __shfl_xor_sync(kFull, mx, 1));
-  byte = scale_byte(fabsf(mx));
+  byte = scale_byte(fabsf(mx), c);
   const float inv = inv_scale(byte == 0xFFu ? 127u : byte);
 #pragma unroll
   for (int i = 0; i < CPT; i += 2) mul2(x[i], x[i + 1], inv);
@@ -818,7 +820,7 @@ __device__ __noinline__ bool fused_append(const DecParams& p, uint8_t* scratch, 
   if (p.new_f32) rotate_quad<D, true>(src, active, c, p.sign, x);
   else rotate_quad<D, false>(src, active, c, p.sign, x);
   uint32_t codes[NW], byte;
-  quantize_quad<D>(x, codes, byte);
+  quantize_quad<D>(x, codes, byte, p.fp4_c);
   if (active) {
     const int64_t dst = (((slot >> p.ps_log2) * p.Hkv + kvh) << p.ps_log2) + (slot & ps_mask);
     uint8_t* gcodes = (is_v ? p.wvc : p.wkc) + dst * C::KROW;
@@ -1482,6 +1484,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.wks = static_cast<uint8_t*>(c.k_scales);
   p.wvc = static_cast<uint8_t*>(c.v_codes);
   p.wvs = static_cast<uint8_t*>(c.v_scales);
+  p.fp4_c = uqh::fp4_c(c);
   p.casc_cu = a.casc.cu;
   p.casc_prefix = a.casc.prefix;
   p.casc_groups = a.casc.groups;

@@ -85,15 +85,17 @@ __device__ __forceinline__ float max_abs_nan(float a, float b) {
 }
 
 // UE8M0 byte of a group with absolute maximum m (m >= 0 or NaN):
-// t = fl32(0.156f * m); E = integer nearest to log2(t); byte = clamp(E+127,
+// t = fl32(c * m), c = 0.156f unless a cache sets its own constant;
+// E = integer nearest to log2(t); byte = clamp(E+127,
 // 0, 254).  For a normal t = 2^(e-127) (1 + f/2^23), log2 t rounds up exactly
 // when 1 + f/2^23 >= sqrt(2), i.e. f >= 0x3504F4 (sqrt(2) is irrational, so
 // there are no ties).  A subnormal t = bits * 2^-149 rounds to 2^-126 (byte 1)
 // when t >= 2^-126.5, i.e. bits >= 5931642; anything smaller clamps to 0.
 // Non-finite m gives 0xFF.  (The 0.156 constant: [UQ-review] §3.3.)
-__device__ __forceinline__ uint32_t scale_byte(float m) {
+constexpr float kFp4C = 0.156f;
+__device__ __forceinline__ uint32_t scale_byte(float m, float c = kFp4C) {
   if (!(m <= 3.40282347e38f)) return 0xFFu;
-  const float t = __fmul_rn(0.156f, m);
+  const float t = __fmul_rn(c, m);
   const uint32_t bits = __float_as_uint(t);
   if (bits >= 0x00800000u) {
     const uint32_t e = bits >> 23, f = bits & 0x7FFFFFu;

@@ -31,6 +31,9 @@ const DevInfo& dev_info();
 
 inline uq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? UQ_OK : UQ_ERR_CUDA; }
 
+// The FP4 scale-rule constant of a cache (0 selects the default 0.156f).
+inline float fp4_c(const uq_cache& c) { return c.fp4_c > 0.f ? c.fp4_c : 0.156f; }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
@@ -79,6 +82,8 @@ uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, fl
 uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s);
 uq_status launch_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+uq_status launch_calibrate(const void* x, bool in_fp32, int64_t n, int d, uint64_t seed, const float* c_list,
+                           int n_c, int mode, double* sse, cudaStream_t s);
 
 // Cascade decode: groups of consecutive sequences that share a key prefix
 // (see casc_shared_keys in uq_device.cuh for the split between the kernels).
