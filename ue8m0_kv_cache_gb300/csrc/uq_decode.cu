@@ -901,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
   uint8_t* myring = ring + warp * C::NST * C::STAGE;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], packed4(KIND) ? 1 + 32 : 1);  // see the copy issue
+    for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], packed4(KIND) ? 32 : 1);  // see the copy issue
     fence_mbar_init();
   }
   if (tid == 0) abort_flag = 0;
@@ -1009,12 +1009,13 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
       return page;
     };
     int pf = page_of_lane(lane), pf_next = page_of_lane(32 + lane);
-    // Lanes 0 and 1 issue the unit's two bulk copies (K codes, V codes); the
-    // FP4 scale rows (64 + 64 bytes at D = 128) are fetched by per-lane 4-byte
-    // cp.async, which costs less than two more bulk-copy requests.  Both
-    // complete on the stage's mbarrier: the copies by their byte count, the
-    // cp.async of every lane by one no-increment arrival each, so an FP4
-    // stage barrier expects 1 + 32 arrivals.
+    // FP4 and TQ4: every lane copies 16-byte chunks of the unit's K and V code
+    // rows and 4-byte words of its scale (or norm) rows with cp.async, and one
+    // no-increment arrival per lane completes the stage barrier (32 arrivals):
+    // per-lane copies go through the load/store path at its full rate, where
+    // each bulk-copy request would cost the copy engine a fixed issue time.
+    // The anchors' larger rows (FP8 2 KB, BF16 4 KB per array and unit) come
+    // by two bulk copies, from lanes 0 and 1, on a barrier of one arrival.
     const uint8_t* cp_base = lane == 1 ? p.vc : p.kc;
     const uint32_t cp_off = lane == 1 ? C::KBYTES : 0;
     const uint32_t ring_u32 = smem_u32(myring), bars_u32 = smem_u32(mybars);
@@ -1022,24 +1023,36 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
       const int tok0 = (ub + j0 + warp + i * kWarps) * kChunk;
       const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
       const uint32_t bar = bars_u32 + 8u * slot;
-      if (lane == 0)
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(uint32_t(2 * C::KBYTES))
-                     : "memory");
-      if (lane < 2)
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                ring_u32 + slot * uint32_t(C::STAGE) + cp_off),
-            "l"(cp_base + row0 * C::KROW), "r"(uint32_t(C::KBYTES)), "r"(bar)
-            : "memory");
+      const uint32_t sbase = ring_u32 + slot * uint32_t(C::STAGE);
       if (packed4(KIND)) {
+        constexpr int CW = C::KBYTES / 16;  // 16-byte chunks per array and unit
+        const uint8_t* gk = p.kc + row0 * C::KROW;
+        const uint8_t* gv = p.vc + row0 * C::KROW;
+#pragma unroll
+        for (int j = lane; j < CW; j += 32) {
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + 16 * j), "l"(gk + 16 * j)
+                       : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + C::KBYTES + 16 * j),
+                       "l"(gv + 16 * j) : "memory");
+        }
         constexpr int SW = C::SBYTES / 4;  // scale (or norm) words per array and unit
 #pragma unroll
         for (int w = lane; w < 2 * SW; w += 32) {
           const uint8_t* g = (w < SW ? p.ks : p.vs) + row0 * C::SROW + 4 * (w < SW ? w : w - SW);
-          const uint32_t d = ring_u32 + slot * uint32_t(C::STAGE) + 2 * C::KBYTES + 4 * w;
-          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(g) : "memory");
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sbase + 2 * C::KBYTES + 4 * w), "l"(g)
+                       : "memory");
         }
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+      } else {
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                       "r"(uint32_t(2 * C::KBYTES)) : "memory");
+        if (lane < 2)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  sbase + cp_off),
+              "l"(cp_base + row0 * C::KROW), "r"(uint32_t(C::KBYTES)), "r"(bar)
+              : "memory");
       }
     };
     for (int i = 0; i < (nw < C::NST ? nw : C::NST); ++i) issue(i, (it + i) % C::NST, __shfl_sync(kFull, pf, i));
