@@ -25,7 +25,6 @@ uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
   return z ^ (z >> 31);
 }
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_status[kMaxDevices];
 DevInfo g_info[kMaxDevices];

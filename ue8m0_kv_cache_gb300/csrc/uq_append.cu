@@ -552,17 +552,24 @@ uq_status run_fp4_append(const CUtensorMap& mk, const CUtensorMap& mv, const App
   constexpr int STAGEB = 2 * kRows * D * (F32 ? 4 : 2);
   constexpr size_t smem = 2 * STAGEB + 1024;
   auto kern = fp4_append_kernel<D, F32, TQ>;
-  static int configured_dev = -1;  // attribute is per device; re-set when the device changes
+  // The shared-memory attribute is per device and kernel: set once per device, with the
+  // blocks per SM it allows (host threads may call concurrently).
+  static std::mutex cfg_mu;
+  static int cfg_per_sm[uqh::kMaxDevices];
   const uqh::DevInfo& di = uqh::dev_info();
-  if (configured_dev != di.device) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return UQ_ERR_CUDA;
-    configured_dev = di.device;
+  if (di.device < 0) return UQ_ERR_CUDA;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lk(cfg_mu);
+    if (cfg_per_sm[di.device] == 0) {
+      int n = 0;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAppendThreads, smem) != cudaSuccess || n < 1)
+        return UQ_ERR_CUDA;
+      cfg_per_sm[di.device] = n;
+    }
+    per_sm = cfg_per_sm[di.device];
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAppendThreads, smem) != cudaSuccess ||
-      per_sm < 1)
-    return UQ_ERR_CUDA;
   const int64_t ntiles = (nrows + kRows - 1) / kRows;
   const int64_t grid = std::min<int64_t>(ntiles, (int64_t)di.sms * per_sm);
   kern<<<(unsigned)grid, kAppendThreads, smem, s>>>(mk, mv, p);

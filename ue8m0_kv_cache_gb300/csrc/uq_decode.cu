@@ -1423,20 +1423,26 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   auto kern = decode_kernel<KIND, D>;
   const uqh::DevInfo& di = uqh::dev_info();
   if (smem > di.smem_optin) return UQ_ERR_UNSUPPORTED;
-  // The attribute is per device; it is raised to the largest size seen so far.
-  static int cfg_dev = -1;
-  static size_t cfg_smem = 0;
-  static int per_sm = 0;
-  if (cfg_dev != di.device || smem > cfg_smem) {
-    const size_t want = smem > cfg_smem || cfg_dev != di.device ? smem : cfg_smem;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)want) != cudaSuccess)
-      return UQ_ERR_CUDA;
-    // occupancy is set by registers and the fixed part of shared memory
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::smem_fixed) != cudaSuccess ||
-        per_sm < 1)
-      return UQ_ERR_CUDA;
-    cfg_dev = di.device;
-    cfg_smem = want;
+  // The shared-memory attribute is per device and kernel; it is raised to the
+  // largest size seen so far on each device (host threads may call concurrently).
+  static std::mutex cfg_mu;
+  static size_t cfg_smem[uqh::kMaxDevices];
+  static int cfg_per_sm[uqh::kMaxDevices];
+  if (di.device < 0) return UQ_ERR_CUDA;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lk(cfg_mu);
+    if (smem > cfg_smem[di.device]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return UQ_ERR_CUDA;
+      // occupancy is set by registers and the fixed part of shared memory
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, C::smem_fixed) != cudaSuccess || n < 1)
+        return UQ_ERR_CUDA;
+      cfg_per_sm[di.device] = n;
+      cfg_smem[di.device] = smem;
+    }
+    per_sm = cfg_per_sm[di.device];
   }
   // Workspace: [pair info][per-slot (m, l) x 8 heads][per-slot O x 8 heads]
   const size_t info = ws_info_bytes(pairs);

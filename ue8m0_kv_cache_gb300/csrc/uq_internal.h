@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -21,7 +22,9 @@ void make_sign_masks(uint64_t seed, int d, SignMasks* out);
 // Device status word of the current device (for in-kernel error records).
 unsigned int* status_word();
 
-// Properties of the current device (cached).
+constexpr int kMaxDevices = 64;
+
+// Properties of the current device (cached; device = -1 when there is none).
 struct DevInfo {
   int device = -1;
   int sms = 0;

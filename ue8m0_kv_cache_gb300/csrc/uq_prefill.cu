@@ -743,15 +743,20 @@ constexpr int kItemRows = kTRows;  // query rows per work item
 // Kernel attributes, once per device; the CTAs per SM.
 template <int D>
 int prefill_ctas_per_sm() {
-  static int cfg_dev = -1;
+  static std::mutex cfg_mu;
+  static bool done[uqh::kMaxDevices];
   const uqh::DevInfo& di = uqh::dev_info();
-  if (cfg_dev != di.device) {
-    if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC<D>::SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
-            cudaSuccess)
-      return 0;
-    cfg_dev = di.device;
+  if (di.device < 0) return 0;
+  {
+    std::lock_guard<std::mutex> lk(cfg_mu);
+    if (!done[di.device]) {
+      if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC<D>::SMEM) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+              cudaSuccess)
+        return 0;
+      done[di.device] = true;
+    }
   }
   // Two CTAs per SM: their shared memory (2 x 93 KB), registers (2 x 128 x 255)
   // and tensor-memory columns (2 x 256 of 512) fit, and each CTA's serial phases
