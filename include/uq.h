@@ -113,7 +113,7 @@ typedef struct uq_cache {
   int32_t num_pages;
   int32_t num_kv_heads;
   int32_t page_size;    /* power of two, 16..256 */
-  int32_t head_dim;     /* 64 or 128 */
+  int32_t head_dim;     /* 64, 128 or 256 (TQ4: 64 or 128) */
   void* k_codes;
   void* k_scales;
   void* v_codes;
@@ -194,8 +194,8 @@ size_t uq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num
  * out         : device fp32 [batch][num_q_heads][head_dim].
  * workspace   : device, >= 16-byte aligned, workspace_bytes long (see
  *               uq_decode_workspace_bytes); contents need not be initialised.
- * Supported: head_dim 64 or 128, page_size a power of two in [16, 256],
- * num_q_heads a multiple of num_kv_heads, batch <= 4096.
+ * Supported: head_dim 64, 128 or 256 (TQ4: 64 or 128), page_size a power of
+ * two in [16, 256], num_q_heads a multiple of num_kv_heads, batch <= 4096.
  */
 uq_status uq_decode_attention(const void* q, const uq_cache* cache, const int32_t* block_table,
                               int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
@@ -220,7 +220,7 @@ uq_status uq_decode_attention(const void* q, const uq_cache* cache, const int32_
  *                written); -1 = no new token (seq_lens[b] must then not
  *                count one).
  * Other arguments and errors as uq_decode_attention.  UQ_ERR_UNSUPPORTED for
- * FP8 / BF16 caches.
+ * FP8 / BF16 / TQ4 caches and for head_dim 256.
  */
 uq_status uq_decode_attention_append(const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
                                      const int64_t* new_slots, const uq_cache* cache, const int32_t* block_table,
@@ -267,7 +267,8 @@ uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const in
  * workspace   : device, 16-byte aligned, at least
  *               uq_prefill_workspace_bytes(num_q_tokens, batch, num_q_heads,
  *               num_kv_heads, head_dim, max_pages_per_seq * page_size) bytes.
- * FP4 caches only (UQ_ERR_UNSUPPORTED otherwise); shapes as the decode.
+ * FP4 caches with head_dim 64 or 128 (UQ_ERR_UNSUPPORTED otherwise); other
+ * shapes as the decode.
  */
 size_t uq_prefill_workspace_bytes(int32_t num_q_tokens, int32_t batch, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t max_keys);
@@ -387,7 +388,7 @@ const char* uq_status_string(uq_status status);
 void uq_rotation_signs(uint64_t seed, int32_t d, int8_t* host_out);
 
 /* ---- test hooks: single stages of the path, for bit-exact checks ---------
- * All pointers are device pointers; d is 64 or 128. */
+ * All pointers are device pointers; d is 64, 128 or 256. */
 
 /* Forward rotation of n_vec fp32 rows: y = fl32(FWHT(s .* x) * fl32(1/sqrt d)). */
 uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, float* y,

@@ -71,7 +71,7 @@ def test_large_workload_sampled_bit_exact(name):
 
 
 @pytest.mark.parametrize("d,ps,T", [(128, 16, 1), (128, 16, 77), (64, 32, 333), (128, 256, 1000),
-                                    (64, 16, 5)])
+                                    (64, 16, 5), (256, 16, 77), (256, 64, 333)])
 def test_edge_shapes(d, ps, T):
     w = workloads.make("gqa8k", B=1, Hkv=3, Hq=3, D=d, ps=ps, seq_lens=[T], seed=9, n_outlier=2,
                        outlier_channels=None)
@@ -116,3 +116,15 @@ def test_anchor_append_bit_exact(dtype, fp32_in):
     fill_cache(w, [cache])
     for b in range(w.B):
         _compare(w, cache, b, np.arange(w.seq_lens[b]), dtype)
+
+
+@pytest.mark.parametrize("fp32_in", [False, True])
+def test_head_dim_256_bit_exact(fp32_in):
+    """D = 256 runs a warp-per-row append (a row is too long for one thread's registers)."""
+    w = workloads.make("gqa8k", B=2, Hkv=2, Hq=2, D=256, ps=16, seq_lens=[300, 17], seed=12, n_outlier=4,
+                       outlier_channels=None, kv_fp32=fp32_in)
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    assert uq.uq_check_device_status() == 0
+    for b in range(2):
+        _compare(w, cache, b, np.arange(w.seq_lens[b]))

@@ -83,7 +83,7 @@ def test_group_sizes(G):
     assert_close(_run(w, cache, q), _ref(w, [0, 1, 2], q), "G=%d" % G)
 
 
-@pytest.mark.parametrize("d,ps", [(64, 16), (128, 32), (64, 256), (128, 128)])
+@pytest.mark.parametrize("d,ps", [(64, 16), (128, 32), (64, 256), (128, 128), (256, 16), (256, 64)])
 def test_head_dims_and_page_sizes(d, ps):
     w = workloads.make("gqa8k", B=2, Hkv=2, Hq=16, D=d, ps=ps, seq_lens=[700, 1], seed=30, n_outlier=3,
                        outlier_channels=None)
@@ -162,3 +162,37 @@ def test_anchor_decode_gqa8k(dtype):
     rng = np.random.default_rng(14)
     seqs = sorted(rng.choice(w.B, 3, replace=False).tolist())
     assert_close(_run(w, cache, q)[seqs], _ref(w, seqs, q, dtype), "anchor gqa8k")
+
+
+@pytest.mark.parametrize("dtype", [uq.FP4_UE8M0, uq.FP8_E4M3, uq.BF16])
+def test_head_dim_256(dtype):
+    w = workloads.make("gqa8k", B=3, Hkv=2, Hq=16, D=256, ps=16, seq_lens=[900, 33, 2000], seed=44, n_outlier=4,
+                       outlier_channels=None)
+    cache = new_cache(w, dtype)
+    fill_cache(w, [cache])
+    q = w.q()
+    assert_close(_run(w, cache, q), _ref(w, [0, 1, 2], q, dtype), "d=256 kind %d" % dtype)
+
+
+def test_head_dim_256_unbuilt_paths_are_unsupported():
+    """At D = 256 the fused append, chunked prefill, cascade, TQ4 and c calibration are not built."""
+    w = workloads.make("gqa8k", B=1, Hkv=1, Hq=8, D=256, ps=16, seq_lens=[64], seed=45)
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    bt = torch.from_numpy(w.block_table).to(DEV)
+    sl = torch.tensor([64], dtype=torch.int32, device=DEV)
+    q = w.q().to(DEV)
+    k, v = w.kv(0, 63, 1, device=DEV)
+    slots = torch.from_numpy(w.slots(0, 63, 1)).to(DEV)
+    calls = [
+        lambda: uq.uq_decode_attention_append(q, k, v, slots, cache, bt, sl),
+        lambda: uq.uq_prefill_attention(q, torch.tensor([0, 1], dtype=torch.int32, device=DEV), cache, bt, sl),
+        lambda: uq.uq_cascade_decode_attention(q, cache, bt, sl, torch.tensor([0, 1], dtype=torch.int32, device=DEV),
+                                               torch.tensor([32], dtype=torch.int32, device=DEV), 32, min_rows=0),
+        lambda: uq.uq_calibrate_c(torch.zeros((4, 256), device=DEV), [0.156]),
+        lambda: uq.uq_quantize_append(k, v, slots, new_cache(w, uq.TQ4)),
+    ]
+    for f in calls:
+        with pytest.raises(uq.UqError) as e:
+            f()
+        assert e.value.status == 2  # UQ_ERR_UNSUPPORTED

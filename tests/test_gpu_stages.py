@@ -21,7 +21,7 @@ def _rows(n, d, seed):
     return x.float()
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_rotation_bit_exact(d):
     x = _rows(4096, d, 1)
     for seed in (0, 42):
@@ -41,7 +41,7 @@ def _check_quant(y):
     assert bad.size == 0, (bad[:5], cc[tuple(bad[0])], rc[tuple(bad[0])], y.reshape(-1, d)[bad[0][0]])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_quantizer_random_rows(d):
     x = _rows(8192, d, 2).numpy()
     _check_quant(oracle.rotate_fp32(x, 42))
@@ -101,7 +101,7 @@ def test_quantizer_nonfinite_groups():
     _check_quant(y)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_query_prologue_bit_exact(d):
     g = torch.Generator().manual_seed(5)
     q = torch.randn(1000, d, generator=g)

@@ -16,7 +16,7 @@ LIB = os.path.join(HERE, "libuq.so")
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "--diag-suppress=177", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(HERE, "..", "include")]
 
 

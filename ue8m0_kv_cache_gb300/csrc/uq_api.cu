@@ -39,7 +39,7 @@ int current_device() {
 
 void make_sign_masks(uint64_t seed, int d, SignMasks* out) {
   std::memset(out, 0, sizeof(*out));
-  for (int i = 0; i < d && i < 128; ++i) out->m[i] = (splitmix64_at(seed, i) >> 63) ? 0x80000000u : 0u;
+  for (int i = 0; i < d && i < 256; ++i) out->m[i] = (splitmix64_at(seed, i) >> 63) ? 0x80000000u : 0u;
 }
 
 unsigned int* status_word() {
@@ -85,7 +85,8 @@ uq_status check_cache(const uq_cache* c) {
   if (c->dtype < UQ_FP4_UE8M0 || c->dtype > UQ_TQ4) return UQ_ERR_INVALID_ARG;
   if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 || c->head_dim <= 0)
     return UQ_ERR_INVALID_ARG;
-  if (c->head_dim != 64 && c->head_dim != 128) return UQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return UQ_ERR_UNSUPPORTED;
+  if (c->head_dim == 256 && c->dtype == UQ_TQ4) return UQ_ERR_UNSUPPORTED;
   if (!is_pow2(c->page_size) || c->page_size < 16 || c->page_size > 256) return UQ_ERR_UNSUPPORTED;
   if ((int64_t)c->num_pages * c->num_kv_heads * c->page_size >= (int64_t(1) << 40)) return UQ_ERR_UNSUPPORTED;
   if (!c->k_codes || !c->v_codes) return UQ_ERR_INVALID_ARG;
@@ -187,7 +188,7 @@ uq_status uq_decode_attention_append(const void* q, const void* k_new, const voi
                                      int32_t num_q_heads, float sm_scale, float* out, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream) {
   if (!cache) return UQ_ERR_INVALID_ARG;
-  if (cache->dtype != UQ_FP4_UE8M0) return UQ_ERR_UNSUPPORTED;
+  if (cache->dtype != UQ_FP4_UE8M0 || cache->head_dim == 256) return UQ_ERR_UNSUPPORTED;
   if (in_dtype != UQ_IN_BF16 && in_dtype != UQ_IN_FP32) return UQ_ERR_INVALID_ARG;
   if (batch > 0 && (!k_new || !v_new || !new_slots)) return UQ_ERR_INVALID_ARG;
   if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return UQ_ERR_ALIGNMENT;
@@ -235,7 +236,7 @@ uq_status uq_prefill_attention(const void* q, const int32_t* cu_q, int32_t num_q
                                size_t workspace_bytes, cudaStream_t stream) {
   uq_status st = check_cache(cache);
   if (st != UQ_OK) return st;
-  if (cache->dtype != UQ_FP4_UE8M0) return UQ_ERR_UNSUPPORTED;
+  if (cache->dtype != UQ_FP4_UE8M0 || cache->head_dim == 256) return UQ_ERR_UNSUPPORTED;
   if (batch < 0 || num_q_tokens < 0 || num_q_heads <= 0 || max_pages_per_seq < 1) return UQ_ERR_INVALID_ARG;
   if (num_q_heads % cache->num_kv_heads != 0) return UQ_ERR_INVALID_ARG;
   if (batch == 0 || num_q_tokens == 0) return UQ_OK;
@@ -344,7 +345,7 @@ void uq_rotation_signs(uint64_t seed, int32_t d, int8_t* host_out) {
 }
 
 uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, float* y, cudaStream_t stream) {
-  if ((d != 64 && d != 128) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
   if (n_vec == 0) return UQ_OK;
   if (!x || !y) return UQ_ERR_INVALID_ARG;
   return uqh::launch_test_rotate(x, n_vec, d, seed, y, stream);
@@ -352,7 +353,7 @@ uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed
 
 uq_status uq_test_quantize_rotated(const float* y, int64_t n_vec, int32_t d, uint8_t* codes, uint8_t* scales,
                                    cudaStream_t stream) {
-  if ((d != 64 && d != 128) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
   if (n_vec == 0) return UQ_OK;
   if (!y || !codes || !scales) return UQ_ERR_INVALID_ARG;
   if (!aligned16(codes)) return UQ_ERR_ALIGNMENT;
@@ -361,7 +362,7 @@ uq_status uq_test_quantize_rotated(const float* y, int64_t n_vec, int32_t d, uin
 
 uq_status uq_test_query_fp8(const void* q, int64_t n_vec, int32_t d, uint64_t seed, uint8_t* out,
                             cudaStream_t stream) {
-  if ((d != 64 && d != 128) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
   if (n_vec == 0) return UQ_OK;
   if (!q || !out) return UQ_ERR_INVALID_ARG;
   if (!aligned16(q)) return UQ_ERR_ALIGNMENT;

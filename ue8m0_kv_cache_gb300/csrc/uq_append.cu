@@ -65,7 +65,7 @@ __device__ __forceinline__ void rotate_regs(float (&u)[D]) {
 // row's D/2 code bytes, `scales` the D/32 scale bytes (little-endian).
 template <int D>
 __device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D / 8],
-                                              uint32_t& scales, float c = kFp4C) {
+                                              uint64_t& scales, float c = kFp4C) {
   scales = 0;
 #pragma unroll
   for (int g = 0; g < D / 32; ++g) {
@@ -83,7 +83,7 @@ __device__ __forceinline__ void quantize_regs(float (&y)[D], uint32_t (&codes)[D
                       (cvt_e2m1x2(e[4], e[5]) << 16) | (cvt_e2m1x2(e[6], e[7]) << 24);
       codes[4 * g + w] = byte == 0xFFu ? 0u : word;
     }
-    scales |= byte << (8 * g);
+    scales |= static_cast<uint64_t>(byte) << (8 * g);
   }
 }
 
@@ -150,7 +150,7 @@ __device__ __forceinline__ void quantize_tq_regs(const float (&y)[D], uint32_t (
 // natural order.
 template <int D, bool KPERM, bool TQ = false>
 __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_base, int64_t row,
-                                          const uint32_t (&codes)[D / 8], uint32_t scales) {
+                                          const uint32_t (&codes)[D / 8], uint64_t scales) {
   constexpr int NG = D / 32;
   uint32_t out[D / 8];
 #pragma unroll
@@ -161,7 +161,10 @@ __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_b
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) cdst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
   if (TQ || D == 128)  // TQ4: the fp32 norm; FP4: D/32 scale bytes
-    *reinterpret_cast<uint32_t*>(scales_base + row * 4) = scales;
+    *reinterpret_cast<uint32_t*>(scales_base + row * 4) = static_cast<uint32_t>(scales);
+  else if (D == 256)
+    *reinterpret_cast<uint2*>(scales_base + row * 8) =
+        make_uint2(static_cast<uint32_t>(scales), static_cast<uint32_t>(scales >> 32));
   else
     *reinterpret_cast<uint16_t*>(scales_base + row * 2) = static_cast<uint16_t>(scales);
 }
@@ -169,11 +172,15 @@ __device__ __forceinline__ void store_row(uint8_t* codes_base, uint8_t* scales_b
 // Quantiser stage of either format, then the store of the row.
 template <int D, bool TQ>
 __device__ __forceinline__ void quantize_store(float (&u)[D], const AppendParams& p, bool is_v, int64_t dst) {
-  uint32_t codes[D / 8], scales;
-  if (TQ)
-    quantize_tq_regs<D>(u, codes, scales, p.tq_tpos);
-  else
+  uint32_t codes[D / 8];
+  uint64_t scales;
+  if (TQ) {
+    uint32_t norm_bits;
+    quantize_tq_regs<D>(u, codes, norm_bits, p.tq_tpos);
+    scales = norm_bits;
+  } else {
     quantize_regs<D>(u, codes, scales, p.c);
+  }
   if (is_v)
     store_row<D, false, TQ>(p.vc, p.vs, dst, codes, scales);
   else
@@ -326,6 +333,91 @@ __global__ void __launch_bounds__(128) fp4_append_small_kernel(const void* k, co
   pdl_trigger();
 }
 
+// D = 256 (FP4): one warp per row of K or V, since a 256-element row is too
+// long for one thread's registers.  Lane l holds elements 8l .. 8l+7: the
+// butterfly strides 1, 2, 4 run inside the lane, 8 .. 128 across lanes
+// (partner l ^ (stride / 8)), each output with the same fp32 operations in the
+// same ascending order as the one-thread rotation; a 32-channel group is 4
+// lanes.  K rows keep the group-interleaved word order (word w of group g at
+// word position 8 w + g).
+template <bool F32>
+__global__ void __launch_bounds__(128) fp4_append_wide_kernel(const void* k, const void* v,
+                                                              const __grid_constant__ AppendParams p) {
+  constexpr int D = 256;
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = p.ntok * p.hkv;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= 2 * nrows) return;  // warp-uniform
+  const bool is_v = gw >= nrows;
+  const int64_t R = is_v ? gw - nrows : gw;
+  const int64_t t = R / p.hkv;
+  const int h = static_cast<int>(R - t * p.hkv);
+  const int64_t slot = p.slots[t];
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (lane == 0) record_error(p.status, kErrBounds);
+    return;
+  }
+  float u[8];
+  if (F32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(is_v ? v : k) + R * D + 8 * lane);
+    const float4 a = src[0], b = src[1];
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u[e] = __uint_as_float(__float_as_uint(x[e]) ^ p.sign.m[8 * lane + e]);
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(is_v ? v : k) + R * D + 8 * lane);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      u[2 * e] = __uint_as_float((ws[e] << 16) ^ p.sign.m[8 * lane + 2 * e]);
+      u[2 * e + 1] = __uint_as_float((ws[e] & 0xFFFF0000u) ^ p.sign.m[8 * lane + 2 * e + 1]);
+    }
+  }
+#pragma unroll
+  for (int hs = 1; hs < 8; hs <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & hs) == 0) {
+        const float a = u[i], b = u[i + hs];
+        u[i] = a + b;
+        u[i + hs] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float o = __shfl_xor_sync(kFull, u[e], m);
+      u[e] = upper ? (o - u[e]) : (u[e] + o);
+    }
+  }
+  const float sc = inv_sqrt_d<D>();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) u[e] *= sc;
+  // group absmax over the group's 4 lanes, scale byte, codes
+  float mx = max_abs_nan(u[0], u[1]);
+#pragma unroll
+  for (int e = 2; e < 8; ++e) mx = max_abs_nan(mx, u[e]);
+  mx = max_abs_nan(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = max_abs_nan(mx, __shfl_xor_sync(kFull, mx, 2));
+  const uint32_t byte = scale_byte(fabsf(mx), p.c);
+  const float inv = inv_scale(byte == 0xFFu ? 127u : byte);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) u[e] *= inv;
+  uint32_t word = cvt_e2m1x2(u[0], u[1]) | (cvt_e2m1x2(u[2], u[3]) << 8) | (cvt_e2m1x2(u[4], u[5]) << 16) |
+                  (cvt_e2m1x2(u[6], u[7]) << 24);
+  if (byte == 0xFFu) word = 0u;
+  const int64_t page = slot >> p.ps_log2;
+  const int64_t dst = ((page * p.hkv + h) << p.ps_log2) + (slot & ((1 << p.ps_log2) - 1));
+  const int g = lane >> 2, w = lane & 3;
+  uint32_t* crow = reinterpret_cast<uint32_t*>((is_v ? p.vc : p.kc) + dst * (D / 2));
+  crow[is_v ? lane : (D / 32) * w + g] = word;
+  if (w == 0) (is_v ? p.vs : p.ks)[dst * (D / 32) + g] = static_cast<uint8_t>(byte);
+  pdl_trigger();
+}
+
 // ------------------------------------------------------------ FP8 / BF16
 struct AnchorParams {
   const void* k;
@@ -422,7 +514,8 @@ __global__ void test_quantize_kernel(const float* y, int64_t n, uint8_t* codes, 
   float u[D];
 #pragma unroll
   for (int i = 0; i < D; ++i) u[i] = y[r * D + i];
-  uint32_t c[D / 8], s;
+  uint32_t c[D / 8];
+  uint64_t s;
   quantize_regs<D>(u, c, s);
   store_row<D, false>(codes, scales, r, c, s);
 }
@@ -607,6 +700,12 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
     for (int k = 0; k < 7; ++k) p.tq_tpos[k] = 0.f;
   }
   p.c = fp4_c(c);
+  if (c.head_dim == 256) {  // FP4 only: one warp per row, any size
+    if (tq) return UQ_ERR_UNSUPPORTED;
+    const unsigned grid = static_cast<unsigned>((2 * nrows + 3) / 4);
+    return cuda_status(in_fp32 ? launch_pdl(fp4_append_wide_kernel<true>, grid, 128, 0, s, k, v, p)
+                               : launch_pdl(fp4_append_wide_kernel<false>, grid, 128, 0, s, k, v, p));
+  }
   // kernel instance by (head_dim, input type, format)
   const int which = (c.head_dim == 128 ? 4 : 0) + (in_fp32 ? 2 : 0) + (tq ? 1 : 0);
   if (nrows <= kSmallAppendRows) {
@@ -668,7 +767,9 @@ uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, fl
   SignMasks sm;
   make_sign_masks(seed, d, &sm);
   const unsigned grid = (unsigned)((n + 127) / 128);
-  if (d == 128)
+  if (d == 256)
+    test_rotate_kernel<256><<<grid, 128, 0, s>>>(x, n, y, sm);
+  else if (d == 128)
     test_rotate_kernel<128><<<grid, 128, 0, s>>>(x, n, y, sm);
   else
     test_rotate_kernel<64><<<grid, 128, 0, s>>>(x, n, y, sm);
@@ -678,7 +779,9 @@ uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, fl
 uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s) {
   const unsigned grid = (unsigned)((n + 127) / 128);
-  if (d == 128)
+  if (d == 256)
+    test_quantize_kernel<256><<<grid, 128, 0, s>>>(y, n, codes, scales);
+  else if (d == 128)
     test_quantize_kernel<128><<<grid, 128, 0, s>>>(y, n, codes, scales);
   else
     test_quantize_kernel<64><<<grid, 128, 0, s>>>(y, n, codes, scales);

@@ -330,8 +330,21 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
   for (int u = 0; u < NU; ++u) {
     const uint8_t* skc = st[u];
     const uint8_t* sks = st[u] + 2 * C::KBYTES;
-    uint32_t kw0[NG], kw1[NG], ksw0, ksw1;
-    if (NG == 4) {
+    uint32_t kw0[NG], kw1[NG], ksw0, ksw1, ksw0b = 0u, ksw1b = 0u;  // scale bytes of groups 0-3 (b: 4-7)
+    if (NG == 8) {  // D = 256: word c of the 8 groups is 32 contiguous bytes
+      const uint4 a0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 32);
+      const uint4 b0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 32 + 16);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 32);
+      const uint4 b1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 32 + 16);
+      kw0[0] = a0.x; kw0[1] = a0.y; kw0[2 % NG] = a0.z; kw0[3 % NG] = a0.w;
+      kw0[4 % NG] = b0.x; kw0[5 % NG] = b0.y; kw0[6 % NG] = b0.z; kw0[7 % NG] = b0.w;
+      kw1[0] = a1.x; kw1[1] = a1.y; kw1[2 % NG] = a1.z; kw1[3 % NG] = a1.w;
+      kw1[4 % NG] = b1.x; kw1[5 % NG] = b1.y; kw1[6 % NG] = b1.z; kw1[7 % NG] = b1.w;
+      const uint2 s0 = *reinterpret_cast<const uint2*>(sks + r * 8);
+      const uint2 s1 = *reinterpret_cast<const uint2*>(sks + (r + 8) * 8);
+      ksw0 = s0.x; ksw0b = s0.y;
+      ksw1 = s1.x; ksw1b = s1.y;
+    } else if (NG == 4) {
       const uint4 x0 = *reinterpret_cast<const uint4*>(skc + r * C::KROW + c * 16);
       const uint4 x1 = *reinterpret_cast<const uint4*>(skc + (r + 8) * C::KROW + c * 16);
       kw0[0] = x0.x; kw0[1] = x0.y; kw0[2 % NG] = x0.z; kw0[3 % NG] = x0.w;
@@ -356,10 +369,11 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
       mma_f16_zc(acc, h0[0], h1[0], h0[1], h1[1], qb[2 * g][0], qb[2 * g][1]);
       mma_f16(acc, h0[2], h1[2], h0[3], h1[3], qb[2 * g + 1][0], qb[2 * g + 1][1]);
       float f0, f1;
-      if (g == 0) { f0 = scale_of<0>(ksw0); f1 = scale_of<0>(ksw1); }
-      else if (g == 1) { f0 = scale_of<1>(ksw0); f1 = scale_of<1>(ksw1); }
-      else if (g == 2) { f0 = scale_of<2>(ksw0); f1 = scale_of<2>(ksw1); }
-      else { f0 = scale_of<3>(ksw0); f1 = scale_of<3>(ksw1); }
+      const uint32_t sw0 = g < 4 ? ksw0 : ksw0b, sw1 = g < 4 ? ksw1 : ksw1b;
+      if ((g & 3) == 0) { f0 = scale_of<0>(sw0); f1 = scale_of<0>(sw1); }
+      else if ((g & 3) == 1) { f0 = scale_of<1>(sw0); f1 = scale_of<1>(sw1); }
+      else if ((g & 3) == 2) { f0 = scale_of<2>(sw0); f1 = scale_of<2>(sw1); }
+      else { f0 = scale_of<3>(sw0); f1 = scale_of<3>(sw1); }
       fma2(sa[0], sa[1], acc[0], acc[1], f0);
       fma2(sa[2], sa[3], acc[2], acc[3], f1);
     }
@@ -368,9 +382,9 @@ __device__ __forceinline__ void units_fp4(const uint8_t* const (&st)[NU], int nv
       const bool v0 = r < nvalid_last, v1 = r + 8 < nvalid_last;
       if (!v0) { t[u][0] = -INFINITY; t[u][1] = -INFINITY; }
       if (!v1) { t[u][2] = -INFINITY; t[u][3] = -INFINITY; }
-      kbad |= (v0 ? has_ff(ksw0) : 0u) | (v1 ? has_ff(ksw1) : 0u);
+      kbad |= (v0 ? has_ff(ksw0) | has_ff(ksw0b) : 0u) | (v1 ? has_ff(ksw1) | has_ff(ksw1b) : 0u);
     } else {
-      kbad |= has_ff(ksw0) | has_ff(ksw1);
+      kbad |= has_ff(ksw0) | has_ff(ksw1) | has_ff(ksw0b) | has_ff(ksw1b);
     }
   }
 
@@ -859,7 +873,8 @@ __device__ __forceinline__ void patch_stage(const uint8_t* scratch, uint8_t* st,
 }
 
 template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) : (packed4(KIND) ? UQ_FP4_MINB : 4))
+    decode_kernel(const __grid_constant__ DecParams p) {
   using C = DC<KIND, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -938,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
       const int hloc = hblk * kHB + r;
       const bool hv = hloc < p.G;
       const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (hv ? hloc : 0)) * D;
-      if (KIND == kFP4) {
+      if constexpr (KIND == kFP4) {
         // Rotate and round on the quad, then regroup through this warp's slice
         // of the combine buffer: thread c needs bytes 32g + 8c .. +7 of its
         // head for every group g (the fragment order of the QK^T loop).
@@ -957,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
           qb[2 * g + 1][1] = e4m3x2_to_f16x2(w.y >> 16);
         }
         __syncwarp();
-      } else if (KIND == kTQ4) {
+      } else if constexpr (KIND == kTQ4) {
         // Rotate on the quad, round to f16 (nearest even), regroup through
         // the warp's slice of the combine buffer: thread c needs channels
         // 32g + 8c .. +7 of its head for every group g.
@@ -1061,8 +1076,10 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
     // query bytes, which is free until the combine.
     int fa_unit = -1;  // index of the unit whose stage takes the scratch row
     uint8_t* fa_scratch = reinterpret_cast<uint8_t*>(comb_o + warp * kHB * D) + kHB * D;
-    if (KIND == kFP4 && p.new_slots != nullptr && nw > 0 && j0 + warp + (nw - 1) * kWarps == nb - 1)
-      if (fused_append<D>(p, fa_scratch, b, kvh, L, bt_row, lane)) fa_unit = nw - 1;
+    if constexpr (KIND == kFP4 && D <= 128) {  // the fused append (FP4, head dims 64 and 128)
+      if (p.new_slots != nullptr && nw > 0 && j0 + warp + (nw - 1) * kWarps == nb - 1)
+        if (fused_append<D>(p, fa_scratch, b, kvh, L, bt_row, lane)) fa_unit = nw - 1;
+    }
 
     WarpState<C::NMMA> S;
     S.M0 = S.M1 = -INFINITY;
@@ -1090,14 +1107,17 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
         it += nw - i;
         break;
       }
-      if (KIND == kFP4 && fa_unit >= 0 && fa_unit - i < nu) {
-        patch_stage<D>(fa_scratch, myring + ((it + fa_unit - i) % C::NST) * C::STAGE, (L - 1) & (kChunk - 1), lane);
-        fa_unit = -1;
-        __syncwarp();
+      if constexpr (KIND == kFP4 && D <= 128) {
+        if (fa_unit >= 0 && fa_unit - i < nu) {
+          patch_stage<D>(fa_scratch, myring + ((it + fa_unit - i) % C::NST) * C::STAGE, (L - 1) & (kChunk - 1),
+                         lane);
+          fa_unit = -1;
+          __syncwarp();
+        }
       }
       const uint8_t* st0 = myring + (it % C::NST) * C::STAGE;
       const int nvalid = L - (ub + j0 + warp + (i + nu - 1) * kWarps) * kChunk;  // of the last unit taken
-      if (KIND == kFP4) {
+      if constexpr (KIND == kFP4) {
         if (nu == 2) {
           const uint8_t* const sts[2] = {st0, myring + ((it + 1) % C::NST) * C::STAGE};
           if (nvalid >= kChunk) units_fp4<D, 2, false>(sts, kChunk, r, c, qb, fac, S);
@@ -1107,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, packed4(KIND) ? UQ_FP4_MINB : 4) dec
           if (nvalid >= kChunk) units_fp4<D, 1, false>(sts, kChunk, r, c, qb, fac, S);
           else units_fp4<D, 1, true>(sts, nvalid, r, c, qb, fac, S);
         }
-      } else if (KIND == kTQ4) {
+      } else if constexpr (KIND == kTQ4) {
         if (nu == 2) {
           const uint8_t* const sts[2] = {st0, myring + ((it + 1) % C::NST) * C::STAGE};
           if (nvalid >= kChunk) units_tq<D, 2, false>(sts, kChunk, r, c, qb, fac, lut, S);
@@ -1562,12 +1582,16 @@ uq_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const int d = c.head_dim;
   switch (c.dtype) {
     case UQ_FP4_UE8M0:
+      if (d == 256) return a.new_slots ? UQ_ERR_UNSUPPORTED : run_decode<kFP4, 256>(a, nhb, s);
       return d == 128 ? run_decode<kFP4, 128>(a, nhb, s) : run_decode<kFP4, 64>(a, nhb, s);
     case UQ_FP8_E4M3:
+      if (d == 256) return run_decode<kFP8, 256>(a, nhb, s);
       return d == 128 ? run_decode<kFP8, 128>(a, nhb, s) : run_decode<kFP8, 64>(a, nhb, s);
     case UQ_TQ4:
+      if (d == 256) return UQ_ERR_UNSUPPORTED;
       return d == 128 ? run_decode<kTQ4, 128>(a, nhb, s) : run_decode<kTQ4, 64>(a, nhb, s);
     default:
+      if (d == 256) return run_decode<kBF16, 256>(a, nhb, s);
       return d == 128 ? run_decode<kBF16, 128>(a, nhb, s) : run_decode<kBF16, 64>(a, nhb, s);
   }
 }
@@ -1577,7 +1601,9 @@ uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, 
   make_sign_masks(seed, d, &sm);
   const int64_t warps = (n + 7) / 8;
   const unsigned grid = (unsigned)((warps + 3) / 4);
-  if (d == 128)
+  if (d == 256)
+    test_query_kernel<256><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+  else if (d == 128)
     test_query_kernel<128><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
   else
     test_query_kernel<64><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);

@@ -23,8 +23,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // fl32(1/sqrt(d)) for the supported head dims.
 template <int D>
 __device__ __forceinline__ float inv_sqrt_d() {
-  static_assert(D == 64 || D == 128, "head_dim");
-  return D == 64 ? __uint_as_float(0x3E000000u) : __uint_as_float(0x3DB504F3u);
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+  return D == 64 ? __uint_as_float(0x3E000000u) : D == 128 ? __uint_as_float(0x3DB504F3u) : __uint_as_float(0x3D800000u);
 }
 
 // (a, b) <- (a + b, a - b) on two lanes: (a0, b0) and (a1, b1).

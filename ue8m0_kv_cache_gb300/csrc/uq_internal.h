@@ -15,7 +15,7 @@ namespace uqh {
 // Per-element XOR masks of the rotation's sign diagonal (0 or 0x80000000),
 // passed to kernels by value so that the library keeps no device state.
 struct SignMasks {
-  uint32_t m[128];
+  uint32_t m[256];
 };
 void make_sign_masks(uint64_t seed, int d, SignMasks* out);
 
