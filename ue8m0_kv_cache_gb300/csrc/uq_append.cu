@@ -33,6 +33,7 @@ namespace {
 using namespace uqd;
 
 constexpr int kRows = 64;             // token-head rows per tile
+constexpr int kAppendStages = 2;      // tiles in the ring of the tiled kernel (all but one in flight)
 constexpr int64_t kSmallAppendRows = 1024;  // token-head rows up to which the direct-load kernel is used
 constexpr int kAppendThreads = 2 * kRows;  // one thread per K row and one per V row
 
@@ -198,8 +199,9 @@ __global__ void __launch_bounds__(kAppendThreads)
   constexpr int TILEB = kRows * ROWB;    // one tensor, one stage
   constexpr int STAGEB = 2 * TILEB;      // K + V
 
+  constexpr int NS = kAppendStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[2];
+  __shared__ uint64_t bars[NS];
   __shared__ int abort_flag;
   // The 128-byte swizzle pattern repeats every 1024 bytes: align the ring.
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -209,8 +211,7 @@ __global__ void __launch_bounds__(kAppendThreads)
   const int64_t nrows = p.ntok * p.hkv;
   const int64_t ntiles = (nrows + kRows - 1) / kRows;
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     abort_flag = 0;
   }
@@ -231,12 +232,15 @@ __global__ void __launch_bounds__(kAppendThreads)
   const int row = tid & (kRows - 1);
   int64_t tile = blockIdx.x;
   uint32_t it = 0;
-  if (tid == 0 && tile < ntiles) issue(tile, 0);
+  if (tid == 0)
+    for (int s = 0; s < NS - 1; ++s)
+      if (tile + static_cast<int64_t>(s) * gridDim.x < ntiles) issue(tile + static_cast<int64_t>(s) * gridDim.x, s);
   for (; tile < ntiles; tile += gridDim.x, ++it) {
-    const int stage = it & 1;
-    const int64_t next = tile + gridDim.x;
-    if (tid == 0 && next < ntiles) issue(next, stage ^ 1);
-    const bool ok = mbar_wait(&bars[stage], (it >> 1) & 1, kWaitBudget);
+    const int stage = it % NS;
+    // the stage of the previous iteration is free again: it takes the tile NS - 1 ahead
+    const int64_t ahead = tile + static_cast<int64_t>(NS - 1) * gridDim.x;
+    if (tid == 0 && ahead < ntiles) issue(ahead, (it + NS - 1) % NS);
+    const bool ok = mbar_wait(&bars[stage], (it / NS) & 1, kWaitBudget);
     const int64_t R = tile * kRows + row;
     if (!ok) {
       record_error(p.status, kErrTimeout);
@@ -275,10 +279,10 @@ __global__ void __launch_bounds__(kAppendThreads)
     __syncthreads();
     if (abort_flag) {
       // Let copies that may still be in flight land before the block exits.
-      if (tid == 0) {
-        mbar_wait(&bars[stage], (it >> 1) & 1, kWaitBudget);
-        if (next < ntiles) mbar_wait(&bars[stage ^ 1], ((it + 1) >> 1) & 1, kWaitBudget);
-      }
+      if (tid == 0)
+        for (int k = 0; k < NS; ++k)
+          if (blockIdx.x + static_cast<int64_t>(it + k) * gridDim.x < ntiles)
+            mbar_wait(&bars[(it + k) % NS], ((it + k) / NS) & 1, kWaitBudget);
       break;
     }
   }
@@ -643,7 +647,7 @@ template <int D, bool F32, bool TQ>
 uq_status run_fp4_append(const CUtensorMap& mk, const CUtensorMap& mv, const AppendParams& p, int64_t nrows,
                          cudaStream_t s) {
   constexpr int STAGEB = 2 * kRows * D * (F32 ? 4 : 2);
-  constexpr size_t smem = 2 * STAGEB + 1024;
+  constexpr size_t smem = kAppendStages * STAGEB + 1024;
   auto kern = fp4_append_kernel<D, F32, TQ>;
   // The shared-memory attribute is per device and kernel: set once per device, with the
   // blocks per SM it allows (host threads may call concurrently).
