@@ -1294,84 +1294,119 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
       }
     }
     const int64_t U = *p.ws_units;
-    // The partials of this row are slots first..last (those with an empty
-    // unit range wrote nothing).  Their (m, l) are read lane-parallel, 32 at a
-    // time; the O rows are then summed in slot order, four loads in flight.
-    float Ms = -INFINITY;
-    for (int base = first; base <= last; base += 32) {
-      const int s = base + lane;
+    float Ms = -INFINITY, Ls = 0.f;
+    if (pitem < 0 && last >= first && last - first < 8) {
+      // Up to 8 partials (the usual case): one round of loads -- lane j's (m, l) of
+      // slot first + j and every lane's channels of all the slots' O rows -- then
+      // the same weights and the same slot-order sums as the general path below.
+      const int s = first + lane;
       int64_t lo = 0, hi = 0;
       if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
-      if (lo < hi) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
-    }
-    // The decode's partials carry p * 2^kPShift against their maximum, the shared-prefix
-    // kernel's plain p: its maxima enter the merge raised by kPShift.
-    if (pitem >= 0)
-      for (int s = lane; s < p.px_splits; s += 32)
-        Ms = fmaxf(Ms, p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
-    float Ls = 0.f;
-    for (int base = first; base <= last; base += 32) {
-      const int s = base + lane;
-      int64_t lo = 0, hi = 0;
-      if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
-      float w = 0.f;
+      const unsigned valid = __ballot_sync(kFull, lo < hi);
+      float m = -INFINITY, lv = 0.f;
       if (lo < hi) {
         const int64_t id = (int64_t)(s + pair) * kHB + hh;
-        w = ex2(p.ws_ml[id * 2] - Ms);
-        Ls += w * p.ws_ml[id * 2 + 1];
+        m = p.ws_ml[id * 2];
+        lv = p.ws_ml[id * 2 + 1];
       }
-      const unsigned valid = __ballot_sync(kFull, lo < hi);
-      const int n = last - base + 1 < 32 ? last - base + 1 : 32;
-      int j = 0;
-      for (; j + 4 <= n; j += 4) {
-        VecF<EPL> v[4];
-        float wj[4];
+      VecF<EPL> v[8];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          wj[t] = __shfl_sync(kFull, w, j + t);
-          if ((valid >> (j + t)) & 1u)
-            v[t] = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + t + pair) * kHB + hh) * D + lane * EPL);
-          else
-            v[t] = VecF<EPL>{};
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) o[e] += wj[t] * v[t].x[e];
+      for (int t = 0; t < 8; ++t) {
+        if ((valid >> t) & 1u)
+          v[t] = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(first + t + pair) * kHB + hh) * D + lane * EPL);
+        else
+          v[t] = VecF<EPL>{};
       }
-      for (; j < n; ++j) {
-        const float wj = __shfl_sync(kFull, w, j);
-        if ((valid >> j) & 1u) {
-          const VecF<EPL> v = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + pair) * kHB + hh) * D + lane * EPL);
+      Ms = m;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
-        }
+      for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
+      const float w = (lo < hi) ? ex2(m - Ms) : 0.f;
+      Ls = w * lv;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float wt = __shfl_sync(kFull, w, t);
+        if ((valid >> t) & 1u)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[e] += wt * v[t].x[e];
       }
-    }
-    if (pitem >= 0) {  // the shared-prefix splits; an empty split (m = -inf) wrote no O row
-      for (int s0 = 0; s0 < p.px_splits; s0 += 32) {
-        const int s = s0 + lane;
+    } else {
+      // The partials of this row are slots first..last (those with an empty
+      // unit range wrote nothing).  Their (m, l) are read lane-parallel, 32 at a
+      // time; the O rows are then summed in slot order, four loads in flight.
+      for (int base = first; base <= last; base += 32) {
+        const int s = base + lane;
+        int64_t lo = 0, hi = 0;
+        if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
+        if (lo < hi) Ms = fmaxf(Ms, p.ws_ml[((int64_t)(s + pair) * kHB + hh) * 2]);
+      }
+      // The decode's partials carry p * 2^kPShift against their maximum, the shared-prefix
+      // kernel's plain p: its maxima enter the merge raised by kPShift.
+      if (pitem >= 0)
+        for (int s = lane; s < p.px_splits; s += 32)
+          Ms = fmaxf(Ms, p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift);
+#pragma unroll
+      for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
+      for (int base = first; base <= last; base += 32) {
+        const int s = base + lane;
+        int64_t lo = 0, hi = 0;
+        if (s <= last) block_range(s, U, p.num_ctas, lo, hi);
         float w = 0.f;
-        bool live = false;
-        if (s < p.px_splits) {
-          const float m = p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift;
-          live = m != -INFINITY;
-          if (live) {
-            w = ex2(m - Ms);
-            Ls += w * p.px_ml[((pitem + s) * p.px_rows + prr) * 2 + 1];
-          }
+        if (lo < hi) {
+          const int64_t id = (int64_t)(s + pair) * kHB + hh;
+          w = ex2(p.ws_ml[id * 2] - Ms);
+          Ls += w * p.ws_ml[id * 2 + 1];
         }
-        const unsigned mask = __ballot_sync(kFull, live);
-        const int cnt = min(32, p.px_splits - s0);
-        for (int j = 0; j < cnt; ++j) {
+        const unsigned valid = __ballot_sync(kFull, lo < hi);
+        const int n = last - base + 1 < 32 ? last - base + 1 : 32;
+        int j = 0;
+        for (; j + 4 <= n; j += 4) {
+          VecF<EPL> v[4];
+          float wj[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            wj[t] = __shfl_sync(kFull, w, j + t);
+            if ((valid >> (j + t)) & 1u)
+              v[t] = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + t + pair) * kHB + hh) * D + lane * EPL);
+            else
+              v[t] = VecF<EPL>{};
+          }
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] += wj[t] * v[t].x[e];
+        }
+        for (; j < n; ++j) {
           const float wj = __shfl_sync(kFull, w, j);
-          if ((mask >> j) & 1u) {
-            const VecF<EPL> v =
-                *reinterpret_cast<const VecF<EPL>*>(p.px_o + ((pitem + s0 + j) * p.px_rows + prr) * D + lane * EPL);
+          if ((valid >> j) & 1u) {
+            const VecF<EPL> v = *reinterpret_cast<const VecF<EPL>*>(p.ws_o + ((int64_t)(base + j + pair) * kHB + hh) * D + lane * EPL);
 #pragma unroll
             for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
+          }
+        }
+      }
+      if (pitem >= 0) {  // the shared-prefix splits; an empty split (m = -inf) wrote no O row
+        for (int s0 = 0; s0 < p.px_splits; s0 += 32) {
+          const int s = s0 + lane;
+          float w = 0.f;
+          bool live = false;
+          if (s < p.px_splits) {
+            const float m = p.px_ml[((pitem + s) * p.px_rows + prr) * 2] + kPShift;
+            live = m != -INFINITY;
+            if (live) {
+              w = ex2(m - Ms);
+              Ls += w * p.px_ml[((pitem + s) * p.px_rows + prr) * 2 + 1];
+            }
+          }
+          const unsigned mask = __ballot_sync(kFull, live);
+          const int cnt = min(32, p.px_splits - s0);
+          for (int j = 0; j < cnt; ++j) {
+            const float wj = __shfl_sync(kFull, w, j);
+            if ((mask >> j) & 1u) {
+              const VecF<EPL> v =
+                  *reinterpret_cast<const VecF<EPL>*>(p.px_o + ((pitem + s0 + j) * p.px_rows + prr) * D + lane * EPL);
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) o[e] += wj * v.x[e];
+            }
           }
         }
       }
