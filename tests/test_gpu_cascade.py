@@ -121,3 +121,19 @@ def test_nan_in_shared_prefix_poisons_the_group():
     got, st = _cascade(w, cache, w.q(), [0, 2], [2048], 2048)
     assert st == 0
     assert np.all(np.isnan(got))  # seq 2 is in no group but its table shares the poisoned page too
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_full_size_prefix128k_sampled(B):
+    """The bench's cascade workload: 131072-token sequences sharing their first 98304 tokens;
+    every sequence through the shared-prefix kernel (min_rows 0); sampled sequences against
+    the oracle."""
+    base = workloads.make("prefix128k")
+    w = workloads.make("prefix128k", B=B, seq_lens=[base.seq_lens[0]] * B)
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    q = w.q()
+    got, st = _cascade(w, cache, q, [0, B], [w.shared_prefix], w.shared_prefix)
+    assert st == 0
+    seqs = [0, B - 1]
+    assert_close(got[seqs], _ref(w, seqs, q), "prefix128k B=%d" % B)

@@ -121,3 +121,21 @@ def test_anchor_cache_is_unsupported():
     c = new_cache(w, uq.FP8_E4M3)
     with pytest.raises(uq.UqError):
         _run(w, c, _queries(w, [4], 62), [4])
+
+
+def test_full_size_sampled():
+    """The bench's prefill: 8 sequences of 64K context, the last 128 tokens of each as the
+    chunk; sampled query tokens of two sequences against the oracle."""
+    B, L, n = 8, 65536, 128
+    w = workloads.make("gqa8k", B=B, seq_lens=[L] * B, seed=70)
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    q = _queries(w, [n] * B, 71)
+    got = _run(w, cache, q, [n] * B)
+    qb = bits(q)
+    for b in (2, 7):
+        oc, bt, lens = oracle_for(w, [b])
+        for i in (0, 77, 127):
+            t = b * n + i
+            ref = oc.decode(qb[t:t + 1], bt, np.array([L - n + i + 1], np.int32))[0]
+            assert_close(got[t][None], ref[None], "seq %d token %d" % (b, i))
