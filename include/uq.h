@@ -315,7 +315,8 @@ uq_status uq_calibrate_c(const void* x, int32_t in_dtype, int64_t n_vec, int32_t
  *               query rows (sequences x num_q_heads / num_kv_heads); smaller
  *               groups run as a plain decode.  The shared-prefix kernel
  *               (tensor-core tiles of 128 query rows) is faster than the decode
- *               from about 64 rows.
+ *               from about 128 rows (measured at 98304 shared of 131072 keys:
+ *               0.91x the plain decode's speed at 64 rows, 1.45x at 128).
  * Work split: group g's first S_g = floor(min(prefix_lens[g], max_prefix_len,
  * max_pages_per_seq * page_size) / 16) * 16 keys go to the shared-prefix kernel
  * (all the group's queries at once); keys S_g .. seq_lens[b]-1 of each sequence

@@ -282,7 +282,7 @@ def uq_cascade_workspace_bytes(batch: int, num_groups: int, num_q_heads: int, nu
                                                max_prefix_len))
 
 
-def uq_cascade_decode_attention(q, cache, block_table, seq_lens, cu_seqs, prefix_lens, max_prefix_len, min_rows=64,
+def uq_cascade_decode_attention(q, cache, block_table, seq_lens, cu_seqs, prefix_lens, max_prefix_len, min_rows=128,
                                 out=None, workspace=None, sm_scale=0.0, stream=None):
     """Cascade decode: q [B][Hq][D] bf16; group g = sequences cu_seqs[g]..cu_seqs[g+1]-1 (int32 [G+1]) whose first
     prefix_lens[g] keys (int32 [G]) are the same pages; returns fp32 [B][Hq][D], equal to uq_decode_attention."""
