@@ -25,13 +25,14 @@
 //     tensor memory; every thread reads its row of S, applies the key factors,
 //     the causal mask and the online softmax, and writes P back to tensor
 //     memory as hi and lo f16 parts; one thread issues O_win += P V' with A
-//     from tensor memory.  O_win sums a window of up to four tiles under one
+//     from tensor memory.  O_win sums a window of up to sixteen tiles under one
 //     reference (running max, RV) and is then added to the row's fp32 O in
 //     registers with IEEE rounding, as the decode adds its per-unit partials.
 //   * Long key ranges are split over CTAs; each (row tile, key split) writes a
 //     partial (m, l, O) and a merge kernel combines them by log-sum-exp and
 //     applies the inverse rotation.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 
 #include "uq_device.cuh"
@@ -42,6 +43,8 @@ namespace {
 using namespace uqd;
 
 constexpr int kPThreads = 128;  // 4 warps: one query row per thread
+constexpr int kTileKeys = 64;   // keys per tile; key splits are whole tiles
+constexpr int kItemCost = 3;    // per-item cost in key tiles, for the split choice (fitted to measured times)
 
 struct PrefillParams {
   const uint8_t* qbytes;     // rotated E4M3 query, [T][Hq][D]
@@ -54,12 +57,10 @@ struct PrefillParams {
   const uint8_t* vc;
   const uint8_t* vs;
   int B, T, Hq, Hkv, G, ps_log2, num_pages;
-  int splits;                // key splits per row tile
-  int kchunk;                // keys per split (multiple of the key tile)
   float sl2e;                // softmax scale * log2(e)
   float* ws_ml;              // partials: [items][128 rows][2]
   float* ws_o;               // partials: [items][128 rows][D]
-  int32_t* item_pre;         // [B + 1] prefix sums of work items per sequence
+  int32_t* item_pre;         // [B + 1] prefix sums of work items per sequence, then S and keys per split
   int64_t max_items;
   unsigned int* status;
   // Cascade mode: "sequence" b is group b, its queries are the decode queries of
@@ -84,13 +85,66 @@ __device__ __forceinline__ int row_tiles(int n, int G, int rows) { return (n * G
 namespace {
 
 // Work items: for every sequence b, kv head, row tile and key split one item,
-// in that order; item_pre[b] counts the items of sequences before b.
+// in that order; item_pre[b] counts the items of sequences before b, and
+// item_pre[B + 1], item_pre[B + 2] receive the split count S and the keys per
+// split.  Both come from the key ranges actually present (the longest one,
+// Lmax), not from the block table's capacity: kchunk = ceil(Lmax / 64 / S) key
+// tiles.  With fixed_splits > 0 (cascade: the decode's merge reads the same S)
+// S is that; otherwise S in [1, max_splits] minimises the estimated time of
+// the busiest CTA under the grid-stride order of the items,
+// ceil(items(S) / ctas) * (tiles per split + kItemCost), kItemCost the
+// per-item cost in key tiles (query staging, pipeline fill, and the 66 KB
+// partial that this kernel writes and the merge reads back).
 // Cascade mode (prefix != nullptr): a group whose shared keys are 0 has no items.
-__global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, int splits, int rows,
-                                    const int32_t* prefix, int min_rows, int cap, int32_t* item_pre) {
+__global__ void prefill_plan_kernel(const int32_t* cu_q, const int32_t* keys, int B, int G, int Hkv, int max_splits,
+                                    int fixed_splits, int rows, const int32_t* prefix, int min_rows, int cap,
+                                    int ctas, int32_t* item_pre) {
   const int lane = threadIdx.x;
+  // pass 1: row-tile units and the longest key range
+  long long units = 0;
+  int lmax = 0;
+  for (int b = lane; b < B; b += 32) {
+    const int n = max(0, cu_q[b + 1] - cu_q[b]);
+    int L;
+    if (prefix != nullptr) {
+      L = casc_shared_keys(n, G, prefix[b], min_rows, cap);
+    } else {
+      L = keys[b];
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+    }
+    if (prefix == nullptr || L > 0) units += static_cast<long long>(Hkv) * row_tiles(n, G, rows);
+    lmax = max(lmax, L);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    units += __shfl_xor_sync(kFull, units, o);
+    lmax = max(lmax, __shfl_xor_sync(kFull, lmax, o));
+  }
+  const int kt = max(1, (lmax + kTileKeys - 1) / kTileKeys);
+  int splits = fixed_splits;
+  if (splits < 1) {
+    const int smax = max(1, min(min(max_splits, kt), 0xFFFFF));
+    long long best = LLONG_MAX;  // (cost << 20) | S: ties go to the smaller S
+    for (int s0 = 1; s0 <= smax; s0 += 32) {
+      const int S = s0 + lane;
+      if (S <= smax) {
+        const long long waves = (units * S + ctas - 1) / ctas;
+        const long long key = ((waves * ((kt + S - 1) / S + kItemCost)) << 20) | S;
+        best = min(best, key);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(kFull, best, o));
+    splits = static_cast<int>(best & 0xFFFFF);
+  }
+  const int kchunk = (kt + splits - 1) / splits * kTileKeys;
+  // pass 2: prefix sums of the items
   int run = 0;
-  if (lane == 0) item_pre[0] = 0;
+  if (lane == 0) {
+    item_pre[0] = 0;
+    item_pre[B + 1] = splits;
+    item_pre[B + 2] = kchunk;
+  }
   for (int b0 = 0; b0 < B; b0 += 32) {
     const int b = b0 + lane;
     int x = 0;
@@ -111,9 +165,9 @@ __global__ void prefill_plan_kernel(const int32_t* cu_q, int B, int G, int Hkv, 
 
 // ------------------------------------------------------------ tensor-memory (tcgen05) kernel
 constexpr int kTRows = 128;     // query rows per CTA
-constexpr int kTKT = 64;        // keys per tile
+constexpr int kTKT = kTileKeys; // keys per tile
 constexpr int kTNST = 3;        // raw stages
-constexpr int kTWin = 4;        // tiles per O window
+constexpr int kTWin = 16;       // tiles per O window
 constexpr int kTCols = 256;     // tensor memory columns: S [0,64), P hi [64,96), P lo [96,128), O_win [128,256)
 constexpr float kTSlack = 8.f;  // running max raised only when a logit exceeds it by more than this (log2)
 
@@ -251,7 +305,8 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
   pdl_wait();
   int64_t total = p.item_pre[p.B];
-  if (total > p.max_items) {
+  const int splits = p.item_pre[p.B + 1], kchunk = p.item_pre[p.B + 2];
+  if (total > p.max_items || splits < 1 || kchunk < kTKT) {
     if (blockIdx.x == 0 && tid == 0) record_error(p.status, kErrBounds);
     total = 0;
   }
@@ -284,14 +339,14 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     const int ctx = p.cascade ? 0 : L - n;
     const int tiles_b = row_tiles(n_plan, p.G, kTRows);
     const int64_t local = item - p.item_pre[b];
-    const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * p.splits));
-    const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * p.splits);
-    const int rtile = rem / p.splits, split = rem - rtile * p.splits;
+    const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * splits));
+    const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * splits);
+    const int rtile = rem / splits, split = rem - rtile * splits;
     const int row0 = rtile * kTRows, nrows = n * p.G;
     const int last_row = min(row0 + kTRows, nrows) - 1;
     const int pos_max = p.cascade ? L - 1 : ctx + last_row / p.G;
-    const int k_lo = split * p.kchunk;
-    const int k_hi = min(k_lo + p.kchunk, pos_max + 1);
+    const int k_lo = split * kchunk;
+    const int k_hi = min(k_lo + kchunk, pos_max + 1);
     const int my_row = row0 + tid;
     const int pos = my_row < nrows ? (p.cascade ? L - 1 : ctx + my_row / p.G) : -1;
     const int pos_lo = p.cascade ? L - 1 : ctx + row0 / p.G;  // the smallest position of the item's rows
@@ -608,7 +663,7 @@ struct PrefillMergeParams {
   const int32_t* item_pre;
   const int32_t* cu_q;
   const int32_t* seq_lens;
-  int B, T, Hq, G, splits, cap, rows;
+  int B, T, Hq, G, cap, rows;
   int64_t max_items;
   float* out;
   uqh::SignMasks sign;
@@ -635,7 +690,8 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
   int L = p.seq_lens[b], n = n_plan;
   L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
   n = n > L ? L : n;
-  if (q0 < 0 || q0 + n > p.T || p.item_pre[p.B] > p.max_items) n = 0;
+  const int splits = p.item_pre[p.B + 1];
+  if (q0 < 0 || q0 + n > p.T || p.item_pre[p.B] > p.max_items || splits < 1) n = 0;
   const int i = t - q0;
   float o[EPL];
 #pragma unroll
@@ -643,20 +699,20 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
   if (i >= 0 && i < n) {
     const int kvh = h / p.G, hl = h - kvh * p.G;
     const int rowi = i * p.G + hl, rtile = rowi / p.rows, rr = rowi - rtile * p.rows;
-    const int64_t item0 = p.item_pre[b] + (static_cast<int64_t>(kvh) * row_tiles(n_plan, p.G, p.rows) + rtile) * p.splits;
+    const int64_t item0 = p.item_pre[b] + (static_cast<int64_t>(kvh) * row_tiles(n_plan, p.G, p.rows) + rtile) * splits;
     float Ms = -INFINITY;
-    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+    for (int s0 = 0; s0 < splits; s0 += 32) {
       const int s = s0 + lane;
-      if (s < p.splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * p.rows + rr) * 2]);
+      if (s < splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * p.rows + rr) * 2]);
     }
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
     float Ls = 0.f;
-    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+    for (int s0 = 0; s0 < splits; s0 += 32) {
       const int s = s0 + lane;
       float w = 0.f;
       bool live = false;
-      if (s < p.splits) {
+      if (s < splits) {
         const float m = p.ws_ml[((item0 + s) * p.rows + rr) * 2];
         live = m != -INFINITY;  // an empty split wrote no output row
         if (live) {
@@ -665,7 +721,7 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
         }
       }
       const unsigned mask = __ballot_sync(kFull, live);
-      const int cnt = min(32, p.splits - s0);
+      const int cnt = min(32, splits - s0);
       for (int j = 0; j < cnt; ++j) {
         const float wj = __shfl_sync(kFull, w, j);
         if ((mask >> j) & 1u) {
@@ -714,24 +770,29 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace bound of one launch.  The split count itself is chosen on the
+// device from the key ranges present (prefill_plan_kernel); the host fixes its
+// largest value, `splits`: the count that gives two waves of two blocks per SM
+// at the bound on row tiles, times four for the prefill (room for the device's
+// choice), as is for the cascade prefix (the decode's merge reads that count).
 struct PrefillPlan {
-  int splits, kchunk;
+  int splits;
   int64_t max_items;
   size_t off_pre, off_q, off_ml, off_o, total;
 };
 
-PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int sms, int rows) {
+PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int sms, int rows, bool fixed) {
   PrefillPlan pl;
   const int G = hq / hkv;
   const int64_t tiles = (static_cast<int64_t>(T) * G + rows - 1) / rows + B;  // bound on row tiles per kv head
   const int64_t base = static_cast<int64_t>(hkv) * tiles;
   const int64_t target = 2LL * 2 * sms;  // two waves of two blocks per SM
   const int max_splits = std::max(1, (max_keys + kTKT - 1) / kTKT);
-  pl.splits = static_cast<int>(std::min<int64_t>(max_splits, std::max<int64_t>(1, (target + base - 1) / base)));
-  pl.kchunk = ((max_keys + pl.splits - 1) / pl.splits + kTKT - 1) / kTKT * kTKT;
+  const int64_t s0 = std::max<int64_t>(1, (target + base - 1) / base);
+  pl.splits = static_cast<int>(std::min<int64_t>(max_splits, fixed ? s0 : 4 * s0));
   pl.max_items = base * pl.splits;
   pl.off_pre = 256;
-  pl.off_q = pl.off_pre + align256(static_cast<size_t>(B + 1) * 4);
+  pl.off_q = pl.off_pre + align256(static_cast<size_t>(B + 3) * 4);
   pl.off_ml = pl.off_q + align256(static_cast<size_t>(T) * hq * d);
   pl.off_o = pl.off_ml + align256(static_cast<size_t>(pl.max_items) * rows * 2 * 4);
   pl.total = pl.off_o + static_cast<size_t>(pl.max_items) * rows * d * 4;
@@ -784,8 +845,6 @@ PrefillParams base_params(const uq_cache& c, const int32_t* block_table, int max
   p.G = hq / c.num_kv_heads;
   p.ps_log2 = uqh::ilog2(c.page_size);
   p.num_pages = c.num_pages;
-  p.splits = pl.splits;
-  p.kchunk = pl.kchunk;
   const float sm = sm_scale > 0.f ? sm_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   p.sl2e = sm * 1.4426950408889634f;
   p.ws_ml = reinterpret_cast<float*>(ws + pl.off_ml);
@@ -799,35 +858,44 @@ PrefillParams base_params(const uq_cache& c, const int32_t* block_table, int max
   return p;
 }
 
+// CTAs of the item kernel's grid (0 on failure).
 template <int D>
-uq_status launch_items(const PrefillParams& p, const PrefillPlan& pl, cudaStream_t s) {
+int item_grid(const PrefillPlan& pl) {
   const int per_sm = prefill_ctas_per_sm<D>();
-  if (per_sm < 1) return UQ_ERR_CUDA;
-  const int64_t grid = std::min<int64_t>(pl.max_items, static_cast<int64_t>(uqh::dev_info().sms) * per_sm);
-  return uqh::cuda_status(uqh::launch_pdl(prefill_tc_kernel<D>, static_cast<unsigned>(std::max<int64_t>(grid, 1)),
-                                          kPThreads, TC<D>::SMEM, s, p));
+  if (per_sm < 1) return 0;
+  return static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(pl.max_items, static_cast<int64_t>(uqh::dev_info().sms) * per_sm)));
+}
+
+template <int D>
+uq_status launch_items(const PrefillParams& p, int grid, cudaStream_t s) {
+  return uqh::cuda_status(
+      uqh::launch_pdl(prefill_tc_kernel<D>, static_cast<unsigned>(grid), kPThreads, TC<D>::SMEM, s, p));
 }
 
 template <int D>
 uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   const uq_cache& c = *a.cache;
   const int G = a.num_q_heads / c.num_kv_heads;
-  const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D,
-                                      a.max_pages * c.page_size, uqh::dev_info().sms, kItemRows);
+  const int cap = a.max_pages * c.page_size;
+  const PrefillPlan pl = plan_prefill(a.num_q_tokens, a.batch, a.num_q_heads, c.num_kv_heads, D, cap,
+                                      uqh::dev_info().sms, kItemRows, false);
   if (a.ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
+  const int grid = item_grid<D>(pl);
+  if (grid < 1) return UQ_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   PrefillParams p = base_params<D>(c, a.block_table, a.max_pages, a.batch, a.num_q_tokens, a.num_q_heads,
                                    a.sm_scale, pl, ws);
   if (!p.status) return UQ_ERR_CUDA;
   p.cu_q = a.cu_q;
   p.seq_lens = a.seq_lens;
-  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.batch, G, c.num_kv_heads, pl.splits, kItemRows, nullptr, 0, 0,
-                                       p.item_pre);
+  prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.seq_lens, a.batch, G, c.num_kv_heads, pl.splits, 0, kItemRows,
+                                       nullptr, 0, cap, grid, p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
   uq_status st = uqh::launch_test_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
                                             c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
-  st = launch_items<D>(p, pl, s);
+  st = launch_items<D>(p, grid, s);
   if (st != UQ_OK) return st;
   PrefillMergeParams mp;
   mp.ws_ml = p.ws_ml;
@@ -839,10 +907,9 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   mp.T = a.num_q_tokens;
   mp.Hq = a.num_q_heads;
   mp.G = G;
-  mp.splits = pl.splits;
   mp.rows = kItemRows;
   mp.max_items = pl.max_items;
-  mp.cap = a.max_pages * c.page_size;
+  mp.cap = cap;
   mp.out = a.out;
   uqh::make_sign_masks(c.rot_seed, D, &mp.sign);
   const int64_t rows = static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads;
@@ -856,8 +923,10 @@ uq_status run_cascade_prefix(const void* q, const uq_cache& c, const int32_t* bl
                              uqh::PrefixPartials* out, cudaStream_t s) {
   const int G = hq / c.num_kv_heads;
   const PrefillPlan pl = plan_prefill(batch, cg.groups, hq, c.num_kv_heads, D, cg.cap, uqh::dev_info().sms,
-                                      kItemRows);
+                                      kItemRows, true);
   if (ws_bytes < pl.total) return UQ_ERR_WORKSPACE;
+  const int grid = item_grid<D>(pl);
+  if (grid < 1) return UQ_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(ws_v);
   PrefillParams p = base_params<D>(c, block_table, max_pages, cg.groups, batch, hq, sm_scale, pl, ws);
   if (!p.status) return UQ_ERR_CUDA;
@@ -866,12 +935,12 @@ uq_status run_cascade_prefix(const void* q, const uq_cache& c, const int32_t* bl
   p.cascade = 1;
   p.min_rows = cg.min_rows;
   p.casc_cap = cg.cap;
-  prefill_plan_kernel<<<1, 32, 0, s>>>(cg.cu, cg.groups, G, c.num_kv_heads, pl.splits, kItemRows, cg.prefix,
-                                       cg.min_rows, cg.cap, p.item_pre);
+  prefill_plan_kernel<<<1, 32, 0, s>>>(cg.cu, nullptr, cg.groups, G, c.num_kv_heads, pl.splits, pl.splits,
+                                       kItemRows, cg.prefix, cg.min_rows, cg.cap, grid, p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
   uq_status st = uqh::launch_test_query_fp8(q, static_cast<int64_t>(batch) * hq, D, c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
-  st = launch_items<D>(p, pl, s);
+  st = launch_items<D>(p, grid, s);
   if (st != UQ_OK) return st;
   out->ml = p.ws_ml;
   out->o = p.ws_o;
@@ -887,7 +956,7 @@ uq_status run_cascade_prefix(const void* q, const uq_cache& c, const int32_t* bl
 namespace uqh {
 
 size_t prefill_workspace_bytes(int T, int B, int hq, int hkv, int d, int max_keys) {
-  return plan_prefill(T, B, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows).total;
+  return plan_prefill(T, B, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows, false).total;
 }
 
 uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s) {
@@ -895,7 +964,7 @@ uq_status launch_prefill(const PrefillArgs& a, cudaStream_t s) {
 }
 
 size_t cascade_prefix_workspace_bytes(int batch, int groups, int hq, int hkv, int d, int max_keys) {
-  return plan_prefill(batch, groups, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows).total;
+  return plan_prefill(batch, groups, hq, hkv, d, max_keys, std::max(1, dev_info().sms), kItemRows, true).total;
 }
 
 uq_status launch_cascade_prefix(const void* q, const uq_cache* cache, const int32_t* block_table, int32_t max_pages,
