@@ -73,6 +73,20 @@ def test_long_context_few_rows_uses_key_splits():
     _check(_run(w, cache, q, chunks), _ref(w, q, chunks), "long")
 
 
+def test_table_larger_than_sequences_and_mixed_lengths():
+    """Key splits come from the longest key range present, not from the block table's
+    capacity: a table with room for 20000 more tokens per sequence, one long sequence and
+    short ones whose later splits are empty, and few row tiles (so many splits)."""
+    lens, chunks = [9000, 70, 640, 5], [3, 2, 64, 5]
+    w = workloads.make("gqa8k", B=4, Hkv=2, Hq=16, seq_lens=lens, seed=63, extra_tokens=20000, n_outlier=3,
+                       outlier_channels=None)
+    assert w.block_table.shape[1] * w.ps >= 29000
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    q = _queries(w, chunks, 64)
+    _check(_run(w, cache, q, chunks), _ref(w, q, chunks), "capacity")
+
+
 def test_empty_chunk_and_single_token():
     lens, chunks = [50, 1, 200], [0, 1, 130]
     w = workloads.make("gqa8k", B=3, Hkv=2, Hq=16, seq_lens=lens, seed=54, n_outlier=3, outlier_channels=None)

@@ -44,6 +44,7 @@ using namespace uqd;
 
 constexpr int kPThreads = 128;  // 4 warps: one query row per thread
 constexpr int kTileKeys = 64;   // keys per tile; key splits are whole tiles
+constexpr int kMergeOneRound = 8;  // the merge loads up to this many splits' partials in one round
 constexpr int kItemCost = 3;    // per-item cost in key tiles, for the split choice (fitted to measured times)
 
 struct PrefillParams {
@@ -700,34 +701,67 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
     const int kvh = h / p.G, hl = h - kvh * p.G;
     const int rowi = i * p.G + hl, rtile = rowi / p.rows, rr = rowi - rtile * p.rows;
     const int64_t item0 = p.item_pre[b] + (static_cast<int64_t>(kvh) * row_tiles(n_plan, p.G, p.rows) + rtile) * splits;
-    float Ms = -INFINITY;
-    for (int s0 = 0; s0 < splits; s0 += 32) {
-      const int s = s0 + lane;
-      if (s < splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * p.rows + rr) * 2]);
-    }
+    float Ms = -INFINITY, Ls = 0.f;
+    if (splits <= kMergeOneRound) {
+      // one round: lane s holds (m, l) of split s, and every lane loads its chunk of
+      // all the splits' O rows before any is used (an empty split's row is never read
+      // into the sum: its m is -inf)
+      float m = -INFINITY, l = 0.f;
+      if (lane < splits) {
+        m = p.ws_ml[((item0 + lane) * p.rows + rr) * 2];
+        l = p.ws_ml[((item0 + lane) * p.rows + rr) * 2 + 1];
+      }
+      float ov[kMergeOneRound][EPL];
 #pragma unroll
-    for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
-    float Ls = 0.f;
-    for (int s0 = 0; s0 < splits; s0 += 32) {
-      const int s = s0 + lane;
-      float w = 0.f;
-      bool live = false;
-      if (s < splits) {
-        const float m = p.ws_ml[((item0 + s) * p.rows + rr) * 2];
-        live = m != -INFINITY;  // an empty split wrote no output row
-        if (live) {
-          w = ex2(m - Ms);
-          Ls += w * p.ws_ml[((item0 + s) * p.rows + rr) * 2 + 1];
+      for (int j = 0; j < kMergeOneRound; ++j)
+        if (j < splits) {
+          const float* src = p.ws_o + ((item0 + j) * p.rows + rr) * D + lane * EPL;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) ov[j][e] = src[e];
+        }
+      Ms = m;
+#pragma unroll
+      for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
+      const bool live = m != -INFINITY;
+      const float w = live ? ex2(m - Ms) : 0.f;
+      Ls = w * l;
+      const unsigned mask = __ballot_sync(kFull, live);
+#pragma unroll
+      for (int j = 0; j < kMergeOneRound; ++j) {
+        const float wj = __shfl_sync(kFull, w, j);
+        if (j < splits && ((mask >> j) & 1u)) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[e] += wj * ov[j][e];
         }
       }
-      const unsigned mask = __ballot_sync(kFull, live);
-      const int cnt = min(32, splits - s0);
-      for (int j = 0; j < cnt; ++j) {
-        const float wj = __shfl_sync(kFull, w, j);
-        if ((mask >> j) & 1u) {
-          const float* src = p.ws_o + ((item0 + s0 + j) * p.rows + rr) * D + lane * EPL;
+    } else {
+      for (int s0 = 0; s0 < splits; s0 += 32) {
+        const int s = s0 + lane;
+        if (s < splits) Ms = fmaxf(Ms, p.ws_ml[((item0 + s) * p.rows + rr) * 2]);
+      }
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o[e] += wj * src[e];
+      for (int k = 16; k > 0; k >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, k));
+      for (int s0 = 0; s0 < splits; s0 += 32) {
+        const int s = s0 + lane;
+        float w = 0.f;
+        bool live = false;
+        if (s < splits) {
+          const float m = p.ws_ml[((item0 + s) * p.rows + rr) * 2];
+          live = m != -INFINITY;  // an empty split wrote no output row
+          if (live) {
+            w = ex2(m - Ms);
+            Ls += w * p.ws_ml[((item0 + s) * p.rows + rr) * 2 + 1];
+          }
+        }
+        const unsigned mask = __ballot_sync(kFull, live);
+        const int cnt = min(32, splits - s0);
+        for (int j = 0; j < cnt; ++j) {
+          const float wj = __shfl_sync(kFull, w, j);
+          if ((mask >> j) & 1u) {
+            const float* src = p.ws_o + ((item0 + s0 + j) * p.rows + rr) * D + lane * EPL;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] += wj * src[e];
+          }
         }
       }
     }
@@ -773,8 +807,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Workspace bound of one launch.  The split count itself is chosen on the
 // device from the key ranges present (prefill_plan_kernel); the host fixes its
 // largest value, `splits`: the count that gives two waves of two blocks per SM
-// at the bound on row tiles, times four for the prefill (room for the device's
-// choice), as is for the cascade prefix (the decode's merge reads that count).
+// at the bound on row tiles, times four for the prefill when the row tiles
+// alone give fewer than two waves (room for the device's choice; with more,
+// extra splits only add partials), as is for the cascade prefix (the decode's
+// merge reads that count).
 struct PrefillPlan {
   int splits;
   int64_t max_items;
@@ -789,7 +825,7 @@ PrefillPlan plan_prefill(int T, int B, int hq, int hkv, int d, int max_keys, int
   const int64_t target = 2LL * 2 * sms;  // two waves of two blocks per SM
   const int max_splits = std::max(1, (max_keys + kTKT - 1) / kTKT);
   const int64_t s0 = std::max<int64_t>(1, (target + base - 1) / base);
-  pl.splits = static_cast<int>(std::min<int64_t>(max_splits, fixed ? s0 : 4 * s0));
+  pl.splits = static_cast<int>(std::min<int64_t>(max_splits, fixed || base >= target ? s0 : 4 * s0));
   pl.max_items = base * pl.splits;
   pl.off_pre = 256;
   pl.off_q = pl.off_pre + align256(static_cast<size_t>(B + 3) * 4);
