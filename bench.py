@@ -739,8 +739,8 @@ def main():
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--no-anchors", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="append64k",
-                    choices=["append64k", "tiny", "gqa8k", "mixed", "prefix128k"])
+    ap.add_argument("--workload", default=None, choices=["append64k", "tiny", "gqa8k", "mixed", "prefix128k"],
+                    help="default: prefix128k for --kernel cascade (the shared-prefix workload), else append64k")
     ap.add_argument("--kernel", default="decode", choices=["decode", "prefill", "cascade", "layers"],
                     help="with a workload other than append64k: what each step runs")
     ap.add_argument("--chunk", type=int, default=16, help="--kernel prefill: query tokens per sequence")
@@ -749,6 +749,8 @@ def main():
     ap.add_argument("--layers", type=int, default=32, help="--kernel layers: attention layers in the stack")
     ap.add_argument("--ctx", type=int, default=32768, help="--kernel layers: context per sequence")
     args = ap.parse_args()
+    if args.workload is None:
+        args.workload = "prefix128k" if args.kernel == "cascade" else "append64k"
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
