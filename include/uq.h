@@ -267,6 +267,9 @@ uq_status uq_decode_attention_tq4(const void* q, const uq_cache* cache, const in
  * workspace   : device, 16-byte aligned, at least
  *               uq_prefill_workspace_bytes(num_q_tokens, batch, num_q_heads,
  *               num_kv_heads, head_dim, max_pages_per_seq * page_size) bytes.
+ *               The key ranges are split over work items on the device, from
+ *               seq_lens (the longest sequence present, not the table's
+ *               capacity); the workspace bounds the largest split count.
  * FP4 caches with head_dim 64 or 128 (UQ_ERR_UNSUPPORTED otherwise); other
  * shapes as the decode.
  */
