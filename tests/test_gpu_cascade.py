@@ -101,6 +101,18 @@ def test_prefix_cut_by_max_prefix_len():
     assert_close(got, _ref(w, [0, 1, 2], q), "cut")
 
 
+def test_max_prefix_far_above_the_prefixes():
+    """The shared-prefix kernel sizes its key splits from the prefixes present, not from
+    max_prefix_len: a bound 32x the longest prefix, and two groups of unequal prefixes."""
+    lens = [1024 + 200, 1024 + 9, 1024 + 77, 1024 + 300, 1024 + 1]  # all share 1024; group 1 claims 512
+    w, cache = _setup(5, 8, lens, 1024, seed=89)
+    q = w.q()
+    got, st = _cascade(w, cache, q, [0, 3, 5], [1024, 512], 32768)
+    assert st == 0
+    assert_close(got, _ref(w, list(range(5)), q), "bound far above")
+    assert np.max(np.abs(got - _plain(w, cache, q))) < 1e-4
+
+
 def test_prefix_longer_than_a_member_is_reported():
     lens = [2048 + 300, 2048 + 17]
     w, cache = _setup(2, 8, lens, 2048, seed=87)
