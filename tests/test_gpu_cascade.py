@@ -104,10 +104,10 @@ def test_prefix_cut_by_max_prefix_len():
 def test_max_prefix_far_above_the_prefixes():
     """The shared-prefix kernel sizes its key splits from the prefixes present, not from
     max_prefix_len: a bound 32x the longest prefix, and two groups of unequal prefixes."""
-    lens = [1024 + 200, 1024 + 9, 1024 + 77, 1024 + 300, 1024 + 1]  # all share 1024; group 1 claims 512
-    w, cache = _setup(5, 8, lens, 1024, seed=89)
+    lens = [2048 + 200, 2048 + 9, 2048 + 77, 2048 + 300, 2048 + 1]  # all share 2048; group 1 claims 1024
+    w, cache = _setup(5, 8, lens, 2048, seed=89)
     q = w.q()
-    got, st = _cascade(w, cache, q, [0, 3, 5], [1024, 512], 32768)
+    got, st = _cascade(w, cache, q, [0, 3, 5], [2048, 1024], 65536)
     assert st == 0
     assert_close(got, _ref(w, list(range(5)), q), "bound far above")
     assert np.max(np.abs(got - _plain(w, cache, q))) < 1e-4
