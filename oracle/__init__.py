@@ -30,6 +30,7 @@ _lib.uqo_inv_sqrt_d.restype = C.c_float
 _lib.uqo_inv_sqrt_d.argtypes = [C.c_int]
 _lib.uqo_rotate_fp32.argtypes = [_f32p, C.c_int, _i8p, _f32p]
 _lib.uqo_inverse_rotate_f64.argtypes = [_f64p, C.c_int, _i8p, _f64p]
+_lib.uqo_inverse_rotate_fp32.argtypes = [_f32p, C.c_int, _i8p, _f32p]
 _lib.uqo_pow2_exponent.restype = C.c_int
 _lib.uqo_pow2_exponent.argtypes = [C.c_double, C.c_int]
 _lib.uqo_scale_byte.restype = C.c_int
@@ -67,15 +68,15 @@ _lib.uqo_decode_ex.argtypes = [C.c_int, _u16p, C.c_int, C.c_int, C.c_int, C.c_in
                                _i32p, C.c_int, _i32p, C.c_double, C.c_uint64, C.c_void_p, _f64p]
 _lib.uqo_f16_round.restype = C.c_double
 _lib.uqo_f16_round.argtypes = [C.c_float]
-_lib.uqo_tq_norm.restype = C.c_float
+_lib.uqo_tq_norm.restype = C.c_double
 _lib.uqo_tq_norm.argtypes = [_f32p, C.c_int]
 _lib.uqo_tq_code.restype = C.c_int
-_lib.uqo_tq_code.argtypes = [C.c_float, _f32p]
+_lib.uqo_tq_code.argtypes = [C.c_double, _f64p]
 _lib.uqo_tq_value.restype = C.c_double
 _lib.uqo_tq_value.argtypes = [C.c_int, _f64p]
-_lib.uqo_tq_quantize_row.argtypes = [_f32p, C.c_int, _i8p, _f32p, _u8p, _f32p]
+_lib.uqo_tq_quantize_row.argtypes = [_f32p, C.c_int, _i8p, _f64p, _u8p, _f32p]
 _lib.uqo_append_tq4.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, _i64p, C.c_int, C.c_int,
-                                C.c_int, C.c_uint64, _f32p, _u8p, _f32p, _u8p, _f32p]
+                                C.c_int, C.c_uint64, _f64p, _u8p, _f32p, _u8p, _f32p]
 _lib.uqo_query_f16.argtypes = [_u16p, C.c_int, C.c_uint64, _f64p]
 
 KIND_FP4, KIND_FP8, KIND_BF16, KIND_TQ4 = 0, 1, 2, 3
@@ -122,6 +123,19 @@ def inverse_rotate_f64(o: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
     out = np.empty_like(flat)
     for r in range(flat.shape[0]):
         _lib.uqo_inverse_rotate_f64(flat[r], d, s, out[r])
+    return out.reshape(o.shape)
+
+
+def inverse_rotate_fp32(o: np.ndarray, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """fp32 inverse rotation s .* fl32(FWHT_fp32(o) * fl32(1/sqrt d)) of each row
+    (the decode's output stage)."""
+    o = _c(o, np.float32)
+    d = o.shape[-1]
+    s = signs(seed, d)
+    flat = o.reshape(-1, d)
+    out = np.empty_like(flat)
+    for r in range(flat.shape[0]):
+        _lib.uqo_inverse_rotate_fp32(flat[r], d, s, out[r])
     return out.reshape(o.shape)
 
 
@@ -219,7 +233,8 @@ class Cache:
             self.vc = np.zeros((rows, head_dim // 2), np.uint8)
             self.ks = np.zeros(rows, np.float32)  # norms
             self.vs = np.zeros(rows, np.float32)
-            self.mags, self.tau = tq_codebook(head_dim)
+            self.cpos = tq_centroids(head_dim)   # fp64 centroids of the non-negative half
+            self.mags = self.cpos                # the decode's reconstruction table (see decode)
         elif kind == KIND_FP8:
             self.kc = np.zeros((rows, head_dim), np.uint8)
             self.vc = np.zeros((rows, head_dim), np.uint8)
@@ -239,21 +254,25 @@ class Cache:
         if self.kind == KIND_FP4:
             _lib.uqo_append_fp4_c(*args, self.seed, np.float32(self.c), self.kc, self.ks, self.vc, self.vs)
         elif self.kind == KIND_TQ4:
-            _lib.uqo_append_tq4(*args, self.seed, _c(self.tau[8:], np.float32), self.kc, self.ks, self.vc, self.vs)
+            _lib.uqo_append_tq4(*args, self.seed, _c(self.cpos, np.float64), self.kc, self.ks, self.vc, self.vs)
         elif self.kind == KIND_FP8:
             _lib.uqo_append_fp8(*args, np.float32(self.k_scale), np.float32(self.v_scale), self.kc, self.vc)
         else:
             _lib.uqo_append_bf16(*args, self.kc, self.vc)
 
-    def decode(self, q_bf16, block_table, seq_lens, sm_scale=0.0):
-        """fp64 decode attention; q: [B][Hq][d] bf16 bits -> [B][Hq][d] float64."""
+    def decode(self, q_bf16, block_table, seq_lens, sm_scale=0.0, tq_table=None):
+        """fp64 decode attention; q: [B][Hq][d] bf16 bits -> [B][Hq][d] float64.
+        TQ4: values are code -> +-table[rank] x norm, the table being the fp64
+        centroids unless tq_table (8 non-negative magnitudes) is given."""
         q = _c(q_bf16, np.uint16)
         B, Hq, d = q.shape
         bt = _c(block_table, np.int32)
         sl = _c(seq_lens, np.int32)
         out = np.empty((B, Hq, d), np.float64)
         ptr = lambda a: None if a is None else a.ctypes.data
-        mags = _c(self.mags, np.float64) if self.kind == KIND_TQ4 else None
+        mags = None
+        if self.kind == KIND_TQ4:
+            mags = _c(self.mags if tq_table is None else tq_table, np.float64)
         _lib.uqo_decode_ex(self.kind, q.reshape(-1), B, Hq, self.Hkv, d, self.ps, ptr(self.kc), ptr(self.ks),
                            ptr(self.vc), ptr(self.vs), np.float32(self.k_scale), np.float32(self.v_scale),
                            bt.reshape(-1), bt.shape[1], sl, float(sm_scale), self.seed, ptr(mags),
@@ -308,8 +327,9 @@ _TQ_BOOKS = {}
 
 
 def tq_codebook(d: int, bits: int = 4):
-    """(f16 magnitudes c_8..c_15 as float64, fp32 thresholds tau_0..tau_14)
-    of the Lloyd-Max codebook for head_dim d (oracle/tq.py), cached."""
+    """(f16 magnitudes c_8..c_15 as float64, fp32 thresholds tau_0..tau_14):
+    the f16 / fp32 roundings of the Lloyd-Max codebook for head_dim d
+    (oracle/tq.py), the form in which the library stores its table; cached."""
     from . import tq
     key = (d, bits)
     if key not in _TQ_BOOKS:
@@ -317,17 +337,30 @@ def tq_codebook(d: int, bits: int = 4):
     return _TQ_BOOKS[key]
 
 
+def tq_centroids(d: int) -> np.ndarray:
+    """fp64 centroids c_8 < ... < c_15 of the non-negative half of the 4-bit
+    Lloyd-Max codebook (oracle/tq.py): the oracle's quantiser and default
+    reconstruction table."""
+    from . import tq
+    key = (d, "c64")
+    if key not in _TQ_BOOKS:
+        _TQ_BOOKS[key] = np.ascontiguousarray(tq.lloyd_max(d, 4)[8:], np.float64)
+    return _TQ_BOOKS[key]
+
+
 def f16_round(x: float) -> float:
     return float(_lib.uqo_f16_round(np.float32(x)))
 
 
-def tq_norm(y: np.ndarray) -> np.float32:
+def tq_norm(y: np.ndarray) -> float:
+    """fp64 Euclidean norm of a rotated row (T3)."""
     y = _c(y, np.float32)
-    return np.float32(_lib.uqo_tq_norm(y, y.size))
+    return float(_lib.uqo_tq_norm(y, y.size))
 
 
-def tq_code(y: float, t_pos: np.ndarray) -> int:
-    return int(_lib.uqo_tq_code(np.float32(y), _c(t_pos, np.float32)))
+def tq_code(u: float, cpos: np.ndarray) -> int:
+    """T4: sign-magnitude nibble of the centroid nearest to u."""
+    return int(_lib.uqo_tq_code(float(u), _c(cpos, np.float64)))
 
 
 def tq_value(code: int, mags: np.ndarray) -> float:
@@ -343,12 +376,12 @@ def tq_quantize_rows(x: np.ndarray, seed: int = DEFAULT_SEED):
     if not f32:
         flat = (flat.astype(np.uint32) << 16).view(np.float32)
     flat = _c(flat, np.float32)
-    _, tau = tq_codebook(d)
+    cpos = tq_centroids(d)
     s = signs(seed, d)
     codes = np.empty((flat.shape[0], d // 2), np.uint8)
     norms = np.empty(flat.shape[0], np.float32)
     for r in range(flat.shape[0]):
-        _lib.uqo_tq_quantize_row(flat[r], d, s, _c(tau[8:], np.float32), codes[r], norms[r:r + 1])
+        _lib.uqo_tq_quantize_row(flat[r], d, s, cpos, codes[r], norms[r:r + 1])
     return codes, norms
 
 

@@ -21,8 +21,10 @@ Readings of this library (listed in the design doc):
       codebook is exactly symmetric; cell masses use the regularised
       incomplete beta function, first moments their closed form
       int x (1-x^2)^k dx = -(1-x^2)^(k+1) / (2(k+1)).
-  T2  stored reconstruction values are the f16 roundings of the centroids;
-      decision thresholds are the fp32 roundings of the fp64 midpoints.
+  T2  the oracle quantises to, and reconstructs with, the fp64 centroids;
+      `codebook` also gives their f16 roundings and the fp32 roundings of the
+      midpoints, the form in which the library stores its table (checked
+      against it exactly).
 """
 import math
 
@@ -98,8 +100,8 @@ def distortion(c: np.ndarray, d: int) -> float:
 
 
 def codebook(d: int, bits: int = 4):
-    """(f16 reconstruction magnitudes of the non-negative half, ascending, as
-    float64; fp32 decision thresholds tau_0 < ... < tau_{L-2}) per T2."""
+    """(f16 roundings of the non-negative centroids, ascending, as float64;
+    fp32 roundings of the midpoints tau_0 < ... < tau_{L-2}) per T2."""
     c = lloyd_max(d, bits)
     L = len(c)
     mags = np.array([float(np.float16(v)) for v in c[L // 2:]], np.float64)

@@ -90,6 +90,28 @@ void uqo_inverse_rotate_f64(const double* o, int d, const int8_t* s, double* out
   for (int i = 0; i < d; ++i) out[i] = (double)s[i] * u[i] * c;
 }
 
+/* Inverse rotation in fp32, the form the decode's output stage takes:       */
+/* out = s .* fl32(FWHT_fp32(o) * fl32(1/sqrt d)), the same ascending-stride  */
+/* butterfly as the forward rotation (H is symmetric, so H^T o = H o), each    */
+/* output fl32(a+b) / fl32(a-b); the signs last (exact).                       */
+void uqo_inverse_rotate_fp32(const float* o, int d, const int8_t* s, float* out) {
+  float u[1024];
+  for (int i = 0; i < d; ++i) u[i] = o[i];
+  for (int h = 1; h < d; h <<= 1) {
+    for (int i = 0; i < d; ++i) {
+      if (i & h) continue;
+      float a = u[i], b = u[i + h];
+      u[i] = a + b;
+      u[i + h] = a - b;
+    }
+  }
+  float c = uqo_inv_sqrt_d(d);
+  for (int i = 0; i < d; ++i) {
+    float y = u[i] * c;
+    out[i] = (s[i] < 0) ? -y : y;
+  }
+}
+
 /* ------------------------------------------------------------------------- */
 /* R2: UE8M0 scale byte of one 32-channel group.                               */
 /* [UQ-review] 3.1/3.3: group absmax m, times the global constant c = 0.156,   */
@@ -373,20 +395,17 @@ void uqo_append_bf16(const void* k, const void* v, int in_fp32, int64_t T, const
 
 /* ------------------------------------------------------------------------- */
 /* TQ4: the TurboQuant Q_mse codebook variant ([TQ-guide] "Lloyd-Max 스칼라    */
-/* 양자화 (Q_mse)" and "직교성을 이용한 내적 보존").  A row is rotated with R1,  */
-/* its L2 norm is stored, and every coordinate of the unit vector y / n is     */
-/* replaced by the index of its nearest Lloyd-Max centroid.  The codebook     */
-/* (computed from the pdf in oracle/tq.py) comes in as two tables: the f16    */
-/* reconstruction magnitudes c_8..c_15 of the non-negative half and the fp32   */
-/* decision thresholds tau_8..tau_14 between them (the negative half mirrors). */
+/* 양자화 (Q_mse)" and "직교성을 이용한 내적 보존").  A row is rotated with R1, */
+/* its L2 norm n is stored, and every coordinate of the unit vector y / n is   */
+/* replaced by the index of its nearest Lloyd-Max centroid.  The codebook      */
+/* (computed from the pdf in oracle/tq.py) comes in as the fp64 centroids      */
+/* c_8 < ... < c_15 of the non-negative half (the negative half mirrors).      */
 /* Readings:                                                       */
-/*   T3  n = fl32(sqrt(S)), S the fp32 sum of fl32(y_i^2) over a balanced     */
-/*       binary tree of adjacent elements (left half + right half,             */
-/*       recursively); non-finite n: norm NaN, zero codes.                     */
-/*   T4  with t_k = fl32(n * tau_k): y >= 0 -> code m = #{k : y >= t_k};       */
-/*       y < 0 -> code 8 | #{k : |y| > t_k}.  This is "index of the first     */
-/*       threshold above y/n" written without a division, on the sign-        */
-/*       magnitude code (bit 3 = negative, bits 0..2 = magnitude rank).        */
+/*   T3  n = sqrt(sum y_i^2) in fp64, stored as fl32(n); u_i = y_i / n in fp64; */
+/*       a non-finite n stores NaN and zero codes; n = 0 stores 0 and zero     */
+/*       codes (every code decodes to 0 there).                                */
+/*   T4  code of u: sign-magnitude nibble, bit 3 set for u < 0, bits 0..2 the  */
+/*       rank of the centroid nearest to |u| (ties to the lower rank).         */
 /*   T5  q~ = f16(R1 q), round to nearest even.                                */
 /* ------------------------------------------------------------------------- */
 double uqo_f16_round(float x) {
@@ -405,24 +424,20 @@ double uqo_f16_round(float x) {
   return signbit(x) ? -r : r;
 }
 
-/* Sum of fl32(y_i^2) over [a, b): fl32(left half + right half), recursively. */
-static float tq_sumsq(const float* y, int a, int b) {
-  if (b - a == 1) return y[a] * y[a];
-  int m = (a + b) / 2;
-  float left = tq_sumsq(y, a, m), right = tq_sumsq(y, m, b);
-  return left + right;
+/* The Euclidean norm of the rotated row, in fp64 (T3). */
+double uqo_tq_norm(const float* y, int d) {
+  double s = 0.0;
+  for (int i = 0; i < d; ++i) s += (double)y[i] * (double)y[i];
+  return sqrt(s);
 }
 
-float uqo_tq_norm(const float* y, int d) { return sqrtf(tq_sumsq(y, 0, d)); }
-
-int uqo_tq_code(float y, const float* t) {
-  int m = 0;
-  if (y >= 0.0f) {
-    for (int k = 0; k < 7; ++k) m += (y >= t[k]);
-    return m;
-  }
-  for (int k = 0; k < 7; ++k) m += (-y > t[k]);
-  return 8 | m;
+/* T4: nearest centroid of u among +-cpos[0..7]. */
+int uqo_tq_code(double u, const double* cpos) {
+  double a = fabs(u);
+  int best = 0;
+  for (int k = 1; k < 8; ++k)
+    if (fabs(a - cpos[k]) < fabs(a - cpos[best])) best = k;
+  return (u < 0.0 ? 8 : 0) | best;
 }
 
 double uqo_tq_value(int code, const double* mags) {
@@ -432,24 +447,24 @@ double uqo_tq_value(int code, const double* mags) {
 
 /* Rotate + quantise one row (fp32 values): d/2 code bytes in natural order   */
 /* (byte j = code(2j) | code(2j+1) << 4) and the fp32 norm.                    */
-void uqo_tq_quantize_row(const float* xr, int d, const int8_t* s, const float* tau_pos,
+void uqo_tq_quantize_row(const float* xr, int d, const int8_t* s, const double* cpos,
                          uint8_t* codes, float* norm) {
-  float y[1024], t[7];
+  float y[1024];
   uqo_rotate_fp32(xr, d, s, y);
-  float n = uqo_tq_norm(y, d);
-  if (!isfinite(n)) {
+  double n = uqo_tq_norm(y, d);
+  if (!isfinite(n) || n == 0.0) {
     memset(codes, 0, (size_t)d / 2);
-    *norm = NAN;
+    *norm = isfinite(n) ? 0.0f : NAN;
     return;
   }
-  for (int k = 0; k < 7; ++k) t[k] = n * tau_pos[k];
   for (int j = 0; j < d / 2; ++j)
-    codes[j] = (uint8_t)(uqo_tq_code(y[2 * j], t) | (uqo_tq_code(y[2 * j + 1], t) << 4));
-  *norm = n;
+    codes[j] = (uint8_t)(uqo_tq_code((double)y[2 * j] / n, cpos) |
+                         (uqo_tq_code((double)y[2 * j + 1] / n, cpos) << 4));
+  *norm = (float)n;
 }
 
 void uqo_append_tq4(const void* k, const void* v, int in_fp32, int64_t T, const int64_t* slots,
-                    int Hkv, int ps, int d, uint64_t seed, const float* tau_pos, uint8_t* kc,
+                    int Hkv, int ps, int d, uint64_t seed, const double* cpos, uint8_t* kc,
                     float* kn, uint8_t* vc, float* vn) {
   int8_t s[1024];
   float xr[1024];
@@ -460,10 +475,10 @@ void uqo_append_tq4(const void* k, const void* v, int in_fp32, int64_t T, const 
     for (int h = 0; h < Hkv; ++h) {
       int64_t src = t * Hkv + h, dst = cache_row(slots[t], h, Hkv, ps);
       load_row(k, in_fp32, src, d, xr);
-      uqo_tq_quantize_row(xr, d, s, tau_pos, row, kn + dst);
+      uqo_tq_quantize_row(xr, d, s, cpos, row, kn + dst);
       for (int j = 0; j < d / 2; ++j) kc[dst * (d / 2) + uqo_kbyte_pos(j, d)] = row[j];
       load_row(v, in_fp32, src, d, xr);
-      uqo_tq_quantize_row(xr, d, s, tau_pos, vc + dst * (d / 2), vn + dst);
+      uqo_tq_quantize_row(xr, d, s, cpos, vc + dst * (d / 2), vn + dst);
     }
   }
 }

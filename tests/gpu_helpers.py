@@ -66,6 +66,20 @@ def oracle_for(w, seqs, dtype=uq.FP4_UE8M0, k_scale=1.0, v_scale=1.0, seed=uq.DE
     return oc, bt, np.array(lens, np.int32)
 
 
+def oracle_from_device(cache, seed=uq.DEFAULT_SEED):
+    """Oracle cache holding a copy of a device cache's bytes (same pages, same
+    layout): the decode oracle then attends to exactly the values the kernel
+    reads."""
+    kind = KIND[cache.dtype]
+    oc = oracle.Cache(kind, cache.num_pages, cache.num_kv_heads, cache.page_size, cache.head_dim,
+                      k_scale=cache.struct.k_scale, v_scale=cache.struct.v_scale, seed=seed)
+    host = lambda t, like: t.detach().cpu().contiguous().view(torch.uint8).numpy().view(like.dtype).reshape(like.shape)
+    oc.kc, oc.vc = host(cache.k_codes, oc.kc), host(cache.v_codes, oc.vc)
+    if oc.ks is not None:
+        oc.ks, oc.vs = host(cache.k_scales, oc.ks), host(cache.v_scales, oc.vs)
+    return oc
+
+
 def errors(got: np.ndarray, ref: np.ndarray):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)

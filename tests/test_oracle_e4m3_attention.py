@@ -58,6 +58,63 @@ def _hadamard(d):
     return np.where(pc % 2 == 0, 1.0, -1.0)
 
 
+# ---------------------------------------------------------------- query (R4) and the FP8 anchor's scale
+def _bf16_of(x):
+    return torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("k", [0, 5, 77, 127])
+def test_query_fp8_of_a_basis_vector_by_hand(k):
+    # R e_k = s_k (column k of H) / sqrt(128): every coordinate is +-0.0883883,
+    # whose nearest E4M3 value is 1.375 * 2^-4 (exponent field 3, mantissa 3):
+    # byte 0x1B, with bit 7 where s_k H[i][k] < 0
+    d = 128
+    q = np.zeros(d, np.float32)
+    q[k] = 1.0
+    got = oracle.query_fp8(_bf16_of(q)[None])[0]
+    s = oracle.signs(oracle.DEFAULT_SEED, d)
+    neg = (s[k] * _hadamard(d)[:, k]) < 0
+    assert np.array_equal(got, np.where(neg, 0x9B, 0x1B).astype(np.uint8))
+
+
+def test_query_fp8_two_hot_by_hand():
+    # q = 2 e_0 + 3 e_5: R q = (2 s_0 H[:,0] + 3 s_5 H[:,5]) / sqrt(128), exact
+    # integers +-5, +-1 before the scale; 5 / sqrt(128) = 0.4419 -> 1.75 * 2^-2
+    # (byte 0x2E), 1 / sqrt(128) -> 0x1B
+    d = 128
+    q = np.zeros(d, np.float32)
+    q[0], q[5] = 2.0, 3.0
+    got = oracle.query_fp8(_bf16_of(q)[None])[0]
+    s = oracle.signs(oracle.DEFAULT_SEED, d)
+    H = _hadamard(d)
+    u = 2 * s[0] * H[:, 0] + 3 * s[5] * H[:, 5]
+    want = np.where(np.abs(u) == 5, 0x2E, 0x1B) | np.where(u < 0, 0x80, 0)
+    assert np.array_equal(got, want.astype(np.uint8))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_query_fp8_is_e4m3_of_the_rotated_query(d):
+    # R4 composes two separately pinned stages: R1 and E4M3 rounding
+    q = _bf16_bits(torch.randn(40, d, generator=torch.Generator().manual_seed(d)).to(torch.bfloat16) * 7)
+    qf = (q.astype(np.uint32) << 16).view(np.float32)
+    want = oracle.e4m3_codes(oracle.rotate_fp32(qf)).reshape(q.shape)
+    assert np.array_equal(oracle.query_fp8(q), want)
+
+
+def test_fp8_append_divides_by_the_tensor_scale():
+    # e4m3(x / k_scale): 3 / 0.5 = 6 -> 0x4C, -3 / 0.5 -> 0xCC, 300 / 0.5 = 600 saturates
+    # to 448 (0x7E); v: 3 / 2 = 1.5 -> 0x3C
+    d, ps = 64, 16
+    cache = oracle.Cache(oracle.KIND_FP8, 1, 1, ps, d, k_scale=0.5, v_scale=2.0)
+    k = np.full((3, 1, d), 3.0, np.float32)
+    k[1] = -3.0
+    k[2] = 300.0
+    v = np.full((3, 1, d), 3.0, np.float32)
+    cache.append(k, v, np.array([0, 1, 2], np.int64))
+    assert np.all(cache.kc[0] == 0x4C) and np.all(cache.kc[1] == 0xCC) and np.all(cache.kc[2] == 0x7E)
+    assert np.all(cache.vc[:3] == 0x3C)
+
+
 def _e2m1(code):
     s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
     v = np.where(e == 0, m * 0.5, 2.0 ** (e - 1) * (1 + m / 2))

@@ -100,3 +100,37 @@ def test_rotation_spreads_outliers():
     ratio_before = np.abs(x).max(1) / np.sqrt((x ** 2).mean(1))
     ratio_after = np.abs(y).max(1) / np.sqrt((y ** 2).mean(1))
     assert np.median(ratio_before) > 7 and np.median(ratio_after) < 4
+
+
+# ---------------------------------------------------------------- fp32 inverse rotation (decode output stage)
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_fp32_inverse_rotation_matches_dense_fp64(d):
+    # out = s .* (H o) / sqrt(d), the transpose of R (H is symmetric), by a dense product
+    rng = np.random.default_rng(7)
+    o = rng.standard_normal((64, d)).astype(np.float32)
+    o[:, 9] *= 30
+    got = oracle.inverse_rotate_fp32(o, 42).astype(np.float64)
+    s = oracle.signs(42, d).astype(np.float64)
+    ref = (o.astype(np.float64) @ _hadamard(d).T.astype(np.float64)) * s / np.sqrt(d)
+    err = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert err.max() < 1e-6
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp32_inverse_rotation_of_basis_vectors_is_exact(d):
+    # R^T e_k = s .* (column k of H) / sqrt(d): every butterfly adds zeros, so the
+    # fp32 result is exactly +-fl32(1/sqrt d) with the sign s_i H[i][k]
+    c = oracle.inv_sqrt_d(d)
+    s = oracle.signs(42, d).astype(np.int64)
+    H = _hadamard(d)
+    got = oracle.inverse_rotate_fp32(np.eye(d, dtype=np.float32), 42)   # row k = R^T e_k
+    want = (H.T * s[None, :]).astype(np.float32) * c                    # row k: s_i H[i][k] c
+    assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
+
+
+def test_fp32_inverse_undoes_forward_rotation():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((50, 128)).astype(np.float32)
+    x[:, [3, 77]] *= 20
+    back = oracle.inverse_rotate_fp32(oracle.rotate_fp32(x))
+    assert np.max(np.abs(back - x) / np.max(np.abs(x), axis=1, keepdims=True)) < 1e-6

@@ -101,37 +101,45 @@ def _rows(n, d, seed):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_codes_are_nearest_centroid_except_at_rounding_ties(d):
+def test_codes_are_nearest_centroid(d):
+    # brute force over all 16 signed centroids (a different formulation from the
+    # oracle's sign + magnitude rank): index of the nearest one, mapped to the
+    # sign-magnitude nibble; the norm by numpy's own fp64 routine
     x = _rows(400, d, 11)
     codes, norms = oracle.tq_quantize_rows(x)
-    mags, _ = oracle.tq_codebook(d)
-    c = np.concatenate((-tq.lloyd_max(d, 4)[8:][::-1], tq.lloyd_max(d, 4)[8:]))
+    c = tq.lloyd_max(d, 4)                                               # ascending, 16 levels
     y = oracle.rotate_fp32(x).astype(np.float64)
-    u = y / norms[:, None].astype(np.float64)
-    nearest = np.argmin(np.abs(u[..., None] - c), axis=-1)               # index 0..15, ascending
+    n = np.linalg.norm(y, axis=1)
+    np.testing.assert_allclose(norms, n.astype(np.float32), rtol=1e-7, atol=0)
+    u = y / n[:, None]
+    nearest = np.argmin(np.abs(u[..., None] - c), axis=-1)               # index 0..15
     want = np.where(nearest >= 8, nearest - 8, 8 | (7 - nearest))
     got = np.stack([codes & 15, codes >> 4], -1).reshape(codes.shape[0], d)
-    bad = np.argwhere(got != want)
-    mids = 0.5 * (c[:-1] + c[1:])
-    for r, i in bad:  # only where y/n sits within fp32 rounding of a decision threshold
-        assert np.min(np.abs(u[r, i] - mids)) < 1e-6 * max(abs(u[r, i]), 1e-3)
-    assert len(bad) <= 2
+    assert np.array_equal(got, want)
 
 
 def test_norm_is_the_vector_norm():
+    # the rotation is orthogonal: the stored norm of R x is |x| up to fp32 rotation error
     x = _rows(200, 128, 12)
     _, norms = oracle.tq_quantize_rows(x)
     np.testing.assert_allclose(norms, np.linalg.norm(x.astype(np.float64), axis=1), rtol=2e-6)
 
 
-def test_code_rule_at_exact_thresholds_and_signs():
-    t = np.array([0.1, 0.2, 0.3, 0.4, 0.5, 0.6, 0.7], np.float32)
-    assert oracle.tq_code(0.0, t) == 0 and oracle.tq_code(-0.0, t) == 0
-    assert oracle.tq_code(0.1, t) == 1 and oracle.tq_code(-0.1, t) == 8      # tie: up for y >= 0, down for y < 0
-    assert oracle.tq_code(0.75, t) == 7 and oracle.tq_code(-0.75, t) == 15
-    assert oracle.tq_code(0.35, t) == 3 and oracle.tq_code(-0.35, t) == 8 | 3
+def test_code_rule_by_hand():
+    cpos = np.array([0.1, 0.2, 0.3, 0.4, 0.5, 0.6, 0.7, 0.8], np.float64)
+    assert oracle.tq_code(0.0, cpos) == 0 and oracle.tq_code(-0.0, cpos) == 0
+    assert oracle.tq_code(0.14, cpos) == 0 and oracle.tq_code(0.16, cpos) == 1
+    assert oracle.tq_code(-0.16, cpos) == 8 | 1 and oracle.tq_code(-0.04, cpos) == 8
+    assert oracle.tq_code(0.95, cpos) == 7 and oracle.tq_code(-1.0, cpos) == 15
+    assert oracle.tq_code(0.349, cpos) == 2 and oracle.tq_code(0.351, cpos) == 3
     mags = np.arange(1, 9, dtype=np.float64)
     assert [oracle.tq_value(k, mags) for k in (0, 7, 8, 15)] == [1.0, 8.0, -1.0, -8.0]
+
+
+def test_zero_row_stores_zero_norm_and_zero_codes():
+    x = np.zeros((1, 128), np.float32)
+    codes, norms = oracle.tq_quantize_rows(x)
+    assert norms[0] == 0.0 and not codes.any()
 
 
 def test_non_finite_row_gets_nan_norm_and_zero_codes():
@@ -144,7 +152,7 @@ def test_non_finite_row_gets_nan_norm_and_zero_codes():
 def test_dequantised_mse_matches_codebook_distortion():
     x = np.random.default_rng(14).standard_normal((3000, 128)).astype(np.float32)
     codes, norms = oracle.tq_quantize_rows(x)
-    mags, _ = oracle.tq_codebook(128)
+    mags = oracle.tq_centroids(128)
     sign = np.where(np.stack([codes & 8, (codes >> 4) & 8], -1).reshape(3000, 128) > 0, -1.0, 1.0)
     mag = mags[np.stack([codes & 7, (codes >> 4) & 7], -1).reshape(3000, 128)]
     y = oracle.rotate_fp32(x).astype(np.float64)
