@@ -394,8 +394,13 @@ void uq_rotation_signs(uint64_t seed, int32_t d, int8_t* host_out);
 /* ---- test hooks: single stages of the path, for bit-exact checks ---------
  * All pointers are device pointers; d is 64, 128 or 256. */
 
-/* Forward rotation of n_vec fp32 rows: y = fl32(FWHT(s .* x) * fl32(1/sqrt d)). */
-uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, float* y,
+/* Rotation of n_vec fp32 rows ([UQ-review] §3.1; [TQ-guide] randomised
+ * Hadamard rotation and its orthogonality).  x, y: device fp32 [n_vec][d].
+ *   inverse = 0: the append's forward rotation, y = fl32(FWHT(s .* x) * fl32(1/sqrt d)).
+ *   inverse = 1: the decode's output stage, y = s .* fl32(FWHT(x) * fl32(1/sqrt d))
+ *                (the same device code as the merge kernels run).
+ * Any other inverse value: UQ_ERR_INVALID_ARG. */
+uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, int32_t inverse, float* y,
                          cudaStream_t stream);
 
 /* Quantiser stage alone on already-rotated fp32 rows: codes [n_vec][d/2],

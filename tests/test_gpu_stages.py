@@ -1,5 +1,5 @@
 """Bit-exact checks of single stages of the CUDA path against the oracle:
-rotation, quantiser (scale byte + E2M1 codes), the decode prologue (rotated
+rotation and its inverse (the decode output stage), quantiser (scale byte + E2M1 codes), the decode prologue (rotated
 E4M3 query) and the E4M3 conversion."""
 import numpy as np
 import pytest
@@ -27,6 +27,16 @@ def test_rotation_bit_exact(d):
     for seed in (0, 42):
         y = uq.uq_test_rotate(x.cuda(), seed).cpu().numpy()
         ref = oracle.rotate_fp32(x.numpy(), seed)
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_inverse_rotation_bit_exact(d):
+    # the merge kernels' output stage (D7) against the oracle's fp32 inverse rotation
+    x = _rows(4096, d, 3)
+    for seed in (0, 42):
+        y = uq.uq_test_rotate(x.cuda(), seed, inverse=True).cpu().numpy()
+        ref = oracle.inverse_rotate_fp32(x.numpy(), seed)
         assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
 
 

@@ -64,7 +64,7 @@ _sig = {
     "uq_check_device_status": (C.c_int, [_vp]),
     "uq_status_string": (C.c_char_p, [C.c_int]),
     "uq_rotation_signs": (None, [C.c_uint64, _i32, _vp]),
-    "uq_test_rotate": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _vp, _vp]),
+    "uq_test_rotate": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _i32, _vp, _vp]),
     "uq_test_quantize_rotated": (C.c_int, [_vp, _i64, _i32, _vp, _vp, _vp]),
     "uq_test_query_fp8": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _vp, _vp]),
     "uq_test_cvt_e4m3": (C.c_int, [_vp, _i64, _vp, _vp]),
@@ -339,11 +339,12 @@ def uq_rotation_signs(seed: int, d: int):
     return list(buf)
 
 
-def uq_test_rotate(x: torch.Tensor, seed: int = DEFAULT_SEED, stream=None) -> torch.Tensor:
+def uq_test_rotate(x: torch.Tensor, seed: int = DEFAULT_SEED, inverse: bool = False, stream=None) -> torch.Tensor:
     _need(x, torch.float32, "x")
     y = torch.empty_like(x)
     d = x.shape[-1]
-    _check(_lib.uq_test_rotate(_ptr(x), x.numel() // d, d, seed, _ptr(y), _stream(stream)), "uq_test_rotate")
+    _check(_lib.uq_test_rotate(_ptr(x), x.numel() // d, d, seed, int(inverse), _ptr(y), _stream(stream)),
+           "uq_test_rotate")
     return y
 
 

@@ -344,10 +344,13 @@ void uq_rotation_signs(uint64_t seed, int32_t d, int8_t* host_out) {
   for (int32_t i = 0; i < d; ++i) host_out[i] = (uqh::splitmix64_at(seed, i) >> 63) ? -1 : 1;
 }
 
-uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, float* y, cudaStream_t stream) {
+uq_status uq_test_rotate(const float* x, int64_t n_vec, int32_t d, uint64_t seed, int32_t inverse, float* y,
+                         cudaStream_t stream) {
   if ((d != 64 && d != 128 && d != 256) || n_vec < 0) return UQ_ERR_UNSUPPORTED;
+  if (inverse != 0 && inverse != 1) return UQ_ERR_INVALID_ARG;
   if (n_vec == 0) return UQ_OK;
   if (!x || !y) return UQ_ERR_INVALID_ARG;
+  if (inverse) return uqh::launch_inverse_rotate(x, n_vec, d, seed, y, stream);
   return uqh::launch_test_rotate(x, n_vec, d, seed, y, stream);
 }
 
@@ -366,7 +369,7 @@ uq_status uq_test_query_fp8(const void* q, int64_t n_vec, int32_t d, uint64_t se
   if (n_vec == 0) return UQ_OK;
   if (!q || !out) return UQ_ERR_INVALID_ARG;
   if (!aligned16(q)) return UQ_ERR_ALIGNMENT;
-  return uqh::launch_test_query_fp8(q, n_vec, d, seed, out, stream);
+  return uqh::launch_query_fp8(q, n_vec, d, seed, out, stream);
 }
 
 uq_status uq_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t stream) {

@@ -17,9 +17,11 @@
 //     touches; a small merge kernel combines them by log-sum-exp and applies
 //     the inverse rotation.
 //   * Each of the 4 warps of a block streams its own units through a ring of
-//     shared-memory stages filled by 1-D bulk copies (TMA engine) on mbarriers:
-//     one unit = 16 rows of K codes, V codes and their scale bytes
-//     (2176 bytes for head_dim 128), 136 bytes per token-head.
+//     shared-memory stages on mbarriers: one unit = 16 rows of K codes, V
+//     codes and their scale bytes (2176 bytes for head_dim 128), 136 bytes per
+//     token-head.  FP4 and TQ4 stages are filled by per-lane 16-byte (codes)
+//     and 4-byte (scales) cp.async copies; the FP8 and BF16 anchors' larger
+//     rows by two 1-D bulk copies (TMA engine) per unit.
 //   * QK^T and P.V run on the tensor cores as warp-level m16n8k16 f16 MMAs on
 //     operands built in registers by the hardware e2m1x2 -> f16x2 conversion.
 //     Keeping operands in registers avoids a second pass through shared
@@ -1416,32 +1418,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
     const float inv = 1.f / Ls;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= inv;
-    if (packed4(KIND)) {
-      // inverse rotation: s .* (H o) / sqrt(D); strides below EPL in-thread,
-      // the rest across lanes.
-#pragma unroll
-      for (int hs = 1; hs < EPL; hs <<= 1)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e)
-          if ((e & hs) == 0) {
-            const float a = o[e], bb = o[e + hs];
-            o[e] = a + bb;
-            o[e + hs] = a - bb;
-          }
-#pragma unroll
-      for (int k = 1; k < 32; k <<= 1) {
-        const bool upper = (lane & k) != 0;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          const float x = __shfl_xor_sync(kFull, o[e], k);
-          o[e] = upper ? (x - o[e]) : (o[e] + x);
-        }
-      }
-      const float sc = inv_sqrt_d<D>();
-#pragma unroll
-      for (int e = 0; e < EPL; ++e)
-        o[e] = __uint_as_float(__float_as_uint(o[e] * sc) ^ p.sign.m[lane * EPL + e]);
-    }
+    if (packed4(KIND)) inverse_rotate_warp<D>(o, lane, p.sign.m);  // out = R^T o
   }
   float* dst = p.out + row * D + lane * EPL;
 #pragma unroll
@@ -1449,9 +1426,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
   pdl_trigger();
 }
 
-// Test hook: the decode prologue alone.  One warp handles 8 query rows.
+// The rotated E4M3 query of n rows (the decode prologue on its own), for the
+// chunked-prefill and cascade paths and the query stage hook.  One warp
+// handles 8 query rows.
 template <int D>
-__global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out,
+__global__ void query_fp8_kernel(const uint16_t* q, int64_t n, uint8_t* out,
                                   const __grid_constant__ uqh::SignMasks sm) {
   const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8 + r;
@@ -1461,6 +1440,21 @@ __global__ void test_query_kernel(const uint16_t* q, int64_t n, uint8_t* out,
   if (valid)
     for (int e = 0; e < D / 16; ++e)
       *reinterpret_cast<uint32_t*>(out + row * D + c * (D / 4) + 4 * e) = bytes[e];
+}
+
+// Stage hook: the merge's inverse rotation alone, one fp32 row per warp.
+template <int D>
+__global__ void inverse_rotate_kernel(const float* x, int64_t n, float* y, const __grid_constant__ uqh::SignMasks sm) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= n) return;  // warp-uniform
+  float o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = x[row * D + lane * EPL + e];
+  inverse_rotate_warp<D>(o, lane, sm.m);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) y[row * D + lane * EPL + e] = o[e];
 }
 
 // ------------------------------------------------------------------ host
@@ -1631,17 +1625,30 @@ uq_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   }
 }
 
-uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out, cudaStream_t s) {
+uq_status launch_inverse_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y, cudaStream_t s) {
+  SignMasks sm;
+  make_sign_masks(seed, d, &sm);
+  const unsigned grid = (unsigned)((n + 3) / 4);
+  if (d == 256)
+    inverse_rotate_kernel<256><<<grid, 128, 0, s>>>(x, n, y, sm);
+  else if (d == 128)
+    inverse_rotate_kernel<128><<<grid, 128, 0, s>>>(x, n, y, sm);
+  else
+    inverse_rotate_kernel<64><<<grid, 128, 0, s>>>(x, n, y, sm);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out, cudaStream_t s) {
   SignMasks sm;
   make_sign_masks(seed, d, &sm);
   const int64_t warps = (n + 7) / 8;
   const unsigned grid = (unsigned)((warps + 3) / 4);
   if (d == 256)
-    test_query_kernel<256><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+    query_fp8_kernel<256><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
   else if (d == 128)
-    test_query_kernel<128><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+    query_fp8_kernel<128><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
   else
-    test_query_kernel<64><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
+    query_fp8_kernel<64><<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(q), n, out, sm);
   return cuda_status(cudaGetLastError());
 }
 

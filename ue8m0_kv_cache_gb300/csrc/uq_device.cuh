@@ -76,6 +76,38 @@ __device__ __forceinline__ void fwht_regs(float (&u)[N]) {
   }
 }
 
+// Inverse rotation of one row spread over a warp, lane l holding elements
+// l*EPL .. l*EPL+EPL-1 (EPL = D/32): o <- s .* fl32(FWHT_fp32(o) * fl32(1/sqrt D)),
+// the transpose of the forward rotation (H is symmetric).  Butterfly strides
+// ascend: those below EPL inside the lane, the rest across lanes by xor
+// shuffles; the lower element of a pair becomes fl32(a+b), the upper fl32(a-b).
+// sign_m[i] is the sign bit (0 or 0x80000000) of s_i.  Every lane must call it.
+template <int D>
+__device__ __forceinline__ void inverse_rotate_warp(float (&o)[D / 32], int lane, const uint32_t* sign_m) {
+  constexpr int EPL = D / 32;
+#pragma unroll
+  for (int hs = 1; hs < EPL; hs <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if ((e & hs) == 0) {
+        const float a = o[e], b = o[e + hs];
+        o[e] = a + b;
+        o[e + hs] = a - b;
+      }
+#pragma unroll
+  for (int k = 1; k < 32; k <<= 1) {
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const float x = __shfl_xor_sync(kFull, o[e], k);
+      o[e] = upper ? (x - o[e]) : (o[e] + x);
+    }
+  }
+  const float sc = inv_sqrt_d<D>();
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = __uint_as_float(__float_as_uint(o[e] * sc) ^ sign_m[lane * EPL + e]);
+}
+
 // max(|a|, |b|) with NaN propagation (the sign of the result is meaningless;
 // callers take fabsf at the end).
 __device__ __forceinline__ float max_abs_nan(float a, float b) {

@@ -80,6 +80,7 @@ uq_status launch_append_fp4(const void* k, const void* v, bool in_fp32, int64_t 
                             const int64_t* slots, const uq_cache& c, cudaStream_t s);  // FP4 and TQ4
 uq_status launch_append_anchor(const void* k, const void* v, bool in_fp32, int64_t ntok,
                                const int64_t* slots, const uq_cache& c, cudaStream_t s);
+uq_status launch_inverse_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y, cudaStream_t s);
 uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, float* y,
                              cudaStream_t s);
 uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
@@ -133,7 +134,7 @@ struct DecodeArgs {
 size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas);
 int decode_max_ctas();
 uq_status launch_decode(const DecodeArgs& a, cudaStream_t s);
-uq_status launch_test_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out,
+uq_status launch_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out,
                                 cudaStream_t s);
 
 // Chunked-prefill attention (uq_prefill.cu).

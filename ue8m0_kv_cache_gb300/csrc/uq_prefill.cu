@@ -770,27 +770,7 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
     const float inv = 1.f / Ls;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= inv;
-#pragma unroll
-    for (int hs = 1; hs < EPL; hs <<= 1)
-#pragma unroll
-      for (int e = 0; e < EPL; ++e)
-        if ((e & hs) == 0) {
-          const float x = o[e], y = o[e + hs];
-          o[e] = x + y;
-          o[e + hs] = x - y;
-        }
-#pragma unroll
-    for (int k = 1; k < 32; k <<= 1) {
-      const bool upper = (lane & k) != 0;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float x = __shfl_xor_sync(kFull, o[e], k);
-        o[e] = upper ? (x - o[e]) : (o[e] + x);
-      }
-    }
-    const float sc = inv_sqrt_d<D>();
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = __uint_as_float(__float_as_uint(o[e] * sc) ^ p.sign.m[lane * EPL + e]);
+    inverse_rotate_warp<D>(o, lane, p.sign.m);  // out = R^T o
   }
   float* dst = p.out + row * D + lane * EPL;
 #pragma unroll
@@ -928,7 +908,7 @@ uq_status run_prefill(const uqh::PrefillArgs& a, cudaStream_t s) {
   prefill_plan_kernel<<<1, 32, 0, s>>>(a.cu_q, a.seq_lens, a.batch, G, c.num_kv_heads, pl.splits, 0, kItemRows,
                                        nullptr, 0, cap, grid, p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
-  uq_status st = uqh::launch_test_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
+  uq_status st = uqh::launch_query_fp8(a.q, static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads, D,
                                             c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
   st = launch_items<D>(p, grid, s);
@@ -974,7 +954,7 @@ uq_status run_cascade_prefix(const void* q, const uq_cache& c, const int32_t* bl
   prefill_plan_kernel<<<1, 32, 0, s>>>(cg.cu, nullptr, cg.groups, G, c.num_kv_heads, pl.splits, pl.splits,
                                        kItemRows, cg.prefix, cg.min_rows, cg.cap, grid, p.item_pre);
   if (cudaGetLastError() != cudaSuccess) return UQ_ERR_CUDA;
-  uq_status st = uqh::launch_test_query_fp8(q, static_cast<int64_t>(batch) * hq, D, c.rot_seed, ws + pl.off_q, s);
+  uq_status st = uqh::launch_query_fp8(q, static_cast<int64_t>(batch) * hq, D, c.rot_seed, ws + pl.off_q, s);
   if (st != UQ_OK) return st;
   st = launch_items<D>(p, grid, s);
   if (st != UQ_OK) return st;
