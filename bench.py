@@ -32,6 +32,8 @@ FP4_BYTES_PER_TOKEN_HEAD = 136   # K and V: 64 code bytes + 4 scale bytes each
 FP8_BYTES_PER_TOKEN_HEAD = 256
 BF16_BYTES_PER_TOKEN_HEAD = 512
 PF_CHUNK = 128                   # prefill chunk per sequence in the prefill measurement
+REPEAT_S = 0.5                   # each timed region repeats its K steps until it lasts this long
+MAX_REPEATS = 400
 METRIC = "decode tokens/s at 64K ctx (KV-read GB/s and quantize GB/s reported)"
 WORKLOAD = "append64k: B8 Hkv8 Hq64 D128 ps16, 32768 cached + 32768 appended tokens/seq, then decode steps"
 
@@ -189,39 +191,62 @@ def _pci_bus_id(dev):
         return None
 
 
-def _cpu_baseline(w, seconds_hint=True):
-    """The oracle, as it stands, decoding one sequence (all 8 kv heads, 64 query
-    heads) at 64K context on this host's cores: once on one thread, and once with
-    one thread per kv head (the C oracle runs outside the interpreter lock)."""
+def _cpu_baseline(w):
+    """The oracle, as it stands, on this host's cores.  Decode: (sequence, kv
+    head) pairs of the 64K workload (8 query heads each) spread over one thread
+    per core -- ceil(cores / 8) sequences, so every core has a pair -- and one
+    pair on one thread.  Quantize: the oracle's append of a token range of the
+    workload, chunked over one thread per core, and on one thread.  The C calls
+    run outside the interpreter lock."""
     from concurrent.futures import ThreadPoolExecutor
     import oracle
+    cores = os.cpu_count() or 1
     L = CTX0 + APPEND
-    seq = 0
-    k, v = w.kv(seq, 0, L, device="cpu")
+    G = HQ // HKV
     to16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    q = to16(w.q(0, device="cpu")[seq:seq + 1])
+    n_seq = (cores + HKV - 1) // HKV
     bt = np.arange(L // PS, dtype=np.int32)[None]
     sl = np.array([L], np.int32)
-    oc = oracle.Cache(oracle.KIND_FP4, L // PS, HKV, PS, D)
-    oc.append(to16(k), to16(v), np.arange(L))
+    pairs = []
+    for seq in range(n_seq):
+        k, v = w.kv(seq, 0, L, device="cpu")
+        q = to16(w.q(0, device="cpu")[seq:seq + 1])
+        for h in range(HKV):  # one single-head cache per (sequence, kv head), its G query heads
+            c = oracle.Cache(oracle.KIND_FP4, L // PS, 1, PS, D)
+            c.append(to16(k[:, h:h + 1]), to16(v[:, h:h + 1]), np.arange(L))
+            pairs.append((c, np.ascontiguousarray(q[:, h * G:(h + 1) * G])))
+    run = lambda cq: cq[0].decode(cq[1], bt, sl)
     t0 = time.perf_counter()
-    oc.decode(q, bt, sl)
+    run(pairs[0])
     dt1 = time.perf_counter() - t0
-    G = HQ // HKV
-    heads = []
-    for h in range(HKV):  # one single-head cache per kv head, its G query heads
-        c = oracle.Cache(oracle.KIND_FP4, L // PS, 1, PS, D)
-        c.append(to16(k[:, h:h + 1]), to16(v[:, h:h + 1]), np.arange(L))
-        heads.append((c, np.ascontiguousarray(q[:, h * G:(h + 1) * G])))
-    threads = min(HKV, os.cpu_count() or 1)
-    with ThreadPoolExecutor(max_workers=threads) as ex:
+    with ThreadPoolExecutor(max_workers=cores) as ex:
         t0 = time.perf_counter()
-        list(ex.map(lambda cq: cq[0].decode(cq[1], bt, sl), heads))
+        list(ex.map(run, pairs))
         dtn = time.perf_counter() - t0
-    return {"value": 1.0 / dtn, "unit": "decode tokens/s", "cores": threads, "kind": "oracle",
-            "sample": "1 sequence x 8 kv heads x 64 query heads at context %d (FP4 cache, fp64 attention), C oracle, "
-                      "one thread per kv head: %.2f s; single thread: %.2f s" % (L, dtn, dt1),
-            "single_thread": {"value": 1.0 / dt1, "cores": 1}}
+    # quantize leg: T tokens x 8 kv heads of sequence 0, bf16 in, FP4 out
+    T = 8192
+    k, v = w.kv(0, 0, T, device="cpu")
+    k16, v16 = to16(k), to16(v)
+    qbytes = T * HKV * (2 * D * 2 + FP4_BYTES_PER_TOKEN_HEAD) + T * 8
+    c1 = oracle.Cache(oracle.KIND_FP4, T // PS, HKV, PS, D)
+    t0 = time.perf_counter()
+    c1.append(k16, v16, np.arange(T))
+    qt1 = time.perf_counter() - t0
+    chunk = (T + cores - 1) // cores
+    chunks = [(i, min(T, i + chunk)) for i in range(0, T, chunk)]
+    cn = oracle.Cache(oracle.KIND_FP4, T // PS, HKV, PS, D)
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(lambda r: cn.append(k16[r[0]:r[1]], v16[r[0]:r[1]], np.arange(r[0], r[1])), chunks))
+        qtn = time.perf_counter() - t0
+    return {"value": n_seq / dtn, "unit": "decode tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d sequences x 8 kv heads (8 query heads each) at context %d, FP4 cache, fp64 attention, "
+                      "C oracle, one thread per (sequence, kv head) on %d threads: %.2f s; one pair on one "
+                      "thread: %.2f s; quantize-append of %d tokens x 8 kv heads: %.2f s on %d threads, "
+                      "%.2f s on one" % (n_seq, L, cores, dtn, dt1, T, qtn, cores, qt1),
+            "single_thread": {"value": 1.0 / (dt1 * HKV), "unit": "decode tokens/s", "cores": 1},
+            "quantize": {"GB_per_s": qbytes / qtn / 1e9, "cores": cores,
+                         "single_thread_GB_per_s": qbytes / qt1 / 1e9}}
 
 
 def run_reference(args):
@@ -332,12 +357,15 @@ def run_uq(args):
     n_th = B * APPEND * HKV
     q_in, q_out = n_th * 2 * D * 2, n_th * FP4_BYTES_PER_TOKEN_HEAD + B * APPEND * 8
     q_t = time_append(fp4)
+    hbm0, _ = _peaks()
     quantize = {"GB_per_s": (q_in + q_out) / q_t / 1e9, "ms": q_t * 1e3, "tokens": B * APPEND,
-                "bytes_in": q_in, "bytes_out": q_out, "launches": 1}
+                "bytes_in": q_in, "bytes_out": q_out, "launches": 1,
+                "frac": (q_in + q_out) / q_t / 1e9 / hbm0, "peak": hbm0}
     tq4_quantize = None
     if "tq4" in caches:  # the codebook variant writes the same 136 B per token-head
         tq_t = time_append(caches["tq4"])
-        tq4_quantize = {"GB_per_s": (q_in + q_out) / tq_t / 1e9, "ms": tq_t * 1e3}
+        tq4_quantize = {"GB_per_s": (q_in + q_out) / tq_t / 1e9, "ms": tq_t * 1e3,
+                        "frac": (q_in + q_out) / tq_t / 1e9 / hbm0}
     del kA, vA, sA, l2_flush
     assert uq.uq_check_device_status() == 0
 
@@ -379,31 +407,43 @@ def run_uq(args):
                 timed_decode.append((e0, e1))
 
     def timed(name, clocks=None):
+        """W warm-up steps, then R repeats of exactly the K timed steps (each repeat
+        replays the same K steps: the same new tokens into the same slots at the
+        same contexts, so every repeat does identical work), R chosen so the timed
+        region lasts >= REPEAT_S.  Returns (median repeat s, median decode launch s,
+        repeat times, clocks)."""
         decode_loop(name, warmup, 0, None)
         torch.cuda.synchronize()
+        t0, t1 = _event_pair()  # one untimed repeat sizes R
+        t0.record(stream)
+        decode_loop(name, steps, warmup, None)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        reps = int(min(MAX_REPEATS, max(1, np.ceil(REPEAT_S / max(t0.elapsed_time(t1) * 1e-3, 1e-6)))))
         if ws > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         if clocks:
             clocks.start()
-        ev = []
-        t0, t1 = _event_pair()
-        t0.record(stream)
-        decode_loop(name, steps, warmup, ev)
-        t1.record(stream)
+        ev, rep_ev = [], []
+        for _ in range(reps):
+            r0, r1 = _event_pair()
+            r0.record(stream)
+            decode_loop(name, steps, warmup, ev)
+            r1.record(stream)
+            rep_ev.append((r0, r1))
         torch.cuda.synchronize()
-        if clocks:
-            clk = clocks.stop()
+        clk = clocks.stop() if clocks else None
         if ws > 1:
             torch.distributed.barrier()
-        total = t0.elapsed_time(t1) * 1e-3
-        dec = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e-3
-        return total, dec, (clk if clocks else None)
+        rep = [a.elapsed_time(b) * 1e-3 for a, b in rep_ev]
+        dec = float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e-3
+        return float(np.median(rep)), dec, rep, clk
 
     clocks = Clocks(local if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0, _pci_bus_id(dev))
-    total, dec_t, clk = timed("fp4", clocks)
+    rep_t, dec_t, rep_all, clk = timed("fp4", clocks)
     assert uq.uq_check_device_status() == 0
-    total = _max_over_ranks(total, ws, dev)
+    total = _max_over_ranks(rep_t, ws, dev)  # one repeat of the K steps, slowest rank
     ctx_mean = L0 + warmup + (steps + 1) / 2.0
     kv_bytes = B * HKV * ctx_mean * FP4_BYTES_PER_TOKEN_HEAD
     hbm, peak_kind = _peaks()
@@ -414,16 +454,23 @@ def run_uq(args):
                 "traffic": _captured_traffic(B * HKV * ctx_mean), "peak_kind": peak_kind,
                 "kernel": "uq_decode_attention_append (fused append + decode, then merge), FP4 cache",
                 "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_t * 1e3,
+                "launch_ms_stat": "median over %d launches" % (len(rep_all) * steps),
                 "frac_of_nominal_8TBps": achieved / 8000.0}
+    timing = {"repeats": len(rep_all), "steps_per_repeat": steps, "repeat_ms_median": rep_t * 1e3,
+              "repeat_ms_min": min(rep_all) * 1e3, "repeat_ms_max": max(rep_all) * 1e3,
+              "timed_region_s": float(sum(rep_all)),
+              "note": "value and ms_per_step from the median repeat of the K steps; every repeat replays the same "
+                      "K steps (same tokens, slots and contexts)"}
 
     anchors = {}
     for name, per in (("fp8", FP8_BYTES_PER_TOKEN_HEAD), ("bf16", BF16_BYTES_PER_TOKEN_HEAD),
                       ("tq4", FP4_BYTES_PER_TOKEN_HEAD)):
         if name not in caches:
             continue
-        tt, dt, _ = timed(name)
+        tt, dt, _, _ = timed(name)
+        gbs = B * HKV * ctx_mean * per / dt / 1e9
         anchors[name] = {"decode_tokens_per_s": B * steps / tt, "ms_per_step": tt / steps * 1e3,
-                         "decode_ms": dt * 1e3, "kv_GB_per_s": B * HKV * ctx_mean * per / dt / 1e9}
+                         "decode_ms": dt * 1e3, "kv_GB_per_s": gbs, "frac": gbs / hbm}
         if name == "tq4":
             anchors[name]["quantize"] = tq4_quantize
     assert uq.uq_check_device_status() == 0
@@ -462,32 +509,51 @@ def run_uq(args):
         del qp, wsp_p, outp
     assert uq.uq_check_device_status() == 0
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: the same K steps (same
+    # tokens, slots, contexts) with each step's inputs copied from pinned host memory and
+    # its output read back, repeated like the device-timed region
     n_e2e = min(steps, 200)
     pin = lambda t: t.cpu().pin_memory()
-    hk = [pin(newk[s]) for s in range(n_e2e)]
-    hv = [pin(newv[s]) for s in range(n_e2e)]
-    hs = [pin(news[s]) for s in range(n_e2e)]
-    hq = [pin(qs[s]) for s in range(n_e2e)]
+    idx = list(range(warmup, warmup + n_e2e))
+    hk = [pin(newk[s]) for s in idx]
+    hv = [pin(newv[s]) for s in idx]
+    hs = [pin(news[s]) for s in idx]
+    hq = [pin(qs[s]) for s in idx]
     hout = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
     dk, dv, dsl, dq = (torch.empty_like(newk[0]), torch.empty_like(newv[0]), torch.empty_like(news[0]),
                        torch.empty_like(qs[0]))
+
+    def e2e_pass():
+        for i, s in enumerate(idx):
+            dk.copy_(hk[i], non_blocking=True)
+            dv.copy_(hv[i], non_blocking=True)
+            dsl.copy_(hs[i], non_blocking=True)
+            dq.copy_(hq[i], non_blocking=True)
+            uq.uq_decode_attention_append(dq, dk, dv, dsl, fp4, bt, lens[s], out=out, workspace=wsp)
+            hout.copy_(out, non_blocking=True)
+
+    e2e_pass()
     torch.cuda.synchronize()
-    t0, t1 = _event_pair()
-    t0.record(stream)
-    for s in range(n_e2e):
-        dk.copy_(hk[s], non_blocking=True)
-        dv.copy_(hv[s], non_blocking=True)
-        dsl.copy_(hs[s], non_blocking=True)
-        dq.copy_(hq[s], non_blocking=True)
-        uq.uq_decode_attention_append(dq, dk, dv, dsl, fp4, bt, lens[s], out=out, workspace=wsp)
-        hout.copy_(out, non_blocking=True)
-    t1.record(stream)
+    e2e_rep = []
+    for _ in range(len(rep_all)):
+        t0, t1 = _event_pair()
+        t0.record(stream)
+        e2e_pass()
+        t1.record(stream)
+        e2e_rep.append((t0, t1))
     torch.cuda.synchronize()
-    e2e_t = t0.elapsed_time(t1) * 1e-3
+    e2e_t = _max_over_ranks(float(np.median([a.elapsed_time(b) * 1e-3 for a, b in e2e_rep])), ws, dev)
     h2d = dk.numel() * 2 + dv.numel() * 2 + dsl.numel() * 8 + dq.numel() * 2
     e2e = {"value": ws * B * n_e2e / e2e_t, "unit": "decode tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": hout.numel() * 4, "steps": n_e2e}
+           "d2h_bytes_per_step": hout.numel() * 4, "steps": n_e2e, "repeats": len(e2e_rep),
+           "stat": "median repeat"}
+    assert uq.uq_check_device_status() == 0
+
+    # ---- the mixed-length serving batch (B 64, seq_len ~ U[8192, 65536]), decode only
+    mixed = None
+    if not args.no_anchors:
+        mixed = _mixed_decode(uq, dev, stream, steps, warmup, hbm, peak_kind)
+    assert uq.uq_check_device_status() == 0
 
     if rank != 0:
         return
@@ -505,8 +571,66 @@ def run_uq(args):
                        "parallelism": "replicas (weak scaling, no collective)" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (FP4 KV read %.0f MB per step)" % (kv_bytes / 1e6)},
             "kv_GB_per_s": achieved, "quantize": quantize, "anchors": anchors, "prefill": prefill, "roofline": roofline,
-            "clocks": clk, "e2e": e2e, "gpu_launches": 2 * steps, "cpu_baseline": cpu}
+            "timing": timing, "mixed": mixed, "clocks": clk, "e2e": e2e,
+            "gpu_launches": 2 * steps * len(rep_all), "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
+
+
+def _mixed_decode(uq, dev, stream, steps, warmup, hbm, peak_kind):
+    """Decode of the mixed-length serving batch: 64 sequences, 8 kv heads, 64 query
+    heads, seq_len ~ U[8192, 65536] (seeded), 1% of tokens x8, shuffled pages.  The
+    cache is filled untimed; each step decodes one query token per sequence (decode +
+    merge launches); R repeats of K steps as the main line."""
+    import workloads
+    w = workloads.make("mixed")
+    cache = uq.KVCache(uq.FP4_UE8M0, w.num_pages, w.Hkv, w.ps, w.D, device=dev)
+    for b in range(w.B):
+        for t0 in range(0, w.seq_lens[b], 8192):
+            n = min(8192, w.seq_lens[b] - t0)
+            k, v = w.kv(b, t0, n, device=dev)
+            uq.uq_quantize_append(k, v, torch.from_numpy(w.slots(b, t0, n)).to(dev), cache)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+    qs = [w.q(s, device=dev) for s in range(4)]
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    wsp = uq.workspace(w.B, w.Hq, w.Hkv, w.D, dev)
+
+    def run(n, ev):
+        for s in range(n):
+            if ev is not None:
+                e0, e1 = _event_pair()
+                e0.record(stream)
+            uq.uq_decode_attention(qs[s % 4], cache, bt, sl, out=out, workspace=wsp)
+            if ev is not None:
+                e1.record(stream)
+                ev.append((e0, e1))
+
+    run(warmup, None)
+    torch.cuda.synchronize()
+    t0, t1 = _event_pair()
+    t0.record(stream)
+    run(steps, None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    reps = int(min(MAX_REPEATS, max(1, np.ceil(REPEAT_S / max(t0.elapsed_time(t1) * 1e-3, 1e-6)))))
+    ev, rep = [], []
+    for _ in range(reps):
+        r0, r1 = _event_pair()
+        r0.record(stream)
+        run(steps, ev)
+        r1.record(stream)
+        rep.append((r0, r1))
+    torch.cuda.synchronize()
+    rt = float(np.median([a.elapsed_time(b) * 1e-3 for a, b in rep]))
+    dt = float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e-3
+    kv = sum(w.seq_lens) * w.Hkv * FP4_BYTES_PER_TOKEN_HEAD
+    res = {"workload": "mixed: B64 Hkv8 Hq64 D128 ps16, seq_len ~ U[8192, 65536] (%d tokens), 1%% of tokens x8"
+                       % sum(w.seq_lens),
+           "decode_tokens_per_s": w.B * steps / rt, "ms_per_step": rt / steps * 1e3, "launch_ms": dt * 1e3,
+           "kv_GB_per_s": kv / dt / 1e9, "frac": kv / dt / 1e9 / hbm, "peak": hbm, "peak_kind": peak_kind,
+           "repeats": reps, "l2": "inputs larger than L2 (%.2f GB per step)" % (kv / 1e9)}
+    del cache, wsp
+    return res
 
 
 def _captured_traffic(token_heads):

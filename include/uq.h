@@ -365,9 +365,11 @@ uq_status uq_tq_codebook(int32_t head_dim, int32_t bits, float* magnitudes, floa
  *   - Batch shapes whose smallest workspace exceeds 8 MiB (roughly more than
  *     2000 (sequence, kv head) pairs at head_dim 128) return UQ_ERR_WORKSPACE
  *     before anything is enqueued; use uq_decode_attention for those.
+ *   - batch > 4096 returns UQ_ERR_UNSUPPORTED, as uq_decode_attention does.
  *   - The first call on a device looks up the scratch array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *     (with that device current), and so does the first call after the
+ *     device's context was replaced (cudaDeviceReset); make such a call before
+ *     any stream capture.
  *   - All calls on a device share the one scratch array, and it keeps the last
  *     call's contents.  Nothing in it needs to start at zero: every entry a
  *     call reads was written earlier in the same call.  Calls that overlap on
@@ -380,7 +382,11 @@ uq_status uq_decode_attention_noalloc(const void* q, const uq_cache* cache, cons
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns UQ_OK, UQ_ERR_DEVICE_TIMEOUT or UQ_ERR_DEVICE_BOUNDS (the
- * first error recorded since the last call), or UQ_ERR_CUDA. */
+ * first error recorded since the last call), or UQ_ERR_CUDA.  After
+ * UQ_ERR_DEVICE_TIMEOUT the outputs of the calls since the previous check are
+ * undefined (a block that gave up left its part of the result unwritten);
+ * after UQ_ERR_DEVICE_BOUNDS the offending accesses were skipped or clamped as
+ * each entry point describes. */
 uq_status uq_check_device_status(cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
@@ -415,6 +421,19 @@ uq_status uq_test_query_fp8(const void* q, int64_t n_vec, int32_t d, uint64_t se
 
 /* E4M3 round-to-nearest-even, saturating, of n fp32 values (n even). */
 uq_status uq_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
+
+/* The append's E2M1 conversion alone ([UQ-review] §3.1: values rounded to the
+ * nearest FP4 E2M1 grid point): codes[i] = code of r[i] (device fp32 [n], n
+ * even), round to nearest with ties to the even code, saturating at +-6;
+ * bits 0..2 the magnitude rank of {0, .5, 1, 1.5, 2, 3, 4, 6}, bit 3 the IEEE
+ * sign bit of r[i].  This is the conversion the append applies to y * 2^-E. */
+uq_status uq_test_cvt_e2m1(const float* r, int64_t n, uint8_t* codes, cudaStream_t stream);
+
+/* The append's UE8M0 scale byte alone ([UQ-review] §3.1/§3.3): bytes[i] = the
+ * byte of a 32-channel group whose absolute maximum is |m[i]| (device fp32
+ * [n]): E = integer nearest to log2(fl32(0.156f * |m|)), byte = clamp(E + 127,
+ * 0, 254); 0 for m = 0; 0xFF for a NaN or infinite m. */
+uq_status uq_test_scale_byte(const float* m, int64_t n, uint8_t* bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -288,6 +288,26 @@ _lib.uqo_group_mse.argtypes = [_f32p, C.c_int64, C.c_float, C.c_int]
 ROUND_CONTINUOUS = -1
 
 
+_lib.uqo_e2m1_codes_bits.argtypes = [C.c_uint32, C.c_int64, _u8p]
+_lib.uqo_scale_bytes_bits.argtypes = [C.c_uint32, C.c_int64, C.c_float, _u8p]
+
+
+def e2m1_codes_of_bits(first: int, n: int) -> np.ndarray:
+    """R3 code of the fp32 values with bit patterns first .. first + n - 1 (NaN: 0xFF)."""
+    assert 0 <= first and first + n <= 1 << 32
+    out = np.empty(n, np.uint8)
+    _lib.uqo_e2m1_codes_bits(first, n, out)
+    return out
+
+
+def scale_bytes_of_bits(first: int, n: int, c: float = None) -> np.ndarray:
+    """R2 byte of a group with absolute maximum |value| for the fp32 bit patterns first .. first + n - 1."""
+    assert 0 <= first and first + n <= 1 << 32
+    out = np.empty(n, np.uint8)
+    _lib.uqo_scale_bytes_bits(first, n, np.float32(C_CONSTANT if c is None else c), out)
+    return out
+
+
 def e2m1_codes(r: np.ndarray) -> np.ndarray:
     r = _c(r, np.float64).reshape(-1)
     out = np.empty(r.size, np.uint8)

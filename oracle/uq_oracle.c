@@ -598,6 +598,28 @@ void uqo_e2m1_codes(const double* r, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)uqo_e2m1_code(r[i]);
 }
 
+/* Enumerations for the exhaustive tests: element i is the fp32 value whose   */
+/* bit pattern is first + i (the caller keeps first + n - 1 <= 0xFFFFFFFF).   */
+/* R3 of that value, read exactly as a double; a NaN pattern gives 0xFF.      */
+void uqo_e2m1_codes_bits(uint32_t first, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t b = first + (uint32_t)i;
+    float f;
+    memcpy(&f, &b, 4);
+    out[i] = isnan(f) ? 0xFF : (uint8_t)uqo_e2m1_code((double)f);
+  }
+}
+
+/* R2 with the pages' constant for a group whose absolute maximum is |value|. */
+void uqo_scale_bytes_bits(uint32_t first, int64_t n, float c, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t b = first + (uint32_t)i;
+    float f;
+    memcpy(&f, &b, 4);
+    out[i] = (uint8_t)uqo_scale_byte(fabsf(f), c, 0);
+  }
+}
+
 void uqo_e4m3_codes(const float* x, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)uqo_e4m3_code(x[i]);
 }

@@ -97,6 +97,10 @@ def test_argument_validation_without_a_device():
     s.k_scale = 0.0
     assert _decode(s, fn=uq._lib.uq_decode_attention_fp8) == E["UQ_ERR_INVALID_ARG"]
     assert uq._lib.uq_test_cvt_e4m3(0x200000, 3, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert uq._lib.uq_test_cvt_e2m1(0x200000, 3, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert uq._lib.uq_test_cvt_e2m1(0, 2, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert uq._lib.uq_test_scale_byte(0x200000, -1, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
+    assert uq._lib.uq_test_scale_byte(0x200000, 0, 0x300000, None) == E["UQ_OK"]
     assert uq._lib.uq_test_rotate(0x200000, 4, 96, 0, 0, 0x300000, None) == E["UQ_ERR_UNSUPPORTED"]
     assert uq._lib.uq_test_rotate(0x200000, 4, 128, 0, 2, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]
     assert uq._lib.uq_test_rotate(0x200000, 4, 128, 0, -1, 0x300000, None) == E["UQ_ERR_INVALID_ARG"]

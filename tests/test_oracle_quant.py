@@ -180,3 +180,14 @@ def test_c_sweep_soft_pin():
     assert abs(c_lin - 0.195) > 0.008, c_lin
     # raw absmax (c = 1) is far worse than the shrunk constant
     assert oracle.group_mse(y, 1.0, oracle.ROUND_LOG2) > 3 * oracle.group_mse(y, 0.156, oracle.ROUND_LOG2)
+
+
+def test_bit_pattern_enumerations_agree_with_the_array_forms():
+    # the exhaustive GPU checks read the oracle through these enumerators
+    first = 0x3E000000
+    vals = np.arange(first, first + 50000, dtype=np.uint32).view(np.float32)
+    assert np.array_equal(oracle.e2m1_codes_of_bits(first, 50000), oracle.e2m1_codes(vals.astype(np.float64)))
+    assert np.array_equal(oracle.scale_bytes_of_bits(first, 50000), oracle.scale_bytes(vals))
+    neg = np.arange(0xC0000000, 0xC0000000 + 1000, dtype=np.uint32).view(np.float32)
+    assert np.array_equal(oracle.scale_bytes_of_bits(0xC0000000, 1000), oracle.scale_bytes(np.abs(neg)))
+    assert oracle.e2m1_codes_of_bits(0x7FC00000, 1)[0] == 0xFF  # NaN pattern

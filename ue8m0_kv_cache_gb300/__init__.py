@@ -68,6 +68,8 @@ _sig = {
     "uq_test_quantize_rotated": (C.c_int, [_vp, _i64, _i32, _vp, _vp, _vp]),
     "uq_test_query_fp8": (C.c_int, [_vp, _i64, _i32, C.c_uint64, _vp, _vp]),
     "uq_test_cvt_e4m3": (C.c_int, [_vp, _i64, _vp, _vp]),
+    "uq_test_cvt_e2m1": (C.c_int, [_vp, _i64, _vp, _vp]),
+    "uq_test_scale_byte": (C.c_int, [_vp, _i64, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -365,6 +367,22 @@ def uq_test_query_fp8(q: torch.Tensor, seed: int = DEFAULT_SEED, stream=None) ->
     out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
     _check(_lib.uq_test_query_fp8(_ptr(q), q.numel() // d, d, seed, _ptr(out), _stream(stream)),
            "uq_test_query_fp8")
+    return out
+
+
+def uq_test_cvt_e2m1(r: torch.Tensor, stream=None) -> torch.Tensor:
+    """E2M1 code (uint8, low nibble) of each fp32 value (even count)."""
+    _need(r, torch.float32, "r")
+    out = torch.empty(r.shape, dtype=torch.uint8, device=r.device)
+    _check(_lib.uq_test_cvt_e2m1(_ptr(r), r.numel(), _ptr(out), _stream(stream)), "uq_test_cvt_e2m1")
+    return out
+
+
+def uq_test_scale_byte(m: torch.Tensor, stream=None) -> torch.Tensor:
+    """UE8M0 scale byte of a group with absolute maximum |m| for each fp32 value."""
+    _need(m, torch.float32, "m")
+    out = torch.empty(m.shape, dtype=torch.uint8, device=m.device)
+    _check(_lib.uq_test_scale_byte(_ptr(m), m.numel(), _ptr(out), _stream(stream)), "uq_test_scale_byte")
     return out
 
 

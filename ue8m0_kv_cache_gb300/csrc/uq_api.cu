@@ -372,6 +372,20 @@ uq_status uq_test_query_fp8(const void* q, int64_t n_vec, int32_t d, uint64_t se
   return uqh::launch_query_fp8(q, n_vec, d, seed, out, stream);
 }
 
+uq_status uq_test_cvt_e2m1(const float* r, int64_t n, uint8_t* codes, cudaStream_t stream) {
+  if (n < 0 || (n & 1)) return UQ_ERR_INVALID_ARG;
+  if (n == 0) return UQ_OK;
+  if (!r || !codes) return UQ_ERR_INVALID_ARG;
+  return uqh::launch_test_cvt_e2m1(r, n, codes, stream);
+}
+
+uq_status uq_test_scale_byte(const float* m, int64_t n, uint8_t* bytes, cudaStream_t stream) {
+  if (n < 0) return UQ_ERR_INVALID_ARG;
+  if (n == 0) return UQ_OK;
+  if (!m || !bytes) return UQ_ERR_INVALID_ARG;
+  return uqh::launch_test_scale_byte(m, n, bytes, stream);
+}
+
 uq_status uq_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t stream) {
   if (n < 0 || (n & 1)) return UQ_ERR_INVALID_ARG;
   if (n == 0) return UQ_OK;

@@ -610,6 +610,22 @@ __global__ void test_cvt_e4m3_kernel(const float* x, int64_t n2, uint16_t* out) 
   if (i < n2) out[i] = static_cast<uint16_t>(cvt_e4m3x2(x[2 * i], x[2 * i + 1]));
 }
 
+// Stage hooks for R3 and R2 alone: the append's own conversion and scale-byte
+// device functions applied to raw values.
+__global__ void test_cvt_e2m1_kernel(const float* r, int64_t n2, uint8_t* out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i < n2) {
+    const uint32_t b = cvt_e2m1x2(r[2 * i], r[2 * i + 1]);
+    out[2 * i] = static_cast<uint8_t>(b & 15u);
+    out[2 * i + 1] = static_cast<uint8_t>(b >> 4);
+  }
+}
+
+__global__ void test_scale_byte_kernel(const float* m, int64_t n, uint8_t* out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i < n) out[i] = static_cast<uint8_t>(scale_byte(fabsf(m[i])));
+}
+
 // ------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -810,6 +826,17 @@ uq_status launch_calibrate(const void* x, bool in_fp32, int64_t n, int d, uint64
     calibrate_kernel<128><<<grid, 128, 0, s>>>(p);
   else
     calibrate_kernel<64><<<grid, 128, 0, s>>>(p);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_test_cvt_e2m1(const float* r, int64_t n, uint8_t* out, cudaStream_t s) {
+  const int64_t n2 = n / 2;
+  test_cvt_e2m1_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, s>>>(r, n2, out);
+  return cuda_status(cudaGetLastError());
+}
+
+uq_status launch_test_scale_byte(const float* m, int64_t n, uint8_t* out, cudaStream_t s) {
+  test_scale_byte_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(m, n, out);
   return cuda_status(cudaGetLastError());
 }
 

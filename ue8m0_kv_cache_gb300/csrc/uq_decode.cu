@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "uq_device.cuh"
@@ -59,6 +60,12 @@ constexpr int kChunk = 16;  // tokens per work unit (the MMA's m for QK)
 // p * 2^kPShift, so the largest value is 2^(kSlack + kPShift) = 2^15, inside f16.
 constexpr float kSlack = 8.f;
 constexpr float kPShift = 7.f;
+// Pair entries of the workspace hold a block index in their low kCtaBits and
+// the call's epoch above them, so the merge can tell this call's entries from
+// an earlier call's (the workspace is never cleared).
+constexpr int kCtaBits = 12;
+constexpr uint32_t kCtaMask = (1u << kCtaBits) - 1;
+constexpr uint32_t kEpochMask = (1u << (32 - kCtaBits)) - 1;
 
 enum Kind { kFP4 = 0, kFP8 = 1, kBF16 = 2, kTQ4 = 3 };
 // FP4 and TQ4 share the 4-bit packed codes, the per-row side array (scale
@@ -100,7 +107,8 @@ struct DecParams {
   float sl2e;  // softmax scale * log2(e)
   float* ws_o;
   float* ws_ml;
-  int32_t* ws_info;
+  uint32_t* ws_info;  // per pair: (epoch << kCtaBits) | first block, then the same for the last block
+  uint32_t epoch;     // tag of this call's pair entries (kEpochBits wide)
   int64_t* ws_units;
   unsigned int* status;
   uqh::SignMasks sign;
@@ -1036,31 +1044,48 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
     const uint8_t* cp_base = lane == 1 ? p.vc : p.kc;
     const uint32_t cp_off = lane == 1 ? C::KBYTES : 0;
     const uint32_t ring_u32 = smem_u32(myring), bars_u32 = smem_u32(mybars);
+    // FP4 / TQ4 per-lane copy sources and destinations, fixed for the segment:
+    // lane l copies 16-byte chunks l, l + 32, ... of the unit's K and V code
+    // rows and 4-byte word l (< 2 SW) of its two side rows.  Per unit only the
+    // row offset changes: one wide multiply-add per array.
+    constexpr int CW = C::KBYTES / 16;  // 16-byte chunks per array and unit
+    constexpr int SW = C::SBYTES / 4;   // side words per array and unit
+    static_assert(CW % 32 == 0 && (2 * SW) % 32 == 0 || (2 * SW) < 32, "copy split over the lanes");
+    const uint8_t* kc_l = p.kc + 16 * lane;
+    const uint8_t* vc_l = p.vc + 16 * lane;
+    const uint8_t* sd_l = lane < SW ? p.ks + 4 * lane : p.vs + 4 * (lane - SW);
+    const uint32_t dc_l = ring_u32 + 16 * lane, ds_l = ring_u32 + 2 * C::KBYTES + 4 * lane;
+    const uint32_t rowh = static_cast<uint32_t>(kvh) << p.ps_log2;  // (page * Hkv + kvh) * ps = page * Hkv * ps + rowh
+    const uint32_t page_rows = static_cast<uint32_t>(p.Hkv) << p.ps_log2;
     auto issue = [&](int i, int slot, int page) {
       const int tok0 = (ub + j0 + warp + i * kWarps) * kChunk;
-      const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
       const uint32_t bar = bars_u32 + 8u * slot;
-      const uint32_t sbase = ring_u32 + slot * uint32_t(C::STAGE);
       if (packed4(KIND)) {
-        constexpr int CW = C::KBYTES / 16;  // 16-byte chunks per array and unit
-        const uint8_t* gk = p.kc + row0 * C::KROW;
-        const uint8_t* gv = p.vc + row0 * C::KROW;
+        // physical row of the unit's first token; < num_pages * Hkv * ps, checked on the host to fit 32 bits
+        const uint32_t row = static_cast<uint32_t>(page) * page_rows + rowh + (tok0 & ps_mask);
+        const uint8_t* gk = kc_l + static_cast<uint64_t>(row) * C::KROW;
+        const uint8_t* gv = vc_l + static_cast<uint64_t>(row) * C::KROW;
+        const uint32_t dst = dc_l + slot * uint32_t(C::STAGE);
 #pragma unroll
-        for (int j = lane; j < CW; j += 32) {
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + 16 * j), "l"(gk + 16 * j)
+        for (int j = 0; j < CW / 32; ++j) {
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 512 * j), "l"(gk + 512 * j)
                        : "memory");
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + C::KBYTES + 16 * j),
-                       "l"(gv + 16 * j) : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + C::KBYTES + 512 * j),
+                       "l"(gv + 512 * j) : "memory");
         }
-        constexpr int SW = C::SBYTES / 4;  // scale (or norm) words per array and unit
+        const uint8_t* gs = sd_l + static_cast<uint64_t>(row) * C::SROW;
+        const uint32_t ds = ds_l + slot * uint32_t(C::STAGE);
 #pragma unroll
-        for (int w = lane; w < 2 * SW; w += 32) {
-          const uint8_t* g = (w < SW ? p.ks : p.vs) + row0 * C::SROW + 4 * (w < SW ? w : w - SW);
-          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sbase + 2 * C::KBYTES + 4 * w), "l"(g)
-                       : "memory");
+        for (int j = 0; j < (2 * SW) / 32; ++j) {  // head_dim 256: words 32..63 are the V side row
+          const uint8_t* g = j == 0 ? gs : p.vs + static_cast<uint64_t>(row) * C::SROW + 4 * lane;
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(ds + 128 * j), "l"(g) : "memory");
         }
+        if ((2 * SW) % 32 != 0 && lane < (2 * SW) % 32)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(ds), "l"(gs) : "memory");
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
       } else {
+        const int64_t row0 = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (tok0 & ps_mask);
+        const uint32_t sbase = ring_u32 + slot * uint32_t(C::STAGE);
         if (lane == 0)
           asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                        "r"(uint32_t(2 * C::KBYTES)) : "memory");
@@ -1152,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
             pf_next = page_of_lane(nx + 32 + lane);
           }
           const int page = __shfl_sync(kFull, pf, nx & 31);
-          fence_proxy_async();
+          if (!packed4(KIND)) fence_proxy_async();  // the bulk copies are async-proxy writes
           issue(nx, (it + k) % C::NST, page);
         }
       }
@@ -1216,8 +1241,9 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
         p.ws_ml[(slot_id * kHB + h) * 2 + 1] = Ls;
       }
       if (tid == 0) {
-        if (j0 == 0) p.ws_info[2 * pair] = blockIdx.x;
-        if (j0 + seg == nb) p.ws_info[2 * pair + 1] = blockIdx.x;
+        const uint32_t tag = (p.epoch << kCtaBits) | blockIdx.x;
+        if (j0 == 0) p.ws_info[2 * pair] = tag;
+        if (j0 + seg == nb) p.ws_info[2 * pair + 1] = tag;
       }
     }
     __syncthreads();
@@ -1238,7 +1264,8 @@ struct alignas(4 * N) VecF {
 struct MergeParams {
   const float* ws_o;
   const float* ws_ml;
-  const int32_t* ws_info;
+  const uint32_t* ws_info;
+  uint32_t epoch;
   const int64_t* ws_units;
   const int32_t* seq_lens;
   int B, Hq, Hkv, G, nhb, cap, num_ctas;
@@ -1287,9 +1314,12 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
     const int pair = (b * p.Hkv + kvh) * p.nhb + hb;
     int first = 1, last = 0;
     if (dec) {
-      first = p.ws_info[2 * pair];
-      last = p.ws_info[2 * pair + 1];
-      if (first < 0 || last < first || last >= p.num_ctas) {  // never written: a decode block gave up
+      // Entries carry this call's epoch; anything else was left by an earlier
+      // call, i.e. no block of this call wrote the entry (one gave up).
+      const uint32_t e0 = p.ws_info[2 * pair], e1 = p.ws_info[2 * pair + 1];
+      first = static_cast<int>(e0 & kCtaMask);
+      last = static_cast<int>(e1 & kCtaMask);
+      if ((e0 >> kCtaBits) != p.epoch || (e1 >> kCtaBits) != p.epoch || last < first || last >= p.num_ctas) {
         record_error(p.status, kErrTimeout);
         first = 1;
         last = 0;
@@ -1460,7 +1490,7 @@ __global__ void inverse_rotate_kernel(const float* x, int64_t n, float* y, const
 // ------------------------------------------------------------------ host
 size_t ws_slot_bytes(int d) { return static_cast<size_t>(kHB) * (d + 2) * sizeof(float); }
 // Workspace: [256-byte header: unit count][pair info, 2 x int32][per-slot (m, l) x 8 heads][per-slot O x 8 heads]
-size_t ws_info_bytes(int pairs) { return 256 + (((static_cast<size_t>(pairs) * 2 * sizeof(int32_t)) + 255) & ~size_t(255)); }
+size_t ws_info_bytes(int64_t pairs) { return 256 + (((static_cast<size_t>(pairs) * 2 * sizeof(int32_t)) + 255) & ~size_t(255)); }
 
 template <int KIND, int D>
 uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
@@ -1469,6 +1499,9 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   const int G = a.num_q_heads / c.num_kv_heads;
   const int pairs = a.batch * c.num_kv_heads * nhb;
   const size_t smem = C::smem_fixed + (static_cast<size_t>(a.batch) + 1) * sizeof(int);
+  // the FP4 / TQ4 copy path indexes physical rows (page * Hkv + head) * page_size + offset in 32 bits
+  if (packed4(KIND) && static_cast<uint64_t>(c.num_pages) * c.num_kv_heads * c.page_size > 0xFFFFFFFFull)
+    return UQ_ERR_UNSUPPORTED;
   auto kern = decode_kernel<KIND, D>;
   const uqh::DevInfo& di = uqh::dev_info();
   if (smem > di.smem_optin) return UQ_ERR_UNSUPPORTED;
@@ -1507,6 +1540,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   int64_t grid = std::min<int64_t>(static_cast<int64_t>(di.sms) * per_sm, fit);
   grid = std::min<int64_t>(grid, std::max<int64_t>(1, max_units / kMinUnitsPerBlock));
   if (grid < 1) return UQ_ERR_WORKSPACE;
+  grid = std::min<int64_t>(grid, kCtaMask + 1);  // block indices fit the pair entries
   const int64_t slots = grid + pairs;
   DecParams p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -1530,7 +1564,9 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   p.sl2e = sm * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   p.ws_units = reinterpret_cast<int64_t*>(ws);
-  p.ws_info = reinterpret_cast<int32_t*>(ws + 256);
+  p.ws_info = reinterpret_cast<uint32_t*>(ws + 256);
+  static std::atomic<uint32_t> epoch_counter{0};
+  p.epoch = epoch_counter.fetch_add(1, std::memory_order_relaxed) & kEpochMask;
   p.ws_ml = reinterpret_cast<float*>(ws + info);
   p.ws_o = p.ws_ml + slots * kHB * 2;
   p.status = uqh::status_word();
@@ -1564,6 +1600,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   mp.ws_o = p.ws_o;
   mp.ws_ml = p.ws_ml;
   mp.ws_info = p.ws_info;
+  mp.epoch = p.epoch;
   mp.ws_units = p.ws_units;
   mp.seq_lens = a.seq_lens;
   mp.B = a.batch;
@@ -1600,7 +1637,7 @@ int decode_max_ctas() { return dev_info().sms * 8; }
 size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas) {
   const int G = hq / hkv;
   const int nhb = (G + kHB - 1) / kHB;
-  const int pairs = batch * hkv * nhb;
+  const int64_t pairs = static_cast<int64_t>(batch) * hkv * nhb;
   return ws_info_bytes(pairs) + static_cast<size_t>(max_ctas + pairs) * ws_slot_bytes(d);
 }
 

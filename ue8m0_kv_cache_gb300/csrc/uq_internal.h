@@ -86,6 +86,8 @@ uq_status launch_test_rotate(const float* x, int64_t n, int d, uint64_t seed, fl
 uq_status launch_test_quantize(const float* y, int64_t n, int d, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s);
 uq_status launch_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+uq_status launch_test_cvt_e2m1(const float* r, int64_t n, uint8_t* out, cudaStream_t s);
+uq_status launch_test_scale_byte(const float* m, int64_t n, uint8_t* out, cudaStream_t s);
 uq_status launch_calibrate(const void* x, bool in_fp32, int64_t n, int d, uint64_t seed, const float* c_list,
                            int n_c, int mode, double* sse, cudaStream_t s);
 

@@ -11,8 +11,12 @@
 // The scratch is a file-scope __device__ array of kScratchBytes.  Every GPU on
 // which the library is loaded holds it until the process exits.  In host code
 // the array's name does not denote a device address, so the address is looked
-// up once per device with cudaGetSymbolAddress (with that device current) and
-// passed to the kernels.
+// up with cudaGetSymbolAddress (with the device current) and passed to the
+// kernels.  The address is kept per device together with the identity of the
+// context it was read in, and read again when the device's current context
+// is a different one (after cudaDeviceReset, for instance).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "uq_internal.h"
@@ -30,17 +34,50 @@ namespace {
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up on the
-// first call for that device.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (the driver numbers every
+// context it creates), or 0 when it cannot be read.  The two driver entry
+// points are fetched through the runtime once; the library links no driver
+// library of its own.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's current
+// context.  The first call on a device (and the first after the context was
+// replaced) looks it up, which may load the library's device code.
 uq_status scratch_for_current_device(void** ptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return UQ_ERR_CUDA;
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, uq_noalloc_scratch) != cudaSuccess || p == nullptr) return UQ_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx != 0 ? ctx : current_context_id();  // the lookup may have made the context current
   }
   *ptr = g_scratch_ptr[dev];
   return UQ_OK;
@@ -56,6 +93,7 @@ extern "C" uq_status uq_decode_attention_noalloc(const void* q, const uq_cache* 
     return UQ_ERR_INVALID_ARG;
   if (num_q_heads % cache->num_kv_heads != 0) return UQ_ERR_INVALID_ARG;
   if (batch == 0) return UQ_OK;
+  if (batch > 4096) return UQ_ERR_UNSUPPORTED;  // as uq_decode_attention; checked before any size arithmetic
   // The smallest workspace the decode accepts: one block plus one partial per
   // (sequence, kv head, head block).  Shapes that need more than the static
   // scratch holds are rejected here, before anything is enqueued.
