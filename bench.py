@@ -504,8 +504,8 @@ def run_uq(args):
         prefill = {"chunk_tokens_per_seq": PF_CHUNK, "context": L0, "ms": pt * 1e3, "TFLOP_per_s": flops / pt / 1e12,
                    "query_tokens_per_s": T / pt, "tensor_peak_TFLOP_per_s": tens_peak,
                    "frac_of_tensor_peak": flops / pt / 1e12 / tens_peak,
-                   "note": "tcgen05 kind::f16, M 128 x N 64 tiles, S/P/O in tensor memory; "
-                           "P.V runs twice (hi + lo parts of P)"}
+                   "note": "QK^T: tcgen05 kind::mxf8f6f4 block-scaled (E4M3 query x E2M1 keys, UE8M0 key scales "
+                           "in tensor memory), M 128 x N 64 tiles; P.V: tcgen05 kind::f16, twice (hi + lo parts of P)"}
         del qp, wsp_p, outp
     assert uq.uq_check_device_status() == 0
 
@@ -736,7 +736,8 @@ def _prefill_only(args, uq, w, cache, bt, sl, dev):
     peak = _tensor_peak()
     line = {"metric": "chunked-prefill attention TFLOP/s", "value": flops / dt / 1e12, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-            "higher_is_better": True, "dtype": "e2m1/ue8m0 cache, f16 tcgen05 operands", "data": "synthetic",
+            "higher_is_better": True, "dtype": "e2m1/ue8m0 cache; block-scaled e4m3 x e2m1 QK, f16 P.V",
+            "data": "synthetic",
             "config": {"workload": args.workload, "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "chunk": n,
                        "tokens": sum(w.seq_lens)},
             "tensor_peak_TFLOP_per_s": peak, "frac_of_tensor_peak": flops / dt / 1e12 / peak,

@@ -14,20 +14,26 @@
 //     tensor-memory lane -- and one range of keys, in tiles of 64 keys.  The
 //     page rows of a tile's K codes, V codes and both scale rows come by 1-D
 //     bulk copies (TMA engine) into a ring of raw stages.
-//   * The CTA converts each raw tile ONCE into f16 operands in the tensor
-//     cores' 128-byte swizzled layout, shared by all 128 rows: K' = code *
-//     2^(byte - R_key) K-major (R_key the key's largest group byte, so every
-//     value is <= 6 in magnitude and the per-key factor 2^(R_key - 127) goes
-//     on the logit), V' = code * 2^(byte - RV) MN-major (channels contiguous,
-//     RV the CTA's running maximum V byte); exact in f16 except where a V
-//     group lies so far below RV that its values underflow.
-//   * One thread issues S = Q K'^T (tcgen05.mma kind::f16, M 128, N 64) into
-//     tensor memory; every thread reads its row of S, applies the key factors,
-//     the causal mask and the online softmax, and writes P back to tensor
-//     memory as hi and lo f16 parts; one thread issues O_win += P V' with A
-//     from tensor memory.  O_win sums a window of up to sixteen tiles under one
-//     reference (running max, RV) and is then added to the row's fp32 O in
-//     registers with IEEE rounding, as the decode adds its per-unit partials.
+//   * QK^T runs on the block-scaled tensor-core path the pages' kernel uses
+//     (§4.2: the matrix unit consumes the FP4 codes and their UE8M0 scale
+//     bytes directly): tcgen05.mma kind::mxf8f6f4 with A = the E4M3 query rows,
+//     B = the tile's E2M1 K codes, one MMA per 32-channel group, the keys'
+//     scale bytes as the B scale factors in tensor memory (the query's are 1).
+//     The K codes are only repacked (the cache interleaves their words by
+//     group; the operand wants natural order, 16 codes per 16-byte chunk);
+//     no K value is ever widened.
+//   * V' = code * 2^(byte - RV) MN-major (channels contiguous, RV the CTA's
+//     running maximum V byte), converted once per tile for all 128 rows: the
+//     V scale varies along the P.V contraction (keys), so it cannot be a
+//     block scale of that MMA.  Exact in f16 except where a V group lies so
+//     far below RV that its values underflow.
+//   * One thread issues the QK^T MMAs into tensor memory; every thread reads
+//     its row of S, applies the softmax scale, the causal mask and the online
+//     softmax, and writes P back to tensor memory (over S) as hi and lo f16
+//     parts; one thread issues O_win += P V' with A from tensor memory.  O_win
+//     sums a window of up to sixteen tiles under one reference (running max,
+//     RV) and is then added to the row's fp32 O in registers with IEEE
+//     rounding, as the decode adds its per-unit partials.
 //   * Long key ranges are split over CTAs; each (row tile, key split) writes a
 //     partial (m, l, O) and a merge kernel combines them by log-sum-exp and
 //     applies the inverse rotation.
@@ -169,22 +175,26 @@ constexpr int kTRows = 128;     // query rows per CTA
 constexpr int kTKT = kTileKeys; // keys per tile
 constexpr int kTNST = 3;        // raw stages
 constexpr int kTWin = 16;       // tiles per O window
-constexpr int kTCols = 256;     // tensor memory columns: S [0,64), P hi [64,96), P lo [96,128), O_win [128,256)
+// Tensor memory columns: S [0,64) (the tile's P hi [0,32) and P lo [32,64) overwrite
+// it once read), the query scale factors [64,68), the key scale factors [96,98),
+// O_win [128, 128 + D).  Scale-factor columns start on 32-column boundaries.
+constexpr int kTCols = 256;
+constexpr int kSfaCol = 64;
+constexpr int kSfbCol = 96;
 constexpr float kTSlack = 8.f;  // running max raised only when a logit exceeds it by more than this (log2)
 
 template <int D>
 struct TC {
   static constexpr int KROW = D / 2, SROW = D / 32, NG = D / 32;
   static constexpr int RAW = 2 * kTKT * KROW + 2 * kTKT * SROW;
-  static constexpr int QB = kTRows * 2 * D;          // Q, f16, [atom][row][128 B]
-  static constexpr int KB = kTKT * 2 * D;            // K', f16, [atom][key][128 B]
+  static constexpr int QB = kTRows * 128;           // Q, E4M3, [row][128 B] (D = 64 uses half of each row)
+  static constexpr int KB = kTKT * 128;              // K, E2M1 padded (16 codes in 8 of every 16 bytes), [key][128 B]
   static constexpr int VB = kTKT * 2 * D;            // V', f16, MN-major: [atom][key][128 B = 64 channels]
   static constexpr int OFF_Q = 0;                    // operands first: 1024-byte aligned
   static constexpr int OFF_K = OFF_Q + QB;
   static constexpr int OFF_V = OFF_K + KB;
   static constexpr int OFF_RAW = OFF_V + VB;
-  static constexpr int OFF_KS = OFF_RAW + kTNST * RAW;  // fp32 [64] per-key logit factors
-  static constexpr int OFF_BAR = OFF_KS + kTKT * 4;
+  static constexpr int OFF_BAR = OFF_RAW + kTNST * RAW;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers and block state, + slack for the 1024-byte alignment
 };
 
@@ -205,11 +215,30 @@ __device__ __forceinline__ uint64_t tc_desc_mn(uint32_t addr, uint32_t lead) {
 constexpr uint32_t tc_idesc(int n, bool b_mn = false) {
   return (1u << 4) | (b_mn ? 1u << 16 : 0u) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24);
 }
+// kind::mxf8f6f4 block-scaled descriptor: A E4M3 (format 0), B E2M1 (format 5),
+// both K-major, N keys, M 128, UE8M0 scale factors (bit 23); the scale byte of
+// each row and key is byte g of its 32-bit scale-factor word (A and B scale
+// factor ids, bits 29-30 and 4-5), g the 32-channel group the MMA covers.
+constexpr uint32_t tc_idesc_bs(int n, int g) {
+  return (5u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
+         (static_cast<uint32_t>(g) << 29) | (static_cast<uint32_t>(g) << 4);
+}
 
 __device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b),
                "r"(idesc), "r"(acc));
+}
+// D (+)= A B with UE8M0 block scales ([UQ-review] §3.2: the key group scale
+// 2^(byte-127) multiplies its 32-channel partial dot product; the query's
+// scale is 1): A the query rows, B the keys, one 32-channel group per call.
+// Scale factors in tensor memory: the word of row (or key) r = 32 j + i sits in
+// lane i of every 32-lane quarter, column sf + j.
+__device__ __forceinline__ void tc_mma_bs(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
 __device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -280,12 +309,11 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   const uint32_t sb = smem_u32(sm);
   const uint32_t q_u32 = sb + C::OFF_Q, k_u32 = sb + C::OFF_K, v_u32 = sb + C::OFF_V;
   uint8_t* raw = sm + C::OFF_RAW;
-  float* kfac = reinterpret_cast<float*>(sm + C::OFF_KS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);  // [0, kTNST) raw ring, [3] S done, [4] P.V done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 64);
   int* s_vmax = reinterpret_cast<int*>(sm + C::OFF_BAR + 72);   // [2] tile max V byte
   int* s_bad = s_vmax + 2;                                      // [2] tile's first key with a 0xFF group
-  int* s_kr = s_bad + 2;                                        // [64] largest K scale byte of each key
+  float* s_sl2e = reinterpret_cast<float*>(s_bad + 2);          // the softmax scale * log2(e)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -293,6 +321,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     fence_mbar_init();
     s_vmax[0] = s_vmax[1] = 0;
     s_bad[0] = s_bad[1] = 0x7FFFFFFF;
+    *s_sl2e = p.sl2e;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -304,6 +333,12 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   tc_after();
   const uint32_t tmem = *tslot;
   const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
+  {  // query scale factors: every query row's group scale is 1 (byte 127), in all four columns
+    const uint32_t one = 0x7F7F7F7Fu;
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(tmem + lanes + kSfaCol),
+                 "r"(one) : "memory");
+    tmem_wait_st();
+  }
   pdl_wait();
   int64_t total = p.item_pre[p.B];
   const int splits = p.item_pre[p.B + 1], kchunk = p.item_pre[p.B + 2];
@@ -398,18 +433,17 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       fence_proxy_async();
       for (int t = 0; t < (ntiles < kTNST ? ntiles : kTNST); ++t) issue(t, page_of(t));
     }
-    // this thread's query row: rotated E4M3 -> f16, in the swizzled K-major A layout
+    // this thread's query row: the rotated E4M3 bytes, 16 per chunk, in the
+    // swizzled K-major A layout of the block-scaled MMA
     {
       const uint8_t* qsrc = p.qbytes + ((static_cast<int64_t>(q0) + (my_row < nrows ? my_row / p.G : 0)) * p.Hq +
                                         kvh * p.G + (my_row < nrows ? my_row % p.G : 0)) * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) {
-        uint2 w = make_uint2(0u, 0u);
-        if (my_row < nrows) w = *reinterpret_cast<const uint2*>(qsrc + 8 * ch);
-        const uint32_t h0 = e4m3x2_to_f16x2(w.x), h1 = e4m3x2_to_f16x2(w.x >> 16);
-        const uint32_t h2 = e4m3x2_to_f16x2(w.y), h3 = e4m3x2_to_f16x2(w.y >> 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_u32 + sw128_off(kTRows, tid, ch)), "r"(h0),
-                     "r"(h1), "r"(h2), "r"(h3) : "memory");
+      for (int ch = 0; ch < D / 16; ++ch) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (my_row < nrows) w = *reinterpret_cast<const uint4*>(qsrc + 16 * ch);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_u32 + tid * 128 + ((ch ^ (tid & 7)) << 4)),
+                     "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w) : "memory");
       }
     }
 
@@ -438,19 +472,16 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         tc_after();
       }
       ok = ok && mbar_spin(&bars[st], ((git + t) / kTNST) & 1, kWaitBudget);
-      // (b) per key: largest K scale byte, logit factor; the tile's largest V byte and first non-finite key
+      // (b) per key: the tile's largest V byte and first non-finite key
       if (tid < kTKT) {
         const int key = kbase + tid;
-        int kr = 0, vmax = 0, bad = 0;
+        int vmax = 0, bad = 0;
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           const int kb = rks[tid * C::SROW + g], vb = rvs[tid * C::SROW + g];
-          kr = max(kr, kb);
           if (vb != 0xFF) vmax = max(vmax, vb);  // a non-finite group is handled by badpos
           bad |= (kb == 0xFF) | (vb == 0xFF);
         }
-        s_kr[tid] = kr;
-        kfac[tid] = pow2f(kr - 127) * p.sl2e;
         if (key < k_hi) {
           atomicMax(&s_vmax[slot], vmax);
           if (bad) atomicMin(&s_bad[slot], key);
@@ -466,44 +497,59 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         s_vmax[slot ^ 1] = 0;
         s_bad[slot ^ 1] = 0x7FFFFFFF;
       }
-      // (c) K' = code * 2^(byte - R_key) and V' = code * 2^(byte - RVn) (0 past the range), 8 channels
-      // of one key per thread and step; 8 neighbouring threads fill one swizzled 128-byte row
+      // (c) K: the codes as they are, repacked from the cache's group-interleaved
+      // words into the padded 4-bit operand layout (16 codes of natural channel
+      // order in the first 8 bytes of each swizzled 16-byte chunk), and each key's
+      // scale-byte word to tensor memory (key 32 j + i: lane i of every quarter,
+      // column kSfbCol + j); V' = code * 2^(byte - RVn) (0 past the range), 8
+      // channels of one key per thread and step.
+      for (int c = tid; c < kTKT * (D / 16); c += kPThreads) {
+        const int key = c / (D / 16), j = c - key * (D / 16);  // chunk j: natural words 2j, 2j+1
+        const uint32_t* kw = reinterpret_cast<const uint32_t*>(rk + key * C::KROW);
+        const uint32_t w0 = kw[NG * ((2 * j) & 3) + ((2 * j) >> 2)];
+        const uint32_t w1 = kw[NG * ((2 * j + 1) & 3) + ((2 * j + 1) >> 2)];
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %3};" ::"r"(k_u32 + key * 128 + ((j ^ (key & 7)) << 4)),
+                     "r"(w0), "r"(w1), "r"(0u) : "memory");
+      }
+      {
+        uint32_t sf0, sf1;
+        if (NG == 4) {
+          sf0 = *reinterpret_cast<const uint32_t*>(rks + lane * 4);
+          sf1 = *reinterpret_cast<const uint32_t*>(rks + (32 + lane) * 4);
+        } else {
+          sf0 = *reinterpret_cast<const uint16_t*>(rks + lane * 2);
+          sf1 = *reinterpret_cast<const uint16_t*>(rks + (32 + lane) * 2);
+        }
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tmem + lanes + kSfbCol), "r"(sf0),
+                     "r"(sf1) : "memory");
+      }
       for (int wi = tid; wi < kTKT * KW; wi += kPThreads) {
         const int tok = wi / KW, ch = wi - tok * KW;  // 16-byte chunk ch = channels 8 ch .. 8 ch + 7
         const int g = ch >> 2;
         const uint32_t off = sw128_off(kTKT, tok, ch);
-        // K rows are group-interleaved (word w of group g at position NG * w + g), V rows natural
-        const uint32_t kw = reinterpret_cast<const uint32_t*>(rk)[tok * KW + NG * (ch & 3) + g];
         const uint32_t vw = reinterpret_cast<const uint32_t*>(rv)[wi];
         const int vb = rvs[tok * C::SROW + g];
-        const float fk = pow2f(static_cast<int>(rks[tok * C::SROW + g]) - s_kr[tok]);
         const float fv = (kbase + tok < k_hi && vb != 0xFF) ? pow2f(vb - RVn) : 0.f;
-        const uint32_t fk2 = pack_f16x2(fk, fk), fv2 = pack_f16x2(fv, fv);
-        uint32_t hk[4], hv[4];
-        e2m1x8_to_f16x2(kw, hk);
+        const uint32_t fv2 = pack_f16x2(fv, fv);
+        uint32_t hv[4];
         e2m1x8_to_f16x2(vw, hv);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          hk[k] = hmul2(hk[k], fk2);
-          hv[k] = hmul2(hv[k], fv2);
-        }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(k_u32 + off), "r"(hk[0]), "r"(hk[1]),
-                     "r"(hk[2]), "r"(hk[3]) : "memory");
+        for (int k = 0; k < 4; ++k) hv[k] = hmul2(hv[k], fv2);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(v_u32 + off), "r"(hv[0]), "r"(hv[1]),
                      "r"(hv[2]), "r"(hv[3]) : "memory");
       }
+      tmem_wait_st();
       fence_proxy_async();  // generic-proxy operand writes, read next by the tensor cores
       tc_before();
       __syncthreads();
-      // (d) S = Q K'^T into tensor memory columns [0, 64)
+      // (d) S = Q K^T into tensor memory columns [0, 64): one block-scaled MMA per
+      // 32-channel group, E4M3 query x E2M1 codes with the keys' UE8M0 bytes
       if (tid == 0) {
         tc_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t a = tc_desc(q_u32 + (ks >> 2) * (kTRows * 128) + (ks & 3) * 32);
-          const uint64_t bd = tc_desc(k_u32 + (ks >> 2) * (kTKT * 128) + (ks & 3) * 32);
-          tc_mma_ss(tmem, a, bd, tc_idesc(kTKT), ks > 0 ? 1u : 0u);
-        }
+        for (int g = 0; g < NG; ++g)
+          tc_mma_bs(tmem, tc_desc(q_u32 + 32 * g), tc_desc(k_u32 + 32 * g), tc_idesc_bs(kTKT, g), tmem + kSfaCol,
+                    tmem + kSfbCol, g > 0 ? 1u : 0u);
         tc_commit(&bars[kTNST]);
       }
       if (warp == 0 && t + kTNST < ntiles) {  // the raw stage is free again
@@ -526,21 +572,25 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
       }
+      // x stays in the MMA's units; the softmax scale (> 0) is applied to the
+      // maximum and fused into the exponent's argument below
       float mx = -INFINITY;
       if (kbase + kTKT <= k_hi && kbase + kTKT - 1 <= pos_lo && pos >= 0) {  // every key visible to the row
 #pragma unroll
-        for (int k = 0; k < kTKT; ++k) {
-          x[k] *= kfac[k];
-          mx = fmaxf(mx, x[k]);
-        }
+        for (int k = 0; k < kTKT; ++k) mx = fmaxf(mx, x[k]);
       } else {
 #pragma unroll
         for (int k = 0; k < kTKT; ++k) {
           const int key = kbase + k;
-          x[k] = (key <= pos && key < k_hi) ? x[k] * kfac[k] : -INFINITY;
+          x[k] = (key <= pos && key < k_hi) ? x[k] : -INFINITY;
           mx = fmaxf(mx, x[k]);
         }
       }
+      // the scale comes from shared memory once per tile: held in a register
+      // across the whole kernel it costs the compiler spills of O
+      float sl2e;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sl2e) : "r"(smem_u32(s_sl2e)));
+      mx *= sl2e;
       const bool need = mx > m + kTSlack || (m == -INFINITY && mx > -INFINITY);
       const bool fold = __syncthreads_or(need || !ok) != 0 || RVn != RV || win == kTWin;
       if (__syncthreads_or(!ok)) {
@@ -579,15 +629,15 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         uint32_t ph[32], pl[32];
 #pragma unroll
         for (int k = 0; k < kTKT; k += 2) {
-          const float p0 = ex2(x[k] - base), p1 = ex2(x[k + 1] - base);
+          const float p0 = ex2(fmaf(x[k], sl2e, -base)), p1 = ex2(fmaf(x[k + 1], sl2e, -base));
           l += p0 + p1;
           const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
           const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
           ph[k / 2] = pack_f16x2(h0, h1);
           pl[k / 2] = pack_f16x2(p0 - h0, p1 - h1);
         }
-        tmem_st32(tmem + lanes + 64, ph);
-        tmem_st32(tmem + lanes + 96, pl);
+        tmem_st32(tmem + lanes + 0, ph);   // over this row's S, already read
+        tmem_st32(tmem + lanes + 32, pl);
         tmem_wait_st();
       }
       tc_before();
@@ -598,8 +648,8 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < kTKT / 16; ++j) {  // keys 16 j .. 16 j + 15: two 8-key rows of swizzle atoms
           const uint64_t bd = tc_desc_mn(v_u32 + j * 2048, kTKT * 128);
-          tc_mma_ts(tmem + 128, tmem + 64 + 8 * j, bd, tc_idesc(D, true), (win > 0 || j > 0) ? 1u : 0u);
-          tc_mma_ts(tmem + 128, tmem + 96 + 8 * j, bd, tc_idesc(D, true), 1u);
+          tc_mma_ts(tmem + 128, tmem + 8 * j, bd, tc_idesc(D, true), (win > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 128, tmem + 32 + 8 * j, bd, tc_idesc(D, true), 1u);
         }
         tc_commit(&bars[kTNST + 1]);
       }
