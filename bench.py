@@ -857,6 +857,7 @@ def run_layers(args):
 
 
 def main():
+    global REPEAT_S
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
@@ -873,10 +874,13 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="with a workload other than append64k: override B")
     ap.add_argument("--layers", type=int, default=32, help="--kernel layers: attention layers in the stack")
     ap.add_argument("--ctx", type=int, default=32768, help="--kernel layers: context per sequence")
+    ap.add_argument("--repeat-s", type=float, default=REPEAT_S,
+                    help="the K timed steps repeat until the timed region lasts this long (0: once)")
     args = ap.parse_args()
     if args.workload is None:
         args.workload = "prefix128k" if args.kernel == "cascade" else "append64k"
     args.warmup = max(args.warmup, 3)
+    REPEAT_S = max(0.0, args.repeat_s)
     if args.impl == "reference":
         run_reference(args)
     elif args.kernel == "layers":
