@@ -149,3 +149,20 @@ def test_full_size_prefix128k_sampled(B):
     assert st == 0
     seqs = [0, B - 1]
     assert_close(got[seqs], _ref(w, seqs, q), "prefix128k B=%d" % B)
+
+
+def test_full_size_prefix128k_every_row():
+    """The prefix128k workload itself (4 sequences of 131072 tokens sharing 98304) through
+    the shared-prefix kernel (min_rows 0, quarter-full row tiles): every output row against
+    the oracle's fp64 decode of the device's own cache bytes."""
+    from gpu_helpers import oracle_from_device
+    from test_gpu_full_size import _oracle_decode
+    w = workloads.make("prefix128k")
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    q = w.q()
+    got, st = _cascade(w, cache, q, [0, w.B], [w.shared_prefix], w.shared_prefix)
+    assert st == 0
+    ref = _oracle_decode(oracle_from_device(cache), bits(q), w.block_table, np.array(w.seq_lens, np.int32))
+    ma, rl = assert_close(got, ref, "prefix128k every row")
+    print("\nprefix128k cascade, every row: max_abs %.2e rel_l2 %.2e" % (ma, rl))

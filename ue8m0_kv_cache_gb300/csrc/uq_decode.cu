@@ -1431,7 +1431,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
           }
           const unsigned mask = __ballot_sync(kFull, live);
           const int cnt = min(32, p.px_splits - s0);
-          for (int j = 0; j < cnt; ++j) {
+          int j = 0;
+          for (; j + 8 <= cnt; j += 8) {  // eight O rows in flight, summed in split order
+            VecF<EPL> v[8];
+            float wj[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              wj[t] = __shfl_sync(kFull, w, j + t);
+              if ((mask >> (j + t)) & 1u)
+                v[t] = *reinterpret_cast<const VecF<EPL>*>(p.px_o + ((pitem + s0 + j + t) * p.px_rows + prr) * D +
+                                                           lane * EPL);
+              else
+                v[t] = VecF<EPL>{};
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) o[e] += wj[t] * v[t].x[e];
+          }
+          for (; j < cnt; ++j) {
             const float wj = __shfl_sync(kFull, w, j);
             if ((mask >> j) & 1u) {
               const VecF<EPL> v =
