@@ -43,10 +43,12 @@
 
 #include "uq_device.cuh"
 #include "uq_internal.h"
+#include "uq_tc.cuh"
 
 namespace {
 
 using namespace uqd;
+using namespace uqtc;
 
 constexpr int kPThreads = 128;  // 4 warps: one query row per thread
 constexpr int kTileKeys = 64;   // keys per tile; key splits are whole tiles
@@ -198,18 +200,6 @@ struct TC {
   static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers and block state, + slack for the 1024-byte alignment
 };
 
-__device__ __forceinline__ uint64_t tc_desc(uint32_t addr) {
-  // shared-memory matrix descriptor: 128-byte swizzle (layout 2), 8-row groups 1024 B apart, version 1
-  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(16 >> 4) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-// MN-major operand with the 128-byte swizzle: 64 contiguous f16 of the M/N
-// dimension per 128-byte row, 8 K rows per 1024-byte atom; the next 8 K rows
-// 1024 bytes on (stride offset), the next 64 M/N elements `lead` bytes on.
-__device__ __forceinline__ uint64_t tc_desc_mn(uint32_t addr, uint32_t lead) {
-  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lead >> 4) & 0x3FFF) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
 // kind::f16 instruction descriptors: D f32, A and B f16, A K-major, B K-major
 // or (b_mn) MN-major, M 128.
 constexpr uint32_t tc_idesc(int n, bool b_mn = false) {
@@ -222,81 +212,6 @@ constexpr uint32_t tc_idesc(int n, bool b_mn = false) {
 constexpr uint32_t tc_idesc_bs(int n, int g) {
   return (5u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
          (static_cast<uint32_t>(g) << 29) | (static_cast<uint32_t>(g) << 4);
-}
-
-__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b),
-               "r"(idesc), "r"(acc));
-}
-// D (+)= A B with UE8M0 block scales ([UQ-review] §3.2: the key group scale
-// 2^(byte-127) multiplies its 32-channel partial dot product; the query's
-// scale is 1): A the query rows, B the keys, one 32-channel group per call.
-// Scale factors in tensor memory: the word of row (or key) r = 32 j + i sits in
-// lane i of every 32-lane quarter, column sf + j.
-__device__ __forceinline__ void tc_mma_bs(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                          uint32_t sfb, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
-}
-__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d), "r"(a_tmem), "l"(b),
-               "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(addr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Bounded wait on an mbarrier phase by polling try_wait without a suspend
-// hint: the tensor-core completions waited for here take a few hundred cycles,
-// and a suspended thread would be woken later than that.
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long long budget) {
-  const uint32_t a = smem_u32(bar);
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(a), "r"(parity)
-                 : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > budget) return false;
-  }
-}
-
-// Byte offset of 16-byte chunk `ch` (8 f16) of row `row` in a K-major
-// operand of `rows` rows stored as 128-byte swizzled atoms: atom ch / 8 is a
-// [rows][128 B] block; inside it the chunk index is XORed with row & 7.
-__device__ __forceinline__ uint32_t sw128_off(int rows, int row, int ch) {
-  return static_cast<uint32_t>((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
 template <int D>
