@@ -511,26 +511,60 @@ def run_uq(args):
 
     # ---- end to end through the public API with host buffers: the same K steps (same
     # tokens, slots, contexts) with each step's inputs copied from pinned host memory and
-    # its output read back, repeated like the device-timed region
+    # its output read back, repeated like the device-timed region.  Each step's inputs
+    # (q, new K, new V, slots) are one packed pinned buffer and one copy; the copies run
+    # on a second stream into double-buffered device inputs and outputs, so step i+1's
+    # inputs and step i-1's output move while step i decodes.
     n_e2e = min(steps, 200)
-    pin = lambda t: t.cpu().pin_memory()
     idx = list(range(warmup, warmup + n_e2e))
-    hk = [pin(newk[s]) for s in idx]
-    hv = [pin(newv[s]) for s in idx]
-    hs = [pin(news[s]) for s in idx]
-    hq = [pin(qs[s]) for s in idx]
-    hout = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
-    dk, dv, dsl, dq = (torch.empty_like(newk[0]), torch.empty_like(newv[0]), torch.empty_like(news[0]),
-                       torch.empty_like(qs[0]))
+    parts = [qs[0], newk[0], newv[0], news[0]]
+    offs, tot = [], 0
+    for t in parts:
+        offs.append(tot)
+        tot += (t.numel() * t.element_size() + 255) // 256 * 256
+
+    def views(buf):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, parts)]
+
+    hin = []
+    for s_ in idx:
+        hb = torch.empty(tot, dtype=torch.uint8).pin_memory()
+        for v_, src in zip(views(hb), (qs[s_], newk[s_], newv[s_], news[s_])):
+            v_.copy_(src.cpu())
+        hin.append(hb)
+    hout = [torch.empty((B, HQ, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    din = [torch.empty(tot, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dviews = [views(b_) for b_ in din]
+    dout = [torch.empty((B, HQ, D), dtype=torch.float32, device=dev) for _ in range(2)]
+    cstream = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    h2d_done, dec_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def h2d(i):  # inputs of step i into buffer i % 2, once step i - 2 has read it
+        with torch.cuda.stream(cstream):
+            if i >= 2:
+                cstream.wait_event(dec_done[i & 1])
+            din[i & 1].copy_(hin[i], non_blocking=True)
+            h2d_done[i & 1].record(cstream)
 
     def e2e_pass():
-        for i, s in enumerate(idx):
-            dk.copy_(hk[i], non_blocking=True)
-            dv.copy_(hv[i], non_blocking=True)
-            dsl.copy_(hs[i], non_blocking=True)
-            dq.copy_(hq[i], non_blocking=True)
-            uq.uq_decode_attention_append(dq, dk, dv, dsl, fp4, bt, lens[s], out=out, workspace=wsp)
-            hout.copy_(out, non_blocking=True)
+        cstream.wait_stream(stream)  # nothing of the previous pass still reads these buffers
+        h2d(0)
+        for i, s_ in enumerate(idx):
+            k2 = i & 1
+            if i + 1 < len(idx):
+                h2d(i + 1)  # queued ahead of step i's read-back, so it runs while step i decodes
+            stream.wait_event(h2d_done[k2])
+            if i >= 2:
+                stream.wait_event(d2h_done[k2])  # step i-2's output has been read back
+            dq, dk, dv, dsl = dviews[k2]
+            uq.uq_decode_attention_append(dq, dk, dv, dsl, fp4, bt, lens[s_], out=dout[k2], workspace=wsp)
+            dec_done[k2].record(stream)
+            with torch.cuda.stream(cstream):
+                cstream.wait_event(dec_done[k2])
+                hout[k2].copy_(dout[k2], non_blocking=True)
+                d2h_done[k2].record(cstream)
+        stream.wait_event(d2h_done[(len(idx) - 1) & 1])
 
     e2e_pass()
     torch.cuda.synchronize()
@@ -543,10 +577,12 @@ def run_uq(args):
         e2e_rep.append((t0, t1))
     torch.cuda.synchronize()
     e2e_t = _max_over_ranks(float(np.median([a.elapsed_time(b) * 1e-3 for a, b in e2e_rep])), ws, dev)
-    h2d = dk.numel() * 2 + dv.numel() * 2 + dsl.numel() * 8 + dq.numel() * 2
+    h2d = sum(t.numel() * t.element_size() for t in parts)
     e2e = {"value": ws * B * n_e2e / e2e_t, "unit": "decode tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": hout.numel() * 4, "steps": n_e2e, "repeats": len(e2e_rep),
-           "stat": "median repeat"}
+           "d2h_bytes_per_step": hout[0].numel() * 4, "steps": n_e2e, "repeats": len(e2e_rep),
+           "stat": "median repeat",
+           "pipeline": "one packed H2D copy per step and one D2H read on a second stream, double-buffered, "
+                       "overlapping the neighbouring steps' decode"}
     assert uq.uq_check_device_status() == 0
 
     # ---- the mixed-length serving batch (B 64, seq_len ~ U[8192, 65536]), decode only
@@ -633,17 +669,26 @@ def _mixed_decode(uq, dev, stream, steps, warmup, hbm, peak_kind):
     return res
 
 
+def decode_source_sha():
+    """First 16 hex digits of the SHA-256 of the FP4 decode kernel's sources
+    (the kernel file, then the header it shares with the tensor-memory decode)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("uq_decode.cu", "uq_decode_common.cuh"):
+        with open(os.path.join(ROOT, "ue8m0_kv_cache_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _captured_traffic(token_heads):
     """DRAM bytes (read + write) of one FP4 decode launch over `token_heads`
     token-heads, scaled from the ncu capture summarised in
     profiles/decode_fp4_traffic.json.  None when that capture is missing or was
     taken on a different version of the decode source."""
-    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "decode_fp4_traffic.json")) as f:
             prof = json.load(f)
-        with open(os.path.join(ROOT, "ue8m0_kv_cache_gb300", "csrc", "uq_decode.cu"), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        sha = decode_source_sha()
     except (OSError, ValueError):
         return None
     if prof.get("source_sha256_16") != sha:
