@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kTNST + 2; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kTNST; ++s) mbar_init(&bars[s], kPThreads);  // every thread's copies arrive
+    for (int s = kTNST; s < kTNST + 2; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     s_vmax[0] = s_vmax[1] = 0;
     s_bad[0] = s_bad[1] = 0x7FFFFFFF;
@@ -312,42 +313,59 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(p.cascade ? q0 : b) * p.max_pages;
     const int lp_last = (L - 1) >> p.ps_log2;
 
-    // warp 0, one lane per bulk copy of a tile: the page of the lane's copy
-    // (a global load, done one tile ahead), then the copy
+    // The tile's keys come in runs of rows_per consecutive keys, one page each.
+    // Lane r of every warp holds the page of run r of a tile (a global load, made
+    // one tile ahead of its use); every thread then copies its share of the
+    // tile with 16-byte cp.async: K and V code chunks c = tid and tid + 128
+    // (rows c / 4), the scale rows' 16-byte chunks by threads 0-31, and one
+    // no-increment arrival on the stage's barrier, which expects all threads.
+    const int rows_per = min(1 << p.ps_log2, kTKT);
+    const int rp_log2 = p.ps_log2 < 6 ? p.ps_log2 : 6;  // log2(rows_per)
     auto page_of = [&](int t) {
-      const int rows_per = min(1 << p.ps_log2, kTKT);
-      const int key = k_lo + t * kTKT + (lane >> 2) * rows_per;
-      int lp = key >> p.ps_log2;
-      lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
-      int page = (lane < 4 * (kTKT / rows_per)) ? bt_row[lp] : 0;
-      if (page < 0 || page >= p.num_pages) {
-        record_error(p.status, kErrBounds);
-        page = 0;
+      int page = 0;
+      if (lane < kTKT / rows_per) {
+        const int key = k_lo + t * kTKT + lane * rows_per;
+        int lp = key >> p.ps_log2;
+        lp = lp > lp_last ? lp_last : lp;  // keys past the sequence: any page of it (masked)
+        page = bt_row[lp];
       }
       return page;
     };
-    auto issue = [&](int t, int page) {
+    auto issue = [&](int t, int page_lane) {
       const int st = (git + t) % kTNST;
-      uint8_t* base = raw + st * C::RAW;
-      const int rows_per = min(1 << p.ps_log2, kTKT);
-      const int runs = kTKT / rows_per;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::RAW);
-      __syncwarp();
-      if (lane < 4 * runs) {
-        const int run = lane >> 2, what = lane & 3;  // 0 K codes, 1 V codes, 2 K scales, 3 V scales
-        const int key = k_lo + t * kTKT + run * rows_per;
-        const int64_t row = ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (key & ((1 << p.ps_log2) - 1));
-        const int rb = what < 2 ? C::KROW : C::SROW;
-        const uint8_t* src = (what == 0 ? p.kc : what == 1 ? p.vc : what == 2 ? p.ks : p.vs) + row * rb;
-        const int dst = (what < 2 ? what * kTKT * C::KROW : 2 * kTKT * C::KROW + (what - 2) * kTKT * C::SROW) +
-                        run * rows_per * rb;
-        bulk_g2s(base + dst, src, static_cast<uint32_t>(rows_per * rb), &bars[st]);
+      const uint32_t base = smem_u32(raw + st * C::RAW);
+      const int ps_mask = (1 << p.ps_log2) - 1;
+      auto row_of = [&](int r) {  // physical row of key row r of the tile
+        int page = __shfl_sync(kFull, page_lane, r >> rp_log2);
+        if (page < 0 || page >= p.num_pages) {
+          record_error(p.status, kErrBounds);
+          page = 0;
+        }
+        const int key = k_lo + t * kTKT + r;
+        return ((static_cast<int64_t>(page) * p.Hkv + kvh) << p.ps_log2) + (key & ps_mask);
+      };
+      constexpr int CPR = C::KROW / 16;  // 16-byte chunks per code row
+#pragma unroll
+      for (int h = 0; h < (kTKT * CPR) / kPThreads; ++h) {
+        const int c = tid + h * kPThreads, r = c / CPR, cc = c - r * CPR;
+        const int64_t row = row_of(r);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + c * 16),
+                     "l"(p.kc + row * C::KROW + 16 * cc) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + kTKT * C::KROW + c * 16),
+                     "l"(p.vc + row * C::KROW + 16 * cc) : "memory");
       }
+      {  // scale rows: 16-byte chunk q of the tile's K (threads 0..) and V (threads 32..) scale rows
+        constexpr int SCH = kTKT * C::SROW / 16;  // chunks per scale array
+        const int q = tid & 31, is_v = tid >> 5;
+        const int r = q * 16 / C::SROW;  // first key row of the chunk (a chunk never spans runs)
+        const int64_t row = row_of(r < kTKT ? r : 0);
+        if (q < SCH && is_v < 2)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + 2 * kTKT * C::KROW + is_v * (kTKT * C::SROW) + q * 16),
+                       "l"((is_v ? p.vs : p.ks) + row * C::SROW) : "memory");
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[st])) : "memory");
     };
-    if (warp == 0) {
-      fence_proxy_async();
-      for (int t = 0; t < (ntiles < kTNST ? ntiles : kTNST); ++t) issue(t, page_of(t));
-    }
+    for (int t = 0; t < (ntiles < kTNST ? ntiles : kTNST); ++t) issue(t, page_of(t));
     // this thread's query row: the rotated E4M3 bytes, 16 per chunk, in the
     // swizzled K-major A layout of the block-scaled MMA
     {
@@ -370,7 +388,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
 
     for (int t = 0; t < ntiles; ++t) {
       // page of the tile this iteration refills, loaded now so its latency hides behind the tile's work
-      const int nxt_page = (warp == 0 && t + kTNST < ntiles) ? page_of(t + kTNST) : 0;
+      const int nxt_page = t + kTNST < ntiles ? page_of(t + kTNST) : 0;
       const int st = (git + t) % kTNST;
       const uint8_t* rk = raw + st * C::RAW;
       const uint8_t* rv = rk + kTKT * C::KROW;
@@ -418,7 +436,9 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       // scale-byte word to tensor memory (key 32 j + i: lane i of every quarter,
       // column kSfbCol + j); V' = code * 2^(byte - RVn) (0 past the range), 8
       // channels of one key per thread and step.
-      for (int c = tid; c < kTKT * (D / 16); c += kPThreads) {
+#pragma unroll
+      for (int h = 0; h < (kTKT * (D / 16)) / kPThreads; ++h) {
+        const int c = tid + h * kPThreads;
         const int key = c / (D / 16), j = c - key * (D / 16);  // chunk j: natural words 2j, 2j+1
         const uint32_t* kw = reinterpret_cast<const uint32_t*>(rk + key * C::KROW);
         const uint32_t w0 = kw[NG * ((2 * j) & 3) + ((2 * j) >> 2)];
@@ -438,13 +458,18 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tmem + lanes + kSfbCol), "r"(sf0),
                      "r"(sf1) : "memory");
       }
-      for (int wi = tid; wi < kTKT * KW; wi += kPThreads) {
+#pragma unroll 4
+      for (int h = 0; h < (kTKT * KW) / kPThreads; ++h) {
+        const int wi = tid + h * kPThreads;
         const int tok = wi / KW, ch = wi - tok * KW;  // 16-byte chunk ch = channels 8 ch .. 8 ch + 7
         const int g = ch >> 2;
         const uint32_t off = sw128_off(kTKT, tok, ch);
         const uint32_t vw = reinterpret_cast<const uint32_t*>(rv)[wi];
         const int vb = rvs[tok * C::SROW + g];
-        const float fv = (kbase + tok < k_hi && vb != 0xFF) ? pow2f(vb - RVn) : 0.f;
+        // 2^(vb - RVn) <= 1; below 2^-126 it is far under f16's range, so 0 serves
+        const float fv = (kbase + tok < k_hi && vb != 0xFF)
+                             ? __uint_as_float(static_cast<uint32_t>(max(vb - RVn + 127, 0)) << 23)
+                             : 0.f;
         const uint32_t fv2 = pack_f16x2(fv, fv);
         uint32_t hv[4];
         e2m1x8_to_f16x2(vw, hv);
@@ -467,10 +492,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
                     tmem + kSfbCol, g > 0 ? 1u : 0u);
         tc_commit(&bars[kTNST]);
       }
-      if (warp == 0 && t + kTNST < ntiles) {  // the raw stage is free again
-        fence_proxy_async();
-        issue(t + kTNST, nxt_page);
-      }
+      if (t + kTNST < ntiles) issue(t + kTNST, nxt_page);  // the raw stage is free again
       ok = mbar_spin(&bars[kTNST], s_phase & 1, kWaitBudget);
       ++s_phase;
       tc_after();
@@ -609,11 +631,11 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   if (failed) {
     if (tid == 0) {
       record_error(p.status, kErrTimeout);
-      // let copies and MMAs in flight finish before the block's memory goes away
-      for (int s = 0; s < kTNST; ++s) mbar_wait(&bars[s], ((git + s) / kTNST) & 1, kWaitBudget);
+      // let the MMAs in flight finish before the block's memory goes away
       if (pv_pending) mbar_wait(&bars[kTNST + 1], pv_phase & 1, kWaitBudget);
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's copies in flight land first
   tc_before();
   __syncthreads();
   if (warp == 0) {
