@@ -40,6 +40,32 @@ for G, lens, seed in [(8, [3000, 17, 0, 129, 2048 + 5], 501), (4, [700, 1], 502)
     ma, rl = assert_close(got, ref, "tc decode G=%d" % G)
     print("G=%d max_abs %.2e rel_l2 %.2e" % (G, ma, rl))
 
+# page sizes above 16 (a tile's units then share pages) and the shared-prefix path, whose
+# per-sequence part runs through this decode from unit S_g / 16
+for ps, seed in [(32, 505), (128, 506)]:
+    w = workloads.make("gqa8k", B=3, Hkv=2, Hq=16, ps=ps, seq_lens=[2100, 640, 33], seed=seed)
+    cache = new_cache(w)
+    fill_cache(w, [cache])
+    q = w.q()
+    got = uq.uq_decode_attention(q.to(DEV), cache, torch.from_numpy(w.block_table).to(DEV),
+                                 torch.tensor(w.seq_lens, dtype=torch.int32, device=DEV)).cpu().numpy()
+    assert uq.uq_check_device_status() == 0
+    ref = oracle_from_device(cache).decode(bits(q), w.block_table, np.array(w.seq_lens, np.int32))
+    ma, rl = assert_close(got, ref, "tc decode ps=%d" % ps)
+    print("ps=%d max_abs %.2e rel_l2 %.2e" % (ps, ma, rl))
+lens = [4096 + 300, 4096 + 17, 4096 + 1000, 4096 + 64]
+w = workloads.make("gqa8k", B=4, Hkv=2, Hq=64, seq_lens=lens, seed=507, shared_prefix=4096)
+cache = new_cache(w)
+fill_cache(w, [cache])
+q = w.q()
+t32 = lambda x: torch.tensor(x, dtype=torch.int32, device=DEV)
+got = uq.uq_cascade_decode_attention(q.to(DEV), cache, torch.from_numpy(w.block_table).to(DEV), t32(lens),
+                                     t32([0, 4]), t32([4096]), 4096, min_rows=0).cpu().numpy()
+assert uq.uq_check_device_status() == 0
+ref = oracle_from_device(cache).decode(bits(q), w.block_table, np.array(lens, np.int32))
+ma, rl = assert_close(got, ref, "tc decode under the cascade")
+print("cascade max_abs %.2e rel_l2 %.2e" % (ma, rl))
+
 # fused append: the cache bytes equal a separate append, the output the plain decode's
 w = workloads.make("gqa8k", B=3, Hkv=2, Hq=16, seq_lens=[1000, 33, 257], seed=504)
 ca, cb = new_cache(w), new_cache(w)
