@@ -39,7 +39,10 @@
 //     applies the inverse rotation.
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 #include <cmath>
+#include <mutex>
 
 #include "uq_device.cuh"
 #include "uq_internal.h"
@@ -183,7 +186,12 @@ constexpr int kTWin = 16;       // tiles per O window
 constexpr int kTCols = 256;
 constexpr int kSfaCol = 64;
 constexpr int kSfbCol = 96;
-constexpr float kTSlack = 8.f;  // running max raised only when a logit exceeds it by more than this (log2)
+// The running max is raised only when a logit exceeds it by more than this
+// (log2 units).  P = 2^(x - max) then stays below 2^14, inside f16 with the hi
+// part exact.  A raise closes the P.V window for the whole 128-row tile, and
+// the logits' spread (a std of ~7 log2 units with rotated outlier channels)
+// made a slack of 8 close it on most tiles.
+constexpr float kTSlack = 14.f;
 
 template <int D>
 struct TC {
@@ -214,6 +222,47 @@ constexpr uint32_t tc_idesc_bs(int n, int g) {
          (static_cast<uint32_t>(g) << 29) | (static_cast<uint32_t>(g) << 4);
 }
 
+// V' of a 64-key tile, MN-major in the 128-byte swizzled layout (see sw128_off):
+// threads t and t ^ 1 of 128 share key row t / 2, each taking half of its
+// channels, so that each thread scales whole 32-channel groups (one multiplier
+// 2^(byte - RVn) per group, 0 for keys past the range and non-finite groups).
+template <int D>
+__device__ __forceinline__ void convert_v_half_row(const uint8_t* rv, const uint8_t* rvs, int t, bool key_ok,
+                                                   int RVn, uint32_t v_dst) {
+  constexpr int KROW = D / 2, SROW = D / 32, WPT = D / 16;  // code bytes per row, groups per row, words per thread
+  const int key = t >> 1, hh = t & 1;
+  uint32_t words[WPT];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(rv + key * KROW + hh * (KROW / 2));
+#pragma unroll
+    for (int i = 0; i < WPT / 4; ++i) {
+      const uint4 w = src[i];
+      words[4 * i] = w.x;
+      words[4 * i + 1] = w.y;
+      words[4 * i + 2] = w.z;
+      words[4 * i + 3] = w.w;
+    }
+  }
+  uint32_t mult[WPT / 4];
+#pragma unroll
+  for (int q2 = 0; q2 < WPT / 4; ++q2) {  // this thread's groups: hh * WPT / 4 + q2
+    const int vb = rvs[key * SROW + hh * (WPT / 4) + q2];
+    const float fv = (key_ok && vb != 0xFF) ? __uint_as_float(static_cast<uint32_t>(max(vb - RVn + 127, 0)) << 23)
+                                            : 0.f;  // 2^(vb - RVn) <= 1; below 2^-126 far under f16's range
+    mult[q2] = pack_f16x2(fv, fv);
+  }
+#pragma unroll
+  for (int e = 0; e < WPT; ++e) {
+    const int q = hh * WPT + e;  // 16-byte chunk q = channels 8q .. 8q + 7
+    uint32_t hv[4];
+    e2m1x8_to_f16x2(words[e], hv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) hv[k] = hmul2(hv[k], mult[e >> 2]);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(v_dst + sw128_off(kTKT, key, q)), "r"(hv[0]),
+                 "r"(hv[1]), "r"(hv[2]), "r"(hv[3]) : "memory");
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using C = TC<D>;
@@ -226,17 +275,15 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   uint8_t* raw = sm + C::OFF_RAW;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);  // [0, kTNST) raw ring, [3] S done, [4] P.V done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 64);
-  int* s_vmax = reinterpret_cast<int*>(sm + C::OFF_BAR + 72);   // [2] tile max V byte
-  int* s_bad = s_vmax + 2;                                      // [2] tile's first key with a 0xFF group
-  float* s_sl2e = reinterpret_cast<float*>(s_bad + 2);          // the softmax scale * log2(e)
+  int* s_vmax = reinterpret_cast<int*>(sm + C::OFF_BAR + 72);   // [2 tiles][2 warps] tile max V byte
+  int* s_bad = s_vmax + 4;                                      // [2 tiles][2 warps] first key with a 0xFF group
+  float* s_sl2e = reinterpret_cast<float*>(s_bad + 4);          // the softmax scale * log2(e)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int s = 0; s < kTNST; ++s) mbar_init(&bars[s], kPThreads);  // every thread's copies arrive
     for (int s = kTNST; s < kTNST + 2; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
-    s_vmax[0] = s_vmax[1] = 0;
-    s_bad[0] = s_bad[1] = 0x7FFFFFFF;
     *s_sl2e = p.sl2e;
   }
   if (warp == 0) {
@@ -406,7 +453,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       }
       ok = ok && mbar_spin(&bars[st], ((git + t) / kTNST) & 1, kWaitBudget);
       // (b) per key: the tile's largest V byte and first non-finite key
-      if (tid < kTKT) {
+      if (tid < kTKT) {  // warps 0, 1: one key per thread, reduced per warp
         const int key = kbase + tid;
         int vmax = 0, bad = 0;
 #pragma unroll
@@ -415,21 +462,20 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
           if (vb != 0xFF) vmax = max(vmax, vb);  // a non-finite group is handled by badpos
           bad |= (kb == 0xFF) | (vb == 0xFF);
         }
-        if (key < k_hi) {
-          atomicMax(&s_vmax[slot], vmax);
-          if (bad) atomicMin(&s_bad[slot], key);
+        const bool in = key < k_hi;
+        const unsigned wv = __reduce_max_sync(kFull, in ? static_cast<unsigned>(vmax) : 0u);
+        const unsigned wb = __reduce_min_sync(kFull, (in && bad) ? static_cast<unsigned>(key) : 0x7FFFFFFFu);
+        if (lane == 0) {  // this tile's slot, read by every thread below before its next write (tile t + 2)
+          s_vmax[2 * slot + warp] = static_cast<int>(wv);
+          s_bad[2 * slot + warp] = static_cast<int>(wb);
         }
       }
       if (__syncthreads_or(!ok)) {
         failed = true;
         break;
       }
-      const int RVn = max(RV, s_vmax[slot]);
-      badpos = min(badpos, s_bad[slot]);
-      if (tid == 0) {
-        s_vmax[slot ^ 1] = 0;
-        s_bad[slot ^ 1] = 0x7FFFFFFF;
-      }
+      const int RVn = max(RV, max(s_vmax[2 * slot], s_vmax[2 * slot + 1]));
+      badpos = min(badpos, min(s_bad[2 * slot], s_bad[2 * slot + 1]));
       // (c) K: the codes as they are, repacked from the cache's group-interleaved
       // words into the padded 4-bit operand layout (16 codes of natural channel
       // order in the first 8 bytes of each swizzled 16-byte chunk), and each key's
@@ -458,26 +504,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
         asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tmem + lanes + kSfbCol), "r"(sf0),
                      "r"(sf1) : "memory");
       }
-#pragma unroll 4
-      for (int h = 0; h < (kTKT * KW) / kPThreads; ++h) {
-        const int wi = tid + h * kPThreads;
-        const int tok = wi / KW, ch = wi - tok * KW;  // 16-byte chunk ch = channels 8 ch .. 8 ch + 7
-        const int g = ch >> 2;
-        const uint32_t off = sw128_off(kTKT, tok, ch);
-        const uint32_t vw = reinterpret_cast<const uint32_t*>(rv)[wi];
-        const int vb = rvs[tok * C::SROW + g];
-        // 2^(vb - RVn) <= 1; below 2^-126 it is far under f16's range, so 0 serves
-        const float fv = (kbase + tok < k_hi && vb != 0xFF)
-                             ? __uint_as_float(static_cast<uint32_t>(max(vb - RVn + 127, 0)) << 23)
-                             : 0.f;
-        const uint32_t fv2 = pack_f16x2(fv, fv);
-        uint32_t hv[4];
-        e2m1x8_to_f16x2(vw, hv);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) hv[k] = hmul2(hv[k], fv2);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(v_u32 + off), "r"(hv[0]), "r"(hv[1]),
-                     "r"(hv[2]), "r"(hv[3]) : "memory");
-      }
+      convert_v_half_row<D>(rv, rvs, tid, kbase + (tid >> 1) < k_hi, RVn, v_u32);
       tmem_wait_st();
       fence_proxy_async();  // generic-proxy operand writes, read next by the tensor cores
       tc_before();
@@ -642,6 +669,587 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTCols));
   }
+  pdl_trigger();
+}
+
+// ------------------------------------------------------------ warp-specialised variant (head_dim 128)
+// The same items, arithmetic and partials as prefill_tc_kernel, with the
+// tile's phases on separate warps so that they overlap across tiles:
+//   * warp 8 fills a 4-stage raw ring with per-lane 16-byte cp.async (page
+//     numbers one tile ahead);
+//   * warps 4-7 ("convert"): the tile's V statistics, the K codes repacked into
+//     the padded operand, the keys' scale words to tensor memory, V' in f16
+//     (operands double-buffered), and per row (thread = row) the fp32 output
+//     O, kept in tensor memory: each window of P.V sums is folded into O with
+//     IEEE adds when the softmax warps ask for it, and O is written at the
+//     item end;
+//   * warps 0-3 ("softmax", thread = row): the item's query rows, then per
+//     tile the row's logits from tensor memory, the mask, the lazy running
+//     maximum (a window is closed, by the fold above, whenever any row's
+//     maximum or the V reference grows, and every kTWin tiles) and P as hi + lo
+//     f16 parts into tensor memory (S and P double-buffered);
+//   * warp 9 (one thread) issues each tile's QK^T as soon as its operands are
+//     ready, warp 10 (one thread) its P.V as soon as P is (tcgen05.mma holds its
+//     issuing thread for about its execution time, so each MMA stream gets a
+//     warp of its own; the registers are budgeted for 12 warps either way).
+// Tensor memory: S/P [2][64] at 0, O_win at 128, query scale factors at 256,
+// key scale factors [2] at 288 and 320, the folded fp32 output O at 384.
+constexpr int kWThreads = 352;
+constexpr int kWNst = 4;
+constexpr uint32_t kWColO = 128, kWColSfa = 256, kWColSfb = 288, kWColAcc = 384;
+constexpr int kWCols = 512;
+
+struct WS {
+  static constexpr int D = 128, KROW = 64, SROW = 4, NG = 4;
+  static constexpr int RAW = 2 * kTKT * KROW + 2 * kTKT * SROW;  // 8704
+  static constexpr int QB = kTRows * 128;
+  static constexpr int KB = kTKT * 128;
+  static constexpr int VB = kTKT * 2 * D;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;       // [2]
+  static constexpr int OFF_V = OFF_K + 2 * KB;   // [2]
+  static constexpr int OFF_RAW = OFF_V + 2 * VB; // [kWNst]
+  static constexpr int OFF_MISC = OFF_RAW + kWNst * RAW;
+  static constexpr int MISC = 4096;
+  static constexpr int SMEM = OFF_MISC + MISC + 1024;
+};
+// barriers
+enum WBar {
+  kWFull = 0, kWEmpty = kWFull + kWNst, kWKv = kWEmpty + kWNst, kWS = kWKv + 2, kWP = kWS + 2, kWO = kWP + 2,
+  kWFold = kWO + 2, kWQ = kWFold + 2, kWDone = kWQ + 1, kWBarCount = kWDone + 1
+};
+// misc byte offsets
+constexpr int kWMTslot = 256, kWMAbort = 260, kWMSl2e = 264;
+constexpr int kWMVmax = 384;          // [2 tiles][2 warps] int
+constexpr int kWMBad = 400;           // [2 tiles][2 warps] int
+constexpr int kWMRv = 288;            // [2] int: RVn of the tile
+constexpr int kWMFl = 296;            // [2] int: fold flag of the tile
+constexpr int kWMRvf = 304;           // [2] float: O's factor for a grown V reference
+constexpr int kWMGfl = 320;           // [2][4] int
+constexpr int kWMAlpha = 512;         // [2][128] float
+constexpr int kWMMfin = kWMAlpha + 1024;  // [128] float
+constexpr int kWMLfin = kWMMfin + 512;    // [128] float
+static_assert(kWMLfin + 512 <= WS::MISC, "misc");
+
+// the per-item quantities every role needs (as prefill_tc_kernel computes them)
+struct WItem {
+  int b, q0, n, nrows, L, ctx, kvh, row0, pos_lo, k_lo, k_hi, ntiles, lp_last;
+  const int32_t* bt_row;
+};
+__device__ __forceinline__ WItem w_item(const PrefillParams& p, int64_t item, int splits, int kchunk, int cap,
+                                        bool report) {
+  WItem it;
+  int lb = 1, hb = p.B;
+  while (lb < hb) {
+    const int mid = (lb + hb) >> 1;
+    if (p.item_pre[mid] > item) hb = mid; else lb = mid + 1;
+  }
+  const int b = lb - 1;
+  const int q0 = p.cu_q[b], n_plan = max(0, p.cu_q[b + 1] - q0);
+  int L = p.seq_lens[b];
+  int n = n_plan;
+  if (p.cascade) {
+    L = casc_shared_keys(n_plan, p.G, L, p.min_rows, p.casc_cap);
+    if (q0 < 0 || q0 + n > p.T) {
+      if (report) record_error(p.status, kErrBounds);
+      L = 0;
+    }
+  } else if (L < 0 || L > cap || n > L || q0 < 0 || q0 + n > p.T) {
+    if (report) record_error(p.status, kErrBounds);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    n = n > L ? L : n;
+    if (q0 < 0 || q0 + n > p.T) n = 0;
+  }
+  const int ctx = p.cascade ? 0 : L - n;
+  const int tiles_b = row_tiles(n_plan, p.G, kTRows);
+  const int64_t local = item - p.item_pre[b];
+  const int kvh = static_cast<int>(local / (static_cast<int64_t>(tiles_b) * splits));
+  const int rem = static_cast<int>(local - static_cast<int64_t>(kvh) * tiles_b * splits);
+  const int rtile = rem / splits, split = rem - rtile * splits;
+  const int row0 = rtile * kTRows, nrows = n * p.G;
+  const int last_row = min(row0 + kTRows, nrows) - 1;
+  const int pos_max = p.cascade ? L - 1 : ctx + last_row / p.G;
+  it.b = b;
+  it.q0 = q0;
+  it.n = n;
+  it.nrows = nrows;
+  it.L = L;
+  it.ctx = ctx;
+  it.kvh = kvh;
+  it.row0 = row0;
+  it.pos_lo = p.cascade ? L - 1 : ctx + row0 / p.G;
+  it.k_lo = split * kchunk;
+  it.k_hi = min(it.k_lo + kchunk, pos_max + 1);
+  it.ntiles = it.k_lo < it.k_hi ? (it.k_hi - it.k_lo + kTKT - 1) / kTKT : 0;
+  it.lp_last = (L - 1) >> p.ps_log2;
+  it.bt_row = p.block_table + static_cast<int64_t>(p.cascade ? q0 : b) * p.max_pages;
+  return it;
+}
+
+__device__ __forceinline__ void w_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void w_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool w_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok)
+               : "r"(smem_u32(bar)), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+// Bounded wait; once any thread has timed out, every wait returns at once so
+// that all roles run to the end with the same control flow.
+__device__ __forceinline__ void w_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+  if (w_poll(bar, parity)) return;
+  const long long t0 = clock64();
+  while (!*abort_flag) {
+    __nanosleep(32);
+    if (w_poll(bar, parity)) return;
+    if (clock64() - t0 > kWaitBudget) {
+      record_error(status, kErrTimeout);
+      *abort_flag = 1;
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWThreads, 1) prefill_ws_kernel(const __grid_constant__ PrefillParams p) {
+  using C = WS;
+  constexpr int D = C::D, NG = C::NG;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t q_u32 = sb + C::OFF_Q, k_u32 = sb + C::OFF_K, v_u32 = sb + C::OFF_V;
+  uint8_t* raw = sm + C::OFF_RAW;
+  uint8_t* misc = sm + C::OFF_MISC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + kWMTslot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + kWMAbort);
+  float* s_sl2e = reinterpret_cast<float*>(misc + kWMSl2e);
+  int* s_vmax = reinterpret_cast<int*>(misc + kWMVmax);
+  int* s_bad = reinterpret_cast<int*>(misc + kWMBad);
+  int* s_rv = reinterpret_cast<int*>(misc + kWMRv);
+  int* s_fl = reinterpret_cast<int*>(misc + kWMFl);
+  float* s_rvf = reinterpret_cast<float*>(misc + kWMRvf);
+  int* s_gfl = reinterpret_cast<int*>(misc + kWMGfl);
+  float* s_alpha = reinterpret_cast<float*>(misc + kWMAlpha);
+  float* s_mfin = reinterpret_cast<float*>(misc + kWMMfin);
+  float* s_lfin = reinterpret_cast<float*>(misc + kWMLfin);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kWNst; ++s) {
+      mbar_init(&bars[kWFull + s], 32);
+      mbar_init(&bars[kWEmpty + s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kWKv + s], 4);
+      mbar_init(&bars[kWS + s], 1);
+      mbar_init(&bars[kWP + s], 4);
+      mbar_init(&bars[kWO + s], 1);
+      mbar_init(&bars[kWFold + s], 4);
+    }
+    mbar_init(&bars[kWQ], 4);
+    mbar_init(&bars[kWDone], 2);
+    fence_mbar_init();
+    *abort_flag = 0;
+    *s_sl2e = p.sl2e;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "r"(kWCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = *tslot;
+  if (warp < 4) {  // query scale factors: byte 127 (scale 1) for every row and group
+    const uint32_t one = 0x7F7F7F7Fu;
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                     tmem + (static_cast<uint32_t>(warp * 32) << 16) + kWColSfa),
+                 "r"(one) : "memory");
+    tmem_wait_st();
+  }
+  pdl_wait();
+  int64_t total = p.item_pre[p.B];
+  const int splits = p.item_pre[p.B + 1], kchunk = p.item_pre[p.B + 2];
+  if (total > p.max_items || splits < 1 || kchunk < kTKT) {
+    if (blockIdx.x == 0 && tid == 0) record_error(p.status, kErrBounds);
+    total = 0;
+  }
+  const int cap = p.max_pages << p.ps_log2;
+  tc_before();
+  __syncthreads();
+  tc_after();
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ copy warp
+    const int rows_per = min(1 << p.ps_log2, kTKT);
+    const int rp_log2 = p.ps_log2 < 6 ? p.ps_log2 : 6;
+    const int ps_mask = (1 << p.ps_log2) - 1;
+    uint32_t g = 0;  // tiles issued so far
+    for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
+      const WItem it = w_item(p, item, splits, kchunk, cap, false);
+      if (it.ntiles == 0) continue;
+      auto page_of = [&](int t) {  // lane r: the page of run r of tile t
+        int page = 0;
+        if (lane < kTKT / rows_per && t < it.ntiles) {
+          int lp = (it.k_lo + t * kTKT + lane * rows_per) >> p.ps_log2;
+          lp = lp > it.lp_last ? it.lp_last : lp;
+          page = it.bt_row[lp];
+        }
+        return page;
+      };
+      int pg = page_of(0);
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
+        const int pg_next = page_of(t + 1);
+        const int st = static_cast<int>(g % kWNst);
+        if (g >= kWNst) w_wait(&bars[kWEmpty + st], ((g - kWNst) / kWNst) & 1, abort_flag, p.status);
+        const uint32_t base = smem_u32(raw + st * C::RAW);
+        auto row_of = [&](int r) {
+          int page = __shfl_sync(kFull, pg, r >> rp_log2);
+          if (page < 0 || page >= p.num_pages) {
+            record_error(p.status, kErrBounds);
+            page = 0;
+          }
+          const int key = it.k_lo + t * kTKT + r;
+          return ((static_cast<int64_t>(page) * p.Hkv + it.kvh) << p.ps_log2) + (key & ps_mask);
+        };
+#pragma unroll
+        for (int h = 0; h < (kTKT * 4) / 32; ++h) {  // code chunks: 4 per 64-byte row
+          const int c = lane + 32 * h, r = c >> 2, cc = c & 3;
+          const int64_t row = row_of(r);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + c * 16),
+                       "l"(p.kc + row * C::KROW + 16 * cc) : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + kTKT * C::KROW + c * 16),
+                       "l"(p.vc + row * C::KROW + 16 * cc) : "memory");
+        }
+        {  // scale rows: lanes 0-15 the K chunks, 16-31 the V chunks (4 keys each)
+          const int q = lane & 15, is_v = lane >> 4;
+          const int64_t row = row_of(q * 4);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + 2 * kTKT * C::KROW + is_v * (kTKT * C::SROW) + q * 16),
+                       "l"((is_v ? p.vs : p.ks) + row * C::SROW) : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[kWFull + st])) : "memory");
+        pg = pg_next;
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ QK^T thread
+    if (lane == 0) {
+      // QK^T(g) once tile g's operands are written (which the convert warps do
+      // only after P.V(g - 2) completed, so the S buffer it overwrites is free)
+      // and, at an item's first tile, the item's query rows are staged
+      uint32_t g = 0, items_q = 0;
+      for (int64_t item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
+        const WItem it = w_item(p, item, splits, kchunk, cap, false);
+        if (it.ntiles == 0) continue;
+        w_wait(&bars[kWQ], items_q & 1, abort_flag, p.status);
+        ++items_q;
+        for (int t = 0; t < it.ntiles; ++t, ++g) {
+          w_wait(&bars[kWKv + (g & 1)], (g >> 1) & 1, abort_flag, p.status);
+          tc_after();
+          const uint32_t kt = k_u32 + (g & 1) * C::KB;
+#pragma unroll
+          for (int gg = 0; gg < NG; ++gg)
+            tc_mma_bs(tmem + 64u * (g & 1), tc_desc(q_u32 + 32 * gg), tc_desc(kt + 32 * gg), tc_idesc_bs(kTKT, gg),
+                      tmem + kWColSfa, tmem + kWColSfb + 32u * (g & 1), gg > 0 ? 1u : 0u);
+          tc_commit(&bars[kWS + (g & 1)]);
+        }
+      }
+      tc_commit(&bars[kWDone]);
+      w_wait(&bars[kWDone], 0, abort_flag, p.status);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ P.V thread
+    if (lane == 0) {
+      // P.V(g) once P(g) is written and, when it opens a window, the closing
+      // window has been folded
+      uint32_t g = 0;
+      uint32_t fcnt[2] = {0u, 0u};  // folds waited for, per tile parity
+      for (int64_t item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
+        const WItem it = w_item(p, item, splits, kchunk, cap, false);
+        for (int t = 0; t < it.ntiles; ++t, ++g) {
+          w_wait(&bars[kWP + (g & 1)], (g >> 1) & 1, abort_flag, p.status);
+          const int fl = *reinterpret_cast<volatile int*>(&s_fl[g & 1]);
+          if (fl) {
+            w_wait(&bars[kWFold + (g & 1)], fcnt[g & 1] & 1, abort_flag, p.status);
+            ++fcnt[g & 1];
+          }
+          tc_after();
+          const uint32_t vt = v_u32 + (g & 1) * C::VB;
+          const uint32_t pcol = tmem + 64u * (g & 1);
+#pragma unroll
+          for (int j = 0; j < kTKT / 16; ++j) {
+            const uint64_t bd = tc_desc_mn(vt + j * 2048, kTKT * 128);
+            tc_mma_ts(tmem + kWColO, pcol + 8 * j, bd, tc_idesc(D, true), (!fl || j > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + kWColO, pcol + 32 + 8 * j, bd, tc_idesc(D, true), 1u);
+          }
+          tc_commit(&bars[kWO + (g & 1)]);
+        }
+      }
+      tc_commit(&bars[kWDone]);
+      w_wait(&bars[kWDone], 0, abort_flag, p.status);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax warps (thread = row)
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t g = 0, items_done = 0;
+    for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
+      const WItem it = w_item(p, item, splits, kchunk, cap, tid == 0);
+      const int my_row = it.row0 + tid;
+      const int pos = my_row < it.nrows ? (p.cascade ? it.L - 1 : it.ctx + my_row / p.G) : -1;
+      if (it.ntiles == 0) {
+        p.ws_ml[item * (kTRows * 2) + 2 * tid] = -INFINITY;
+        p.ws_ml[item * (kTRows * 2) + 2 * tid + 1] = 0.f;
+        continue;
+      }
+      {  // this row's rotated E4M3 query bytes, swizzled K-major A operand
+        const uint8_t* qsrc = p.qbytes + ((static_cast<int64_t>(it.q0) + (my_row < it.nrows ? my_row / p.G : 0)) * p.Hq +
+                                          it.kvh * p.G + (my_row < it.nrows ? my_row % p.G : 0)) * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 16; ++ch) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (my_row < it.nrows) w = *reinterpret_cast<const uint4*>(qsrc + 16 * ch);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_u32 + tid * 128 + ((ch ^ (tid & 7)) << 4)),
+                       "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w) : "memory");
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) w_arrive(&bars[kWQ]);
+      }
+      float m = -INFINITY, l = 0.f;
+      int RV = 0, win = 0;
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
+        const int kbase = it.k_lo + t * kTKT;
+        w_wait(&bars[kWS + (g & 1)], (g >> 1) & 1, abort_flag, p.status);
+        tc_after();
+        float x[kTKT];
+        {
+          uint32_t r32[32];
+          tmem_ld32(tmem + lanes + 64u * (g & 1), r32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r32[k]);
+          tmem_ld32(tmem + lanes + 64u * (g & 1) + 32, r32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
+        }
+        float mx = -INFINITY;
+        if (kbase + kTKT <= it.k_hi && kbase + kTKT - 1 <= it.pos_lo && pos >= 0) {
+#pragma unroll
+          for (int k = 0; k < kTKT; ++k) mx = fmaxf(mx, x[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kTKT; ++k) {
+            const int key = kbase + k;
+            x[k] = (key <= pos && key < it.k_hi) ? x[k] : -INFINITY;
+            mx = fmaxf(mx, x[k]);
+          }
+        }
+        float sl2e;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sl2e) : "r"(smem_u32(s_sl2e)));
+        mx *= sl2e;
+        const bool need = mx > m + kTSlack || (m == -INFINITY && mx > -INFINITY);
+        const int rvn = *reinterpret_cast<volatile int*>(&s_rv[g & 1]);
+        const unsigned vote = __ballot_sync(kFull, need);
+        if (lane == 0) s_gfl[(g & 1) * 4 + warp] = vote != 0u;
+        w_bar(1, 128);
+        const int* gf = s_gfl + (g & 1) * 4;
+        const bool fold = t == 0 || (gf[0] | gf[1] | gf[2] | gf[3]) || rvn != RV || win == kTWin;
+        if (fold) {
+          float a = 1.f;
+          if (need) {
+            const float mn = fmaxf(m, mx);
+            a = m == -INFINITY ? 0.f : ex2(m - mn);
+            l *= a;
+            m = mn;
+          }
+          s_alpha[(g & 1) * kTRows + tid] = a;
+          if (tid == 0) {
+            s_fl[g & 1] = 1;
+            s_rvf[g & 1] = t == 0 ? 1.f : pow2f(RV - rvn);
+          }
+          RV = rvn;
+          win = 0;
+        } else if (tid == 0) {
+          s_fl[g & 1] = 0;
+        }
+        ++win;
+        {
+          const float base = m == -INFINITY ? 0.f : m;
+          uint32_t ph[32], pl[32];
+#pragma unroll
+          for (int k = 0; k < kTKT; k += 2) {
+            const float p0 = ex2(fmaf(x[k], sl2e, -base)), p1 = ex2(fmaf(x[k + 1], sl2e, -base));
+            l += p0 + p1;
+            const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+            const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+            ph[k / 2] = pack_f16x2(h0, h1);
+            pl[k / 2] = pack_f16x2(p0 - h0, p1 - h1);
+          }
+          tmem_st32(tmem + lanes + 64u * (g & 1), ph);
+          tmem_st32(tmem + lanes + 64u * (g & 1) + 32, pl);
+          tmem_wait_st();
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0) w_arrive(&bars[kWP + (g & 1)]);
+      }
+      s_mfin[tid] = m;
+      s_lfin[tid] = l;
+      w_bar(3, 256);  // the convert warps write the item's partials
+      w_bar(4, 256);  // and have read these rows before the next item reuses them
+      ++items_done;
+    }
+  } else {
+    // ------------------------------------------------------------ convert warps (thread ct = row)
+    const int ct = tid - 128, cw = warp - 4;
+    const uint32_t lanes = static_cast<uint32_t>(cw * 32) << 16;
+    uint32_t g = 0;
+    for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
+      const WItem it = w_item(p, item, splits, kchunk, cap, false);
+      if (it.ntiles == 0) continue;
+      const int my_row = it.row0 + ct;
+      const int pos = my_row < it.nrows ? (p.cascade ? it.L - 1 : it.ctx + my_row / p.G) : -1;
+      int RV = 0, badpos = 0x7FFFFFFF;
+      bool ovalid = false;  // O (tensor memory, columns kWColAcc..) holds a folded window of this item
+      // fold of tile gt (local t_local): wait for its P (the flag), then, if it
+      // opens a window, add the closing window into O and rescale
+      auto fold_check = [&](uint32_t gt, int t_local) {
+        w_wait(&bars[kWP + (gt & 1)], (gt >> 1) & 1, abort_flag, p.status);
+        if (!*reinterpret_cast<volatile int*>(&s_fl[gt & 1])) return;
+        if (t_local > 0) {  // the window P.V(gt - 1) closed
+          w_wait(&bars[kWO + ((gt - 1) & 1)], ((gt - 1) >> 1) & 1, abort_flag, p.status);
+          tc_after();
+          const float f = s_alpha[(gt & 1) * kTRows + ct] * s_rvf[gt & 1];
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t w32[32], o32[32];
+            tmem_ld32(tmem + lanes + kWColO + c0, w32);
+            if (ovalid) tmem_ld32(tmem + lanes + kWColAcc + c0, o32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float o = ovalid ? __uint_as_float(o32[k]) + __uint_as_float(w32[k]) : __uint_as_float(w32[k]);
+              o32[k] = __float_as_uint(o * f);
+            }
+            tmem_st32(tmem + lanes + kWColAcc + c0, o32);
+          }
+          tmem_wait_st();
+          ovalid = true;
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0) w_arrive(&bars[kWFold + (gt & 1)]);
+      };
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
+        const int st = static_cast<int>(g % kWNst);
+        const uint8_t* rk = raw + st * C::RAW;
+        const uint8_t* rv = rk + kTKT * C::KROW;
+        const uint8_t* rks = rv + kTKT * C::KROW;
+        const uint8_t* rvs = rks + kTKT * C::SROW;
+        const int kbase = it.k_lo + t * kTKT;
+        const int slot = g & 1;
+        w_wait(&bars[kWFull + st], (g / kWNst) & 1, abort_flag, p.status);
+        if (ct < kTKT) {  // per key (convert warps 0, 1): the largest V byte and the first non-finite key
+          const int key = kbase + ct;
+          int vmax = 0, bad = 0;
+#pragma unroll
+          for (int gg = 0; gg < NG; ++gg) {
+            const int kb = rks[ct * C::SROW + gg], vb = rvs[ct * C::SROW + gg];
+            if (vb != 0xFF) vmax = max(vmax, vb);
+            bad |= (kb == 0xFF) | (vb == 0xFF);
+          }
+          const bool in = key < it.k_hi;
+          const unsigned wv = __reduce_max_sync(kFull, in ? static_cast<unsigned>(vmax) : 0u);
+          const unsigned wb = __reduce_min_sync(kFull, (in && bad) ? static_cast<unsigned>(key) : 0x7FFFFFFFu);
+          if (lane == 0) {  // this tile's slot, read below by every convert thread before the next write (tile g + 2)
+            s_vmax[2 * slot + cw] = static_cast<int>(wv);
+            s_bad[2 * slot + cw] = static_cast<int>(wb);
+          }
+        }
+        w_bar(2, 128);
+        const int RVn = max(RV, max(s_vmax[2 * slot], s_vmax[2 * slot + 1]));
+        badpos = min(badpos, min(s_bad[2 * slot], s_bad[2 * slot + 1]));
+        if (ct == 0) s_rv[slot] = RVn;
+        RV = RVn;
+        // the operand buffers of this slot were last read by tile g - 2's MMAs
+        if (g >= 2) w_wait(&bars[kWO + slot], ((g - 2) >> 1) & 1, abort_flag, p.status);
+        tc_after();
+        const uint32_t kt_u32 = k_u32 + slot * C::KB, vt_u32 = v_u32 + slot * C::VB;
+#pragma unroll
+        for (int h = 0; h < (kTKT * (D / 16)) / 128; ++h) {
+          const int c = ct + h * 128;
+          const int key = c / (D / 16), j = c - key * (D / 16);
+          const uint32_t* kw = reinterpret_cast<const uint32_t*>(rk + key * C::KROW);
+          const uint32_t w0 = kw[NG * ((2 * j) & 3) + ((2 * j) >> 2)];
+          const uint32_t w1 = kw[NG * ((2 * j + 1) & 3) + ((2 * j + 1) >> 2)];
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %3};" ::"r"(kt_u32 + key * 128 + ((j ^ (key & 7)) << 4)),
+                       "r"(w0), "r"(w1), "r"(0u) : "memory");
+        }
+        {
+          const uint32_t sf0 = *reinterpret_cast<const uint32_t*>(rks + lane * 4);
+          const uint32_t sf1 = *reinterpret_cast<const uint32_t*>(rks + (32 + lane) * 4);
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(
+                           tmem + lanes + kWColSfb + 32u * slot),
+                       "r"(sf0), "r"(sf1) : "memory");
+        }
+        convert_v_half_row<D>(rv, rvs, ct, kbase + (ct >> 1) < it.k_hi, RVn, vt_u32);
+        tmem_wait_st();
+        fence_proxy_async();
+        tc_before();
+        __syncwarp();
+        if (lane == 0) {
+          w_arrive(&bars[kWKv + slot]);
+          w_arrive(&bars[kWEmpty + st]);
+        }
+        if (t >= 1) fold_check(g - 1, t - 1);
+      }
+      // the item's last tile: its fold, then the last window into O
+      const uint32_t gl = g - 1;
+      fold_check(gl, it.ntiles - 1);
+      w_wait(&bars[kWO + (gl & 1)], (gl >> 1) & 1, abort_flag, p.status);
+      tc_after();
+      w_bar(3, 256);  // the softmax warps' (m, l) of this item are in shared memory
+      const float osc = pow2f(RV - 127);  // V' was code * 2^(byte - RV)
+      float* ml_out = p.ws_ml + item * (kTRows * 2);
+      float* o_out = p.ws_o + item * (static_cast<int64_t>(kTRows) * D);
+      const bool live = !*abort_flag;
+      if (live) {
+        ml_out[2 * ct] = s_mfin[ct];
+        ml_out[2 * ct + 1] = pos >= badpos ? __int_as_float(0x7FC00000) : s_lfin[ct];
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {  // O + the last window, scaled, to the item's partial
+        uint32_t w32[32], o32[32];
+        tmem_ld32(tmem + lanes + kWColO + c0, w32);
+        if (ovalid) tmem_ld32(tmem + lanes + kWColAcc + c0, o32);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              v[e] = (ovalid ? __uint_as_float(o32[k + e]) + __uint_as_float(w32[k + e]) : __uint_as_float(w32[k + e])) * osc;
+            *reinterpret_cast<float4*>(o_out + static_cast<int64_t>(ct) * D + c0 + k) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+        }
+      }
+      tc_before();
+      w_bar(4, 256);
+    }
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kWCols));
   pdl_trigger();
 }
 
@@ -862,9 +1470,34 @@ PrefillParams base_params(const uq_cache& c, const int32_t* block_table, int max
 }
 
 // CTAs of the item kernel's grid (0 on failure).
+// The warp-specialised kernel (head_dim 128) is selected with UQ_PREFILL=ws,
+// read once per process.
+bool prefill_ws_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("UQ_PREFILL");
+    return e != nullptr && std::strcmp(e, "ws") == 0;
+  }();
+  return on;
+}
+
+// One CTA per SM; the dynamic shared-memory attribute once per device.
+int prefill_ws_ctas_per_sm() {
+  static std::mutex cfg_mu;
+  static bool done[uqh::kMaxDevices];
+  const uqh::DevInfo& di = uqh::dev_info();
+  if (di.device < 0) return 0;
+  std::lock_guard<std::mutex> lk(cfg_mu);
+  if (!done[di.device]) {
+    if (cudaFuncSetAttribute(prefill_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WS::SMEM) != cudaSuccess)
+      return 0;
+    done[di.device] = true;
+  }
+  return 1;
+}
+
 template <int D>
 int item_grid(const PrefillPlan& pl) {
-  const int per_sm = prefill_ctas_per_sm<D>();
+  const int per_sm = (D == 128 && prefill_ws_enabled()) ? prefill_ws_ctas_per_sm() : prefill_ctas_per_sm<D>();
   if (per_sm < 1) return 0;
   return static_cast<int>(std::max<int64_t>(
       1, std::min<int64_t>(pl.max_items, static_cast<int64_t>(uqh::dev_info().sms) * per_sm)));
@@ -872,6 +1505,9 @@ int item_grid(const PrefillPlan& pl) {
 
 template <int D>
 uq_status launch_items(const PrefillParams& p, int grid, cudaStream_t s) {
+  if (D == 128 && prefill_ws_enabled())
+    return uqh::cuda_status(
+        uqh::launch_pdl(prefill_ws_kernel, static_cast<unsigned>(grid), kWThreads, WS::SMEM, s, p));
   return uqh::cuda_status(
       uqh::launch_pdl(prefill_tc_kernel<D>, static_cast<unsigned>(grid), kPThreads, TC<D>::SMEM, s, p));
 }
