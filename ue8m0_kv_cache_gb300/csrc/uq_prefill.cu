@@ -1469,16 +1469,18 @@ PrefillParams base_params(const uq_cache& c, const int32_t* block_table, int max
   return p;
 }
 
-// CTAs of the item kernel's grid (0 on failure).
-// The warp-specialised kernel (head_dim 128) is selected with UQ_PREFILL=ws,
-// read once per process.
+// Head_dim 128 runs the warp-specialised kernel unless UQ_PREFILL=tc selects
+// the single-role one (read once per process); head_dim 64 always runs the
+// single-role kernel.
 bool prefill_ws_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("UQ_PREFILL");
-    return e != nullptr && std::strcmp(e, "ws") == 0;
+    return !(e != nullptr && std::strcmp(e, "tc") == 0);
   }();
   return on;
 }
+
+// CTAs of the item kernel's grid (0 on failure).
 
 // One CTA per SM; the dynamic shared-memory attribute once per device.
 int prefill_ws_ctas_per_sm() {
@@ -1495,6 +1497,7 @@ int prefill_ws_ctas_per_sm() {
   return 1;
 }
 
+// CTAs of the item kernel's grid (0 on failure).
 template <int D>
 int item_grid(const PrefillPlan& pl) {
   const int per_sm = (D == 128 && prefill_ws_enabled()) ? prefill_ws_ctas_per_sm() : prefill_ctas_per_sm<D>();
