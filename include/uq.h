@@ -435,6 +435,21 @@ uq_status uq_test_cvt_e2m1(const float* r, int64_t n, uint8_t* codes, cudaStream
  * 0, 254); 0 for m = 0; 0xFF for a NaN or infinite m. */
 uq_status uq_test_scale_byte(const float* m, int64_t n, uint8_t* bytes, cudaStream_t stream);
 
+/* Injected decode timeout: the device-side failure path, exercised without a
+ * GPU fault.  Arms the next decode launch that runs the warp-level decode
+ * kernel (uq_decode_attention, _append, _noalloc and the cascade's decode, any
+ * cache dtype; not the opt-in tensor-memory FP4 decode, which ignores it):
+ * warp 0 of block `cta` also waits, at its first unit, on a shared-memory
+ * barrier that nothing arrives at, for at most budget_cycles SM clock cycles
+ * (plus at most one hardware suspend interval of the wait instruction).  The
+ * wait runs out; the kernel records UQ_ERR_DEVICE_TIMEOUT in the device status
+ * word, waits (bounded) for that warp's copies in flight and ends the block's
+ * work.  That call's output is undefined and the next uq_check_device_status
+ * returns UQ_ERR_DEVICE_TIMEOUT; later calls are unaffected (one launch only).
+ * If block `cta` or its warp 0 has no units, nothing happens.  Host-only:
+ * returns UQ_ERR_INVALID_ARG for cta < 0 or budget_cycles < 0, else UQ_OK. */
+uq_status uq_test_arm_decode_timeout(int32_t cta, int64_t budget_cycles);
+
 #ifdef __cplusplus
 }
 #endif

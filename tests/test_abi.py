@@ -162,3 +162,10 @@ def test_calibration_and_constant_argument_validation_without_a_device():
     assert _append(s) == E["UQ_ERR_INVALID_ARG"]
     s.fp4_c = float("nan")
     assert _decode(s) == E["UQ_ERR_INVALID_ARG"]
+
+
+def test_timeout_hook_rejects_negative_arguments_on_the_host():
+    # only invalid arguments here: a valid call would arm the next decode launch of this process
+    for cta, budget in ((-1, 1000), (0, -1)):
+        with pytest.raises(uq.UqError):
+            uq.uq_test_arm_decode_timeout(cta, budget)

@@ -70,6 +70,7 @@ _sig = {
     "uq_test_cvt_e4m3": (C.c_int, [_vp, _i64, _vp, _vp]),
     "uq_test_cvt_e2m1": (C.c_int, [_vp, _i64, _vp, _vp]),
     "uq_test_scale_byte": (C.c_int, [_vp, _i64, _vp, _vp]),
+    "uq_test_arm_decode_timeout": (C.c_int, [_i32, _i64]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -384,6 +385,12 @@ def uq_test_scale_byte(m: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty(m.shape, dtype=torch.uint8, device=m.device)
     _check(_lib.uq_test_scale_byte(_ptr(m), m.numel(), _ptr(out), _stream(stream)), "uq_test_scale_byte")
     return out
+
+
+def uq_test_arm_decode_timeout(cta: int, budget_cycles: int) -> None:
+    """Arm an injected timeout in the next warp-level decode launch (see uq.h):
+    that call then ends with UQ_ERR_DEVICE_TIMEOUT in the device status word."""
+    _check(_lib.uq_test_arm_decode_timeout(int(cta), int(budget_cycles)), "uq_test_arm_decode_timeout")
 
 
 def uq_test_cvt_e4m3(x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -393,4 +393,10 @@ uq_status uq_test_cvt_e4m3(const float* x, int64_t n, uint8_t* out, cudaStream_t
   return uqh::launch_test_cvt_e4m3(x, n, out, stream);
 }
 
+uq_status uq_test_arm_decode_timeout(int32_t cta, int64_t budget_cycles) {
+  if (cta < 0 || budget_cycles < 0) return UQ_ERR_INVALID_ARG;
+  uqh::arm_decode_stall(cta, static_cast<long long>(budget_cycles));
+  return UQ_OK;
+}
+
 }  // extern "C"

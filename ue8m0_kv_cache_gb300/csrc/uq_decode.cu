@@ -42,6 +42,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <cmath>
 
 #include "uq_decode_common.cuh"
@@ -705,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
   float* comb_o = comb_ml + kWarps * kHB * 2;
   int* pre = reinterpret_cast<int*>(comb_o + kWarps * kHB * D);
   __shared__ int abort_flag;
+  __shared__ uint64_t stall_bar;  // injected timeout: nothing ever arrives at it
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, c = lane & 3;
   const int ps_mask = (1 << p.ps_log2) - 1;
@@ -741,8 +743,13 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
     for (int s = 0; s < C::NST; ++s) mbar_init(&mybars[s], packed4(KIND) ? 32 : 1);  // see the copy issue
     fence_mbar_init();
   }
-  if (tid == 0) abort_flag = 0;
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&stall_bar, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
+  bool stall = p.stall_cta == static_cast<int>(blockIdx.x) && warp == 0;  // warp-uniform
 
   const int pps = p.Hkv * p.nhb;  // (kv head, head block) pairs per sequence
   const int64_t U = static_cast<int64_t>(pre[p.B]) * pps;
@@ -936,6 +943,10 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? (packed4(KIND) ? 2 : 1) :
       const int nu = (packed4(KIND) && i + 1 < nw) ? 2 : 1;  // warp-uniform
       bool ok = mbar_wait(&mybars[it % C::NST], (it / C::NST) & 1, kWaitBudget);
       if (nu == 2) ok = ok && mbar_wait(&mybars[(it + 1) % C::NST], ((it + 1) / C::NST) & 1, kWaitBudget);
+      if (stall) {  // injected timeout (test hook): a bounded wait that runs out
+        ok = ok && mbar_wait(&stall_bar, 0, p.stall_budget);
+        stall = false;
+      }
       if (!__all_sync(kFull, ok)) {
         if (lane == 0) {
           record_error(p.status, kErrTimeout);
@@ -1377,6 +1388,7 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
   grid = std::min<int64_t>(grid, kCtaMask + 1);  // block indices fit the pair entries
   const int64_t slots = grid + pairs;
   DecParams p;
+  uqh::take_decode_stall(&p.stall_cta, &p.stall_budget);
   p.q = static_cast<const uint16_t*>(a.q);
   p.kc = static_cast<const uint8_t*>(c.k_codes);
   p.ks = static_cast<const uint8_t*>(c.k_scales);
@@ -1477,6 +1489,25 @@ uq_status run_decode(const uqh::DecodeArgs& a, int nhb, cudaStream_t s) {
 }  // namespace
 
 namespace uqh {
+
+namespace {
+std::mutex stall_mu;
+int stall_cta = -1;
+long long stall_budget = 0;
+}  // namespace
+
+void arm_decode_stall(int cta, long long budget) {
+  std::lock_guard<std::mutex> lk(stall_mu);
+  stall_cta = cta;
+  stall_budget = budget;
+}
+
+void take_decode_stall(int* cta, long long* budget) {
+  std::lock_guard<std::mutex> lk(stall_mu);
+  *cta = stall_cta;
+  *budget = stall_budget;
+  stall_cta = -1;
+}
 
 int decode_max_ctas() { return dev_info().sms * 8; }
 

@@ -91,6 +91,11 @@ struct DecParams {
   const int32_t* casc_cu;
   const int32_t* casc_prefix;
   int casc_groups, casc_min_rows, casc_cap;
+  // Injected timeout (test hook; stall_cta < 0: none): warp 0 of block
+  // stall_cta also waits, at its first unit, on a barrier that nothing
+  // arrives at, for at most stall_budget cycles, and so takes the timeout path.
+  int stall_cta;
+  long long stall_budget;
 };
 
 // Contiguous range [lo, hi) of the U units that block c of C handles.

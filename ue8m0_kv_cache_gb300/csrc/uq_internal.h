@@ -136,6 +136,11 @@ struct DecodeArgs {
 size_t decode_workspace_bytes(int batch, int hq, int hkv, int d, int max_ctas);
 int decode_max_ctas();
 uq_status launch_decode(const DecodeArgs& a, cudaStream_t s);
+// Injected decode timeout (test hook): arm makes the next decode launch's
+// block `cta` stall (warp 0, at most budget cycles); take hands the armed
+// values to that launch and disarms (cta -1: nothing armed).
+void arm_decode_stall(int cta, long long budget);
+void take_decode_stall(int* cta, long long* budget);
 uq_status launch_query_fp8(const void* q, int64_t n, int d, uint64_t seed, uint8_t* out,
                                 cudaStream_t s);
 
