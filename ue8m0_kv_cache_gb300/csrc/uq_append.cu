@@ -240,8 +240,12 @@ __global__ void __launch_bounds__(kAppendThreads)
     // the stage of the previous iteration is free again: it takes the tile NS - 1 ahead
     const int64_t ahead = tile + static_cast<int64_t>(NS - 1) * gridDim.x;
     if (tid == 0 && ahead < ntiles) issue(ahead, (it + NS - 1) % NS);
-    const bool ok = mbar_wait(&bars[stage], (it / NS) & 1, kWaitBudget);
     const int64_t R = tile * kRows + row;
+    // the row's token and its slot, read before the stage wait so that the
+    // global load's latency passes during the wait and the rotation
+    const int64_t t = R < nrows ? R / p.hkv : 0;
+    const int64_t slot = R < nrows ? __ldg(p.slots + t) : -1;
+    const bool ok = mbar_wait(&bars[stage], (it / NS) & 1, kWaitBudget);
     if (!ok) {
       record_error(p.status, kErrTimeout);
       abort_flag = 1;
@@ -265,9 +269,7 @@ __global__ void __launch_bounds__(kAppendThreads)
         }
       }
       rotate_regs<D>(u);
-      const int64_t t = R / p.hkv;
       const int h = static_cast<int>(R - t * p.hkv);
-      const int64_t slot = p.slots[t];
       if (slot >= p.num_slots) {
         record_error(p.status, kErrBounds);
       } else if (slot >= 0) {
