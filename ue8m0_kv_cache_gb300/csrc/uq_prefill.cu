@@ -525,16 +525,16 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
       tc_after();
       // (e) this thread's row: logits, mask, online softmax, P to tensor memory
       float x[kTKT];
-      {
-        uint32_t r32[32];
-        tmem_ld32(tmem + lanes + 0, r32);
+      {  // both halves of the row's logits in flight, one wait
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tmem + lanes + 0, ra);
+        tmem_ld32(tmem + lanes + 32, rb);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r32[k]);
-        tmem_ld32(tmem + lanes + 32, r32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
+        for (int k = 0; k < 32; ++k) {
+          x[k] = __uint_as_float(ra[k]);
+          x[32 + k] = __uint_as_float(rb[k]);
+        }
       }
       // x stays in the MMA's units; the softmax scale (> 0) is applied to the
       // maximum and fused into the exponent's argument below
@@ -1029,16 +1029,16 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_ws_kernel(const __grid_c
         w_wait(&bars[kWS + (g & 1)], (g >> 1) & 1, abort_flag, p.status);
         tc_after();
         float x[kTKT];
-        {
-          uint32_t r32[32];
-          tmem_ld32(tmem + lanes + 64u * (g & 1), r32);
+        {  // both halves of the row's logits in flight, one wait
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tmem + lanes + 64u * (g & 1), ra);
+          tmem_ld32(tmem + lanes + 64u * (g & 1) + 32, rb);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r32[k]);
-          tmem_ld32(tmem + lanes + 64u * (g & 1) + 32, r32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(r32[k]);
+          for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(ra[k]);
+            x[32 + k] = __uint_as_float(rb[k]);
+          }
         }
         float mx = -INFINITY;
         if (kbase + kTKT <= it.k_hi && kbase + kTKT - 1 <= it.pos_lo && pos >= 0) {
