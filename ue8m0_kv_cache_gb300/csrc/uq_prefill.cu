@@ -9,11 +9,11 @@
 // the output is rotated back.
 //
 // GB300 design (many query rows per key: a dense contraction, unlike decode)
-//   * A CTA of 4 warps takes 128 query rows of one (sequence, kv head) --
-//     consecutive (token, head) pairs of the chunk, one row per thread and per
-//     tensor-memory lane -- and one range of keys, in tiles of 64 keys.  The
-//     page rows of a tile's K codes, V codes and both scale rows come by 1-D
-//     bulk copies (TMA engine) into a ring of raw stages.
+//   * A work item is 128 query rows of one (sequence, kv head) -- consecutive
+//     (token, head) pairs of the chunk, one row per tensor-memory lane -- and
+//     one range of keys, in tiles of 64 keys.  The page rows of a tile's K
+//     codes, V codes and both scale rows are copied by 16-byte cp.async into a
+//     ring of raw stages.
 //   * QK^T runs on the block-scaled tensor-core path the pages' kernel uses
 //     (§4.2: the matrix unit consumes the FP4 codes and their UE8M0 scale
 //     bytes directly): tcgen05.mma kind::mxf8f6f4 with A = the E4M3 query rows,
@@ -22,21 +22,26 @@
 //     The K codes are only repacked (the cache interleaves their words by
 //     group; the operand wants natural order, 16 codes per 16-byte chunk);
 //     no K value is ever widened.
-//   * V' = code * 2^(byte - RV) MN-major (channels contiguous, RV the CTA's
+//   * V' = code * 2^(byte - RV) MN-major (channels contiguous, RV the item's
 //     running maximum V byte), converted once per tile for all 128 rows: the
 //     V scale varies along the P.V contraction (keys), so it cannot be a
 //     block scale of that MMA.  Exact in f16 except where a V group lies so
 //     far below RV that its values underflow.
-//   * One thread issues the QK^T MMAs into tensor memory; every thread reads
-//     its row of S, applies the softmax scale, the causal mask and the online
-//     softmax, and writes P back to tensor memory (over S) as hi and lo f16
-//     parts; one thread issues O_win += P V' with A from tensor memory.  O_win
-//     sums a window of up to sixteen tiles under one reference (running max,
-//     RV) and is then added to the row's fp32 O in registers with IEEE
+//   * Each row's logits are read from tensor memory, masked (causal), and go
+//     through the online softmax (lazy running maximum); P goes back over S
+//     as hi and lo f16 parts, and O_win += P V' runs with A from tensor
+//     memory.  O_win sums a window of up to sixteen tiles under one reference
+//     (running max, RV) and is then added to the row's fp32 O with IEEE
 //     rounding, as the decode adds its per-unit partials.
-//   * Long key ranges are split over CTAs; each (row tile, key split) writes a
-//     partial (m, l, O) and a merge kernel combines them by log-sum-exp and
-//     applies the inverse rotation.
+//   * Two kernels do this.  prefill_ws_kernel (head_dim 128, the default)
+//     gives each stage warps of its own -- copy, V statistics and operand
+//     conversion, softmax, and one thread each issuing QK^T and P.V -- with O
+//     in tensor memory and S/P and the operands double-buffered, one CTA per
+//     SM.  prefill_tc_kernel (head_dim 64, or UQ_PREFILL=tc) runs every stage
+//     in the same 4 warps, O in registers, two CTAs per SM.
+//   * Long key ranges are split over work items; each (row tile, key split)
+//     writes a partial (m, l, O) and a merge kernel combines them by
+//     log-sum-exp and applies the inverse rotation.
 #include <algorithm>
 #include <climits>
 #include <cstdlib>
