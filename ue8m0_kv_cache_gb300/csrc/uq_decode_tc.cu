@@ -749,7 +749,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       }
     }
     tc_commit(&bars[kBarDone]);
-    tc_wait(&bars[kBarDone], 0, abort_flag, p.status);
+    // the MMAs in flight finish before the tensor memory is freed, after an
+    // abort too (bounded, whatever the abort flag says)
+    if (!mbar_wait_sleep(&bars[kBarDone], 0, kWaitBudget)) record_error(p.status, kErrTimeout);
   }
   tc_before();
   __syncthreads();

@@ -967,7 +967,9 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_ws_kernel(const __grid_c
         }
       }
       tc_commit(&bars[kWDone]);
-      w_wait(&bars[kWDone], 0, abort_flag, p.status);
+      // this thread's MMAs in flight finish before the tensor memory is freed,
+      // after an abort too (bounded, whatever the abort flag says)
+      if (!mbar_wait_sleep(&bars[kWDone], 0, kWaitBudget)) record_error(p.status, kErrTimeout);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ P.V thread
@@ -998,7 +1000,9 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_ws_kernel(const __grid_c
         }
       }
       tc_commit(&bars[kWDone]);
-      w_wait(&bars[kWDone], 0, abort_flag, p.status);
+      // this thread's MMAs in flight finish before the tensor memory is freed,
+      // after an abort too (bounded, whatever the abort flag says)
+      if (!mbar_wait_sleep(&bars[kWDone], 0, kWaitBudget)) record_error(p.status, kErrTimeout);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ softmax warps (thread = row)

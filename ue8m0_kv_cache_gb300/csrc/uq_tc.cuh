@@ -92,6 +92,25 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long l
   }
 }
 
+// Bounded wait that sleeps between polls, for waits that are off the critical
+// path (the final wait for a thread's own MMAs before tensor memory is freed,
+// taken whatever an abort flag says).  Returns false if the budget ran out.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long budget) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(a), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > budget) return false;
+    __nanosleep(64);
+  }
+}
+
 // Byte offset of 16-byte chunk `ch` (8 f16) of row `row` in a K-major
 // operand of `rows` rows stored as 128-byte swizzled atoms: atom ch / 8 is a
 // [rows][128 B] block; inside it the chunk index is XORed with row & 7.
