@@ -40,3 +40,37 @@ def test_injected_decode_timeout_is_reported_and_the_next_call_is_clean(dtype):
         assert uq.uq_check_device_status() == 0
         assert torch.equal(again, ref), "cta %d" % cta
 
+
+
+def test_injected_timeout_in_the_fused_step_then_the_same_step_clean():
+    """The bench's step (fused append + decode): after a timed-out call, running the
+    same step again leaves the cache and the output exactly as one clean call does
+    (the timed-out call may or may not have written each new token: same bytes)."""
+    dev = torch.device("cuda")
+    lens = [3000, 2048, 4096, 1500]
+    w = workloads.make("gqa8k", B=4, Hkv=8, Hq=64, seq_lens=lens, seed=92)
+    clean, hit = new_cache(w, fill=0), new_cache(w, fill=0)
+    for b in range(w.B):
+        k, v = w.kv(b, 0, lens[b] - 1, device=dev)
+        sl_b = torch.from_numpy(w.slots(b, 0, lens[b] - 1)).to(dev)
+        for c in (clean, hit):
+            uq.uq_quantize_append(k, v, sl_b, c)
+    g = torch.Generator(device=dev)
+    g.manual_seed(93)
+    k_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.tensor([int(w.block_table[b, (L - 1) // w.ps]) * w.ps + (L - 1) % w.ps for b, L in enumerate(lens)],
+                         dtype=torch.int64, device=dev)
+    q = w.q().to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ref = uq.uq_decode_attention_append(q, k_new, v_new, slots, clean, bt, sl)
+    assert uq.uq_check_device_status() == 0
+    uq.uq_test_arm_decode_timeout(0, BUDGET)
+    uq.uq_decode_attention_append(q, k_new, v_new, slots, hit, bt, sl)  # its output is undefined
+    assert uq.uq_check_device_status() == UQ_ERR_DEVICE_TIMEOUT
+    again = uq.uq_decode_attention_append(q, k_new, v_new, slots, hit, bt, sl)
+    assert uq.uq_check_device_status() == 0
+    for name in ("k_codes", "k_scales", "v_codes", "v_scales"):
+        assert torch.equal(getattr(clean, name), getattr(hit, name)), name
+    assert torch.equal(again, ref)
